@@ -1,0 +1,77 @@
+"""The pins catch planted mistakes.
+
+Each case copies the oracle's C source, plants one plausible mistake (a
+dropped term, a wrong sign, a wrong index, a transposed operand, a wrong tie
+rule), compiles the copy on the CPU and runs the pin suite against it.  The
+suite must fail for every one.
+"""
+import concurrent.futures as fut
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "rmsnorm drops eps": ("ss / (double)d + eps", "ss / (double)d"),
+    "rmsnorm sum instead of mean": ("sqrt(ss / (double)d + eps)", "sqrt(ss + eps)"),
+    "router tie picks higher index": ("if (best < 0 || z[e] > z[best]) best = e;",
+                                      "if (best < 0 || z[e] >= z[best]) best = e;"),
+    "softmax drops normaliser": ("p[e] = exp(z[e] - zmax) / sum;", "p[e] = exp(z[e] - zmax);"),
+    "router ignores bias": ("z[e] = acc + (bias ? (double)bias[e] : 0.0);", "z[e] = acc;"),
+    "router weight transposed": ("oracle_bf16_value(W[(size_t)e * d + i])",
+                                 "oracle_bf16_value(W[(size_t)i * E + e])"),
+    "silu sign": ("double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
+    "swiglu product not rounded": ("a[j] = q_bf16(silu * u);", "a[j] = silu * u;"),
+    "gate and up swapped": ("double silu = g / (1.0 + exp(-g));\n    a[j] = q_bf16(silu * u);",
+                            "double silu = u / (1.0 + exp(-u));\n    a[j] = q_bf16(silu * g);"),
+    "down projection transposed": ("Wd[(size_t)m * I + j]", "Wd[(size_t)j * d + m]"),
+    "shared experts dropped": ("for (int s = 0; s < S; ++s) {", "for (int s = 0; s < 0; ++s) {"),
+    "shared weight not one": ("for (int m = 0; m < d; ++m) acc[m] += y[m];",
+                              "for (int m = 0; m < d; ++m) acc[m] += 0.5 * y[m];"),
+    "residual dropped": ("for (int m = 0; m < d; ++m) h[m] += acc[m];",
+                         "for (int m = 0; m < d; ++m) h[m] = acc[m];"),
+    "routed weights renormalised": ("psel[j] = p[force_sel[j]];\n    }\n  }",
+                                    "psel[j] = p[force_sel[j]];\n    }\n  }\n"
+                                    "  { double t = 0; for (int j = 0; j < k; ++j) t += psel[j];"
+                                    " for (int j = 0; j < k; ++j) psel[j] /= t; }"),
+    "argmax tie picks higher id": ("    if (acc > best) {\n      second = best;",
+                                   "    if (acc >= best) {\n      second = best;"),
+    "embedding row off by one": ("h[i] = oracle_bf16_value(w->embed[(size_t)x * d + i]);",
+                                 "h[i] = oracle_bf16_value(w->embed[(size_t)((x + 1) % c->vocab) * d + i]);"),
+    "drafts misaligned": ("draft_ids[(size_t)b * K + (i - 1)]", "draft_ids[(size_t)b * K + (K - i)]"),
+    "accept commits one token too few": ("for (int i = 0; i <= n; ++i) out[i] = y[i];",
+                                         "for (int i = 0; i < n; ++i) out[i] = y[i];"),
+    "accept keeps later matches": ("while (n < K && d[n] == y[n]) ++n;",
+                                   "for (int i = 0; i < K; ++i) n += (d[i] == y[i]);"),
+    "bf16 ties away from zero": ("double r = nearbyint(q);", "double r = round(q);"),
+}
+
+
+def _run_mutant(name, old, new, tmp):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name!r} must occur exactly once"
+    tag = "".join(c if c.isalnum() else "_" for c in name)
+    c_path = os.path.join(tmp, f"{tag}.c")
+    so_path = os.path.join(tmp, f"{tag}.so")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-fvisibility=hidden", "-o", so_path, c_path, "-lm"])
+    env = dict(os.environ, MOE_ORACLE_LIB=so_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode
+
+
+def test_every_planted_mistake_fails_a_pin():
+    with tempfile.TemporaryDirectory() as tmp:
+        with fut.ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+            results = list(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp), MUTANTS.items()))
+    survivors = [n for n, rc in results if rc == 0]
+    assert not survivors, f"pins did not catch: {survivors}"
