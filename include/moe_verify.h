@@ -1,0 +1,213 @@
+/*
+ * moe_verify.h - C ABI of the GB300 (sm_103a) MoE greedy-verify library.
+ *
+ * The library runs the batched greedy verification step of a FastMTP-style
+ * speculative decoder over a DeepSeek-3B-MoE-style target stack, and the
+ * acceptance rule that follows it.
+ *
+ *   Architecture: "Jina AI Releases jina-ocr-v1, a 3.4B MoE Document Parser
+ *   With Built-In Speculative Decoding", architecture paragraph (12 decoder
+ *   layers, 64 routed experts, two shared experts, top-6 routing).
+ *   Verification and acceptance: the same article, FastMTP paragraph (the
+ *   decoder checks K drafts greedily, keeps the longest prefix equal to its
+ *   own choices and commits one more token of its own, K+1 tokens when all
+ *   drafts match), and "Jina-OCR-v1: Efficient Document Parsing with
+ *   Speculative Decoding and Dense Verifiable Rewards", Abstract (greedy
+ *   verification makes decoding lossless).
+ *
+ * Per verify token x the step computes
+ *   h = E[x]
+ *   for each layer l:  xhat = bf16(RMSNorm(h) * g_l)
+ *                      z = xhat W_r^T (+ b);  p = softmax(z);  S = top-k of z
+ *                      a_e = bf16(silu(xhat W_g,e^T) * (xhat W_u,e^T))
+ *                      h += sum_{e in S} p_e a_e W_d,e^T + sum_shared a_s W_d,s^T
+ *   target = argmax_v bf16(RMSNorm(h) * g_f) . W_lm[v]   (lowest v on ties)
+ * The target stack has no attention on this path, so a verify token's target
+ * depends on that token alone.
+ *
+ * Conventions
+ *   - Every pointer argument is device memory unless its comment says host.
+ *     The caller owns all of it; the library never frees caller memory.
+ *   - bf16 tensors are passed as raw 16-bit patterns (void*), PyTorch Linear
+ *     layout [out_features, in_features], row-major, contiguous.
+ *   - Calls that take a cuda_stream (a cudaStream_t, NULL = legacy default
+ *     stream) only enqueue work on it and return without synchronising,
+ *     except where noted.  moe_verify_step, moe_verify_accept and
+ *     moe_verify_layer allocate nothing, do no host-device copies and may be
+ *     captured into a CUDA graph.
+ *   - Argument errors are found on the host and returned at once; nothing is
+ *     enqueued then.  Errors found on the device (an id outside [0, V), a
+ *     bounded wait that ran out) set a sticky flag in the context; the next
+ *     moe_verify_sync_status reports and clears it.  No device code traps.
+ *   - A context is not thread safe: calls on one context must not overlap on
+ *     the host, and work enqueued on different streams for one context must
+ *     not overlap on the device (it shares one workspace).
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_VERIFY_API __attribute__((visibility("default")))
+#else
+#define MOE_VERIFY_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_verify_ctx moe_verify_ctx; /* opaque */
+
+typedef enum {
+  MOE_VERIFY_OK = 0,
+  MOE_VERIFY_ERR_ARG = -1,         /* bad argument (NULL, size out of range) */
+  MOE_VERIFY_ERR_CUDA = -2,        /* a CUDA runtime or driver call failed */
+  MOE_VERIFY_ERR_OOM = -3,         /* device memory allocation failed */
+  MOE_VERIFY_ERR_ID_RANGE = -4,    /* a token id was outside [0, vocab) */
+  MOE_VERIFY_ERR_TIMEOUT = -5,     /* a bounded device wait ran out */
+  MOE_VERIFY_ERR_UNSUPPORTED = -6  /* shape or device this build does not run */
+} moe_verify_status;
+
+/* Shape of the target stack and the workspace bounds. */
+typedef struct {
+  int32_t n_layers;     /* L >= 1 (the decoder: 12) */
+  int32_t hidden;       /* d: multiple of 64, <= 8192 (1280) */
+  int32_t n_experts;    /* E routed experts: 1..256 (64) */
+  int32_t top_k;        /* k: 1..min(E, 16) (6) */
+  int32_t n_shared;     /* S shared experts, weight 1: 0..8 (2) */
+  int32_t expert_inter; /* I of a routed expert: 1..8192 (896) */
+  int32_t shared_inter; /* I of a shared expert: 1..8192 (896) */
+  int32_t vocab;        /* V: 2..2^30 (129280) */
+  float rms_eps;        /* RMSNorm epsilon (1e-6) */
+  int32_t max_batch;    /* largest B a step may be given, >= 1 */
+  int32_t max_k;        /* largest K (drafts per sequence), 0..15 */
+} moe_verify_config;
+
+/* Weights, all device pointers of bf16 patterns unless noted.  The per-layer
+ * members are HOST arrays of n_layers device pointers. */
+typedef struct {
+  const void* embed;                /* [V, d] token embedding */
+  const void* final_norm;           /* [d] gain of the final RMSNorm */
+  const void* lm_head;              /* [V, d] */
+  const void* const* norm;          /* L x [d] gain of the pre-MoE RMSNorm */
+  const void* const* router;        /* L x [E, d] */
+  const float* const* router_bias;  /* L x [E] fp32 added to router logits, or NULL */
+  const void* const* w_gate;        /* L x [E, I, d] */
+  const void* const* w_up;          /* L x [E, I, d] */
+  const void* const* w_down;        /* L x [E, d, I] */
+  const void* const* s_gate;        /* L x [S, Is, d]  (NULL when S == 0) */
+  const void* const* s_up;          /* L x [S, Is, d] */
+  const void* const* s_down;        /* L x [S, d, Is] */
+} moe_verify_weights;
+
+/* Optional device outputs for tests and diagnostics (caller-owned; any member
+ * may be NULL; pass NULL for the whole struct in timed runs).  T = B*(K+1)
+ * verify tokens in sequence-major order. */
+typedef struct {
+  int32_t* topk_idx; /* [L, T, k] selected experts, in selection order */
+  float* topk_w;     /* [L, T, k] their softmax weights */
+  float* hidden;     /* [L+1, T, d] residual stream entering layer l (l = L: after the last) */
+  float* logits;     /* [T, V] lm_head logits (step only) */
+} moe_verify_probe;
+
+/* Initialise a context: validates the config, allocates the library-owned
+ * weights and workspace (sized for max_batch and max_k), copies and repacks
+ * the weights into them (the caller may free its weights afterwards) and
+ * prepares the TMA descriptors.  Synchronous: returns after the copies on
+ * cuda_stream are complete.  Needs a device of compute capability 10.3
+ * (sm_103a); other devices give MOE_VERIFY_ERR_UNSUPPORTED.  On error *out is
+ * NULL and nothing stays allocated. */
+MOE_VERIFY_API int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* weights,
+                    void* cuda_stream, moe_verify_ctx** out);
+
+/* Greedy verification of B sequences with K drafts each (the FastMTP
+ * paragraph's verify step).  Sequence b's verify tokens are
+ *   x_b = [context_ids[b], draft_ids[b*K + 0], ..., draft_ids[b*K + K-1]]
+ * and target_ids[b*(K+1) + i] receives the target stack's greedy choice for
+ * the token that follows x_b[i].
+ *   context_ids  [B] int32: each sequence's last committed token
+ *   draft_ids    [B, K] int32 (may be NULL when K == 0)
+ *   target_ids   [B, K+1] int32, written
+ *   probe        NULL or diagnostics (see moe_verify_probe)
+ * 1 <= B <= max_batch, 0 <= K <= max_k.  A verify token outside [0, V) sets
+ * the sticky MOE_VERIFY_ERR_ID_RANGE flag and its target is -1. */
+MOE_VERIFY_API int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
+                    int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
+                    void* cuda_stream);
+
+/* The acceptance rule (FastMTP paragraph): for each sequence,
+ *   n = the length of the longest prefix with draft_ids[b,i] == target_ids[b,i]
+ *   committed[b, 0..n] = target_ids[b, 0..n], committed[b, n+1..K] = -1
+ *   accept_len[b] = n  (accepted drafts; n+1 tokens are committed)
+ * A sequence with a draft or target id outside [0, V) gets accept_len -1 and
+ * a row of -1, and sets the sticky MOE_VERIFY_ERR_ID_RANGE flag.
+ *   draft_ids [B, K] int32 (may be NULL when K == 0), target_ids [B, K+1]
+ *   int32, committed [B, K+1] int32 written, accept_len [B] int32 written.
+ * 1 <= B, 0 <= K <= 15 (B is not bounded by max_batch). */
+MOE_VERIFY_API int moe_verify_accept(moe_verify_ctx* ctx, const int32_t* draft_ids, const int32_t* target_ids,
+                      int32_t B, int32_t K, int32_t* committed, int32_t* accept_len,
+                      void* cuda_stream);
+
+/* One decoder block on T tokens with bf16 input and output:
+ *   h = h_in;  one block of layer `layer`;  h_out = bf16(h)  (nearest even).
+ *   h_in, h_out [T, d] bf16 patterns (may not overlap), 1 <= T <= max_batch *
+ *   (max_k + 1).  probe members topk_idx/topk_w/hidden use L = 1 (the hidden
+ *   probe gets [2, T, d]: the input and the fp32 output before rounding). */
+MOE_VERIFY_API int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32_t T, void* h_out,
+                     const moe_verify_probe* probe, void* cuda_stream);
+
+/* Convenience form of one decode iteration on HOST buffers: copies
+ * context_ids [B] and draft_ids [B, K] from host memory (pinned memory makes
+ * the copies asynchronous), runs moe_verify_step and moe_verify_accept on
+ * cuda_stream, copies committed [B, K+1] and accept_len [B] back to host
+ * memory, and waits for the stream.  target_ids (device, [B, K+1]) may be
+ * NULL; the context's own buffer is used then.  Not capturable. */
+MOE_VERIFY_API int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
+                           const int32_t* host_draft_ids, int32_t B, int32_t K,
+                           int32_t* host_committed, int32_t* host_accept_len,
+                           void* cuda_stream);
+
+/* Waits for the device, then returns and clears the sticky device error:
+ * MOE_VERIFY_OK, MOE_VERIFY_ERR_ID_RANGE, MOE_VERIFY_ERR_TIMEOUT or
+ * MOE_VERIFY_ERR_CUDA. */
+MOE_VERIFY_API int moe_verify_sync_status(moe_verify_ctx* ctx);
+
+/* Frees everything the context owns (synchronises the device first).  NULL
+ * is allowed. */
+MOE_VERIFY_API void moe_verify_destroy(moe_verify_ctx* ctx);
+
+/* Static description of a status code; never NULL. */
+MOE_VERIFY_API const char* moe_verify_strerror(int status);
+
+/* Host-only checks, usable without a GPU. */
+
+/* MOE_VERIFY_OK when the config is one this build runs, else an error code
+ * (ARG for out-of-range fields, UNSUPPORTED for shapes the kernels do not
+ * tile). */
+MOE_VERIFY_API int moe_verify_check_config(const moe_verify_config* config);
+
+/* Bytes of device memory moe_verify_init allocates for this config (weights
+ * plus workspace), or 0 for an invalid config. */
+MOE_VERIFY_API uint64_t moe_verify_device_bytes(const moe_verify_config* config);
+
+/* Per-launch time of the library's kernel families, for profiling.
+ * moe_verify_set_timing(ctx, 1) makes later steps record CUDA events around
+ * each launch of the grouped expert GEMMs and of the lm_head kernel on the
+ * step's stream (this breaks graph capture: use it outside capture only).
+ * moe_verify_get_timing synchronises and reports the sums since the last
+ * reset, in milliseconds, and the launch counts:
+ *   ms[0], n[0]: gate/up + SwiGLU GEMM   ms[1], n[1]: down + combine GEMM
+ *   ms[2], n[2]: lm_head + argmax        ms[3], n[3]: routing kernels
+ * reset != 0 clears the sums afterwards. */
+MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
+MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] host*/, int64_t* n /*[4] host*/,
+                          int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

@@ -1,0 +1,291 @@
+"""Python binding of the C ABI in include/moe_verify.h.
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+library.  Tensors are PyTorch CUDA tensors (device memory and streams are the
+only things PyTorch provides here).  If the library cannot be loaded the
+calls raise; there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+_P = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+OK = 0
+ERR_ARG = -1
+ERR_CUDA = -2
+ERR_OOM = -3
+ERR_ID_RANGE = -4
+ERR_TIMEOUT = -5
+ERR_UNSUPPORTED = -6
+
+EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_verify_layer",
+            "moe_verify_decode_host", "moe_verify_sync_status", "moe_verify_destroy",
+            "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
+            "moe_verify_set_timing", "moe_verify_get_timing")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layers", _i32), ("hidden", _i32), ("n_experts", _i32), ("top_k", _i32),
+                ("n_shared", _i32), ("expert_inter", _i32), ("shared_inter", _i32),
+                ("vocab", _i32), ("rms_eps", ctypes.c_float), ("max_batch", _i32),
+                ("max_k", _i32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", _P), ("final_norm", _P), ("lm_head", _P), ("norm", _P),
+                ("router", _P), ("router_bias", _P), ("w_gate", _P), ("w_up", _P),
+                ("w_down", _P), ("s_gate", _P), ("s_up", _P), ("s_down", _P)]
+
+
+class Probe(ctypes.Structure):
+    _fields_ = [("topk_idx", _P), ("topk_w", _P), ("hidden", _P), ("logits", _P)]
+
+
+class MoeVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+
+
+_lib = None
+
+
+def load(build_if_missing: bool = True):
+    """Load libmoe_verify.so (building it first if needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing; run the build first")
+    L = ctypes.CDLL(path)
+    L.moe_verify_init.restype = _i32
+    L.moe_verify_init.argtypes = [_P, _P, _P, ctypes.POINTER(_P)]
+    L.moe_verify_step.restype = _i32
+    L.moe_verify_step.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
+    L.moe_verify_accept.restype = _i32
+    L.moe_verify_accept.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
+    L.moe_verify_layer.restype = _i32
+    L.moe_verify_layer.argtypes = [_P, _i32, _P, _i32, _P, _P, _P]
+    L.moe_verify_decode_host.restype = _i32
+    L.moe_verify_decode_host.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
+    L.moe_verify_sync_status.restype = _i32
+    L.moe_verify_sync_status.argtypes = [_P]
+    L.moe_verify_destroy.restype = None
+    L.moe_verify_destroy.argtypes = [_P]
+    L.moe_verify_strerror.restype = ctypes.c_char_p
+    L.moe_verify_strerror.argtypes = [_i32]
+    L.moe_verify_check_config.restype = _i32
+    L.moe_verify_check_config.argtypes = [_P]
+    L.moe_verify_device_bytes.restype = ctypes.c_uint64
+    L.moe_verify_device_bytes.argtypes = [_P]
+    L.moe_verify_set_timing.restype = _i32
+    L.moe_verify_set_timing.argtypes = [_P, _i32]
+    L.moe_verify_get_timing.restype = _i32
+    L.moe_verify_get_timing.argtypes = [_P, _P, _P, _i32]
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    return load().moe_verify_strerror(int(code)).decode()
+
+
+def make_config(cfg, max_batch: int, max_k: int) -> Config:
+    """Config struct from a shape record with the synthetic module's field names."""
+    return Config(cfg.n_layers, cfg.hidden, cfg.n_experts, cfg.top_k, cfg.n_shared,
+                  cfg.expert_inter, cfg.shared_inter, cfg.vocab, float(cfg.rms_eps),
+                  int(max_batch), int(max_k))
+
+
+def check_config(cfg, max_batch: int, max_k: int) -> int:
+    c = make_config(cfg, max_batch, max_k)
+    return int(load().moe_verify_check_config(ctypes.byref(c)))
+
+
+def device_bytes(cfg, max_batch: int, max_k: int) -> int:
+    c = make_config(cfg, max_batch, max_k)
+    return int(load().moe_verify_device_bytes(ctypes.byref(c)))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev_i32(t):
+    import torch
+    assert t.is_cuda and t.dtype == torch.int32 and t.is_contiguous(), "int32 contiguous CUDA tensor expected"
+    return t
+
+
+def weights_to_device(w: Dict[str, np.ndarray], device="cuda") -> Dict[str, object]:
+    """Upload the synthetic module's weight dict (bf16 bit patterns) to the GPU."""
+    import torch
+    out = {}
+    for k, v in w.items():
+        if v is None:
+            continue
+        if v.dtype == np.uint16:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).to(device).view(torch.bfloat16)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v)).to(device)
+    return out
+
+
+class MoeVerify:
+    """One library context: weights and workspace on the current CUDA device."""
+
+    def __init__(self, cfg, weights: Dict[str, object], max_batch: int, max_k: int, stream=None):
+        import torch
+        self.lib = load()
+        self.cfg = cfg
+        self.max_batch, self.max_k = int(max_batch), int(max_k)
+        self._c = make_config(cfg, max_batch, max_k)
+        dw = {k: (v if isinstance(v, torch.Tensor) else None) for k, v in weights.items()}
+        if any(v is None for v in dw.values()):
+            dw = weights_to_device(weights)
+        L = cfg.n_layers
+        keep = []
+
+        def per_layer(name):
+            t = dw.get(name)
+            if t is None:
+                return None
+            arr = (_P * L)(*[t[l].data_ptr() for l in range(L)])
+            keep.append(arr)
+            return ctypes.cast(arr, _P)
+
+        W = Weights(_ptr(dw["embed"]), _ptr(dw["final_norm"]), _ptr(dw["lm_head"]),
+                    per_layer("norm"), per_layer("router"), per_layer("router_bias"),
+                    per_layer("w_gate"), per_layer("w_up"), per_layer("w_down"),
+                    per_layer("s_gate"), per_layer("s_up"), per_layer("s_down"))
+        h = _P()
+        rc = self.lib.moe_verify_init(ctypes.byref(self._c), ctypes.byref(W),
+                                      _stream_handle(stream), ctypes.byref(h))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_init")
+        self.handle = h
+        del keep, dw
+
+    # -- the calls -----------------------------------------------------------
+    def step(self, context_ids, draft_ids, target_ids=None, probe: Optional[Probe] = None,
+             stream=None):
+        import torch
+        context_ids = _dev_i32(context_ids)
+        B = context_ids.shape[0]
+        K = 0 if draft_ids is None else draft_ids.shape[1]
+        if target_ids is None:
+            target_ids = torch.empty((B, K + 1), dtype=torch.int32, device=context_ids.device)
+        rc = self.lib.moe_verify_step(self.handle, _ptr(context_ids),
+                                      _ptr(draft_ids) if K > 0 else None, B, K, _ptr(target_ids),
+                                      ctypes.byref(probe) if probe is not None else None,
+                                      _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_step")
+        return target_ids
+
+    def accept(self, draft_ids, target_ids, committed=None, accept_len=None, stream=None):
+        import torch
+        B, K1 = target_ids.shape
+        K = K1 - 1
+        if committed is None:
+            committed = torch.empty((B, K1), dtype=torch.int32, device=target_ids.device)
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32, device=target_ids.device)
+        rc = self.lib.moe_verify_accept(self.handle, _ptr(draft_ids) if K > 0 else None,
+                                        _ptr(target_ids), B, K, _ptr(committed), _ptr(accept_len),
+                                        _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_accept")
+        return committed, accept_len
+
+    def layer(self, layer: int, h_in, h_out=None, probe: Optional[Probe] = None, stream=None):
+        import torch
+        T = h_in.shape[0]
+        if h_out is None:
+            h_out = torch.empty_like(h_in)
+        rc = self.lib.moe_verify_layer(self.handle, int(layer), _ptr(h_in), T, _ptr(h_out),
+                                       ctypes.byref(probe) if probe is not None else None,
+                                       _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_layer")
+        return h_out
+
+    def decode_host(self, context_ids: np.ndarray, draft_ids: Optional[np.ndarray],
+                    committed: np.ndarray, accept_len: np.ndarray, stream=None):
+        """Host buffers in and out (pinned numpy views make the copies asynchronous)."""
+        B = context_ids.shape[0]
+        K = 0 if draft_ids is None else draft_ids.shape[1]
+        rc = self.lib.moe_verify_decode_host(
+            self.handle, context_ids.ctypes.data,
+            draft_ids.ctypes.data if K > 0 else None, B, K, committed.ctypes.data,
+            accept_len.ctypes.data, _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_decode_host")
+        return committed, accept_len
+
+    def sync_status(self) -> int:
+        return int(self.lib.moe_verify_sync_status(self.handle))
+
+    def set_timing(self, enable: bool):
+        rc = self.lib.moe_verify_set_timing(self.handle, 1 if enable else 0)
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_set_timing")
+
+    def get_timing(self, reset: bool = True):
+        ms = (ctypes.c_double * 4)()
+        n = (ctypes.c_int64 * 4)()
+        rc = self.lib.moe_verify_get_timing(self.handle, ms, n, 1 if reset else 0)
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_get_timing")
+        return list(ms), list(n)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.moe_verify_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logits: bool = False,
+               device="cuda"):
+    """Allocate probe buffers; returns (Probe struct, dict of tensors)."""
+    import torch
+    t = {}
+    if topk:
+        t["topk_idx"] = torch.full((L, T, cfg.top_k), -7, dtype=torch.int32, device=device)
+        t["topk_w"] = torch.zeros((L, T, cfg.top_k), dtype=torch.float32, device=device)
+    if hidden:
+        t["hidden"] = torch.zeros((L + 1, T, cfg.hidden), dtype=torch.float32, device=device)
+    if logits:
+        t["logits"] = torch.zeros((T, cfg.vocab), dtype=torch.float32, device=device)
+    p = Probe(_ptr(t.get("topk_idx")), _ptr(t.get("topk_w")), _ptr(t.get("hidden")),
+              _ptr(t.get("logits")))
+    return p, t
+
+
+__all__ = ["load", "MoeVerify", "MoeVerifyError", "Probe", "make_probe", "check_config",
+           "device_bytes", "strerror", "weights_to_device", "EXPORTED"]

@@ -1,0 +1,721 @@
+// Host side of the C ABI declared in include/moe_verify.h: argument checks,
+// library-owned weights and workspace, TMA descriptors and the launch order
+// of one verify step.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/moe_verify.h"
+#include "internal.h"
+
+using mv::Item;
+
+struct TimingPair {
+  int family;
+  cudaEvent_t a, b;
+};
+
+struct moe_verify_ctx {
+  moe_verify_config cfg;
+  int device = 0, num_sms = 0;
+  int L = 0, d = 0, E = 0, k = 0, S = 0, I = 0, Is = 0, V = 0;
+  int nE = 0, kS = 0, I_pad = 0, d_pad = 0, V_pad = 0, mt_gu = 0, mt_dn = 0;
+  int T_max = 0, rows_max = 0, items_cap = 0;
+  // library-owned weights
+  __nv_bfloat16 *w_gu = nullptr, *w_dn = nullptr, *w_lm = nullptr, *embed = nullptr,
+                *router = nullptr;
+  float *gain = nullptr, *final_gain = nullptr, *bias = nullptr;
+  bool has_bias = false;
+  // workspace
+  float* h = nullptr;
+  float* y = nullptr;
+  __nv_bfloat16 *xhat = nullptr, *xperm = nullptr, *abuf = nullptr, *xf = nullptr;
+  int32_t *topk_idx = nullptr, *bad = nullptr, *perm_token = nullptr, *perm_slot = nullptr,
+          *expert_off = nullptr, *n_items = nullptr;
+  float *topk_w = nullptr, *perm_w = nullptr;
+  Item *items_gu = nullptr, *items_dn = nullptr;
+  unsigned int *done_route = nullptr, *done_lm = nullptr;
+  unsigned long long* keys = nullptr;
+  uint32_t* status = nullptr;
+  int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
+          *io_alen = nullptr;
+  CUtensorMap map_gu, map_dn, map_lm, map_x, map_a, map_f;
+  std::vector<void*> allocs;
+  // profiling
+  bool timing = false;
+  std::vector<TimingPair> pending;
+  std::vector<cudaEvent_t> event_pool;
+  double ms[4] = {0, 0, 0, 0};
+  int64_t launches[4] = {0, 0, 0, 0};
+};
+
+namespace {
+
+#define CK(x)                                   \
+  do {                                          \
+    cudaError_t _e = (x);                       \
+    if (_e != cudaSuccess) return MOE_VERIFY_ERR_CUDA; \
+  } while (0)
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+struct Derived {
+  int nE, kS, I_pad, d_pad, V_pad, mt_gu, mt_dn, T_max, rows_max, items_cap;
+};
+
+int check(const moe_verify_config* c) {
+  if (!c) return MOE_VERIFY_ERR_ARG;
+  if (c->n_layers < 1 || c->n_layers > 256) return MOE_VERIFY_ERR_ARG;
+  if (c->hidden < 64 || c->hidden > 8192) return MOE_VERIFY_ERR_ARG;
+  if (c->n_experts < 1 || c->n_experts > 256) return MOE_VERIFY_ERR_ARG;
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) return MOE_VERIFY_ERR_ARG;
+  if (c->n_shared < 0 || c->n_shared > 8) return MOE_VERIFY_ERR_ARG;
+  if (c->expert_inter < 1 || c->expert_inter > 8192) return MOE_VERIFY_ERR_ARG;
+  if (c->shared_inter < 1 || c->shared_inter > 8192) return MOE_VERIFY_ERR_ARG;
+  if (c->vocab < 2 || c->vocab > (1 << 30)) return MOE_VERIFY_ERR_ARG;
+  if (!(c->rms_eps > 0.f) || !(c->rms_eps < 1.f)) return MOE_VERIFY_ERR_ARG;
+  if (c->max_batch < 1 || c->max_k < 0 || c->max_k > 15) return MOE_VERIFY_ERR_ARG;
+  if (c->hidden % 64 != 0) return MOE_VERIFY_ERR_UNSUPPORTED;
+  const int64_t T_max = (int64_t)c->max_batch * (c->max_k + 1);
+  if (T_max > 4096) return MOE_VERIFY_ERR_UNSUPPORTED;
+  if (T_max * c->top_k > 32768) return MOE_VERIFY_ERR_UNSUPPORTED;
+  return MOE_VERIFY_OK;
+}
+
+Derived derive(const moe_verify_config* c) {
+  Derived r;
+  r.nE = c->n_experts + c->n_shared;
+  r.kS = c->top_k + c->n_shared;
+  const int Imax = c->expert_inter > c->shared_inter ? c->expert_inter : c->shared_inter;
+  r.I_pad = round_up(Imax, 64);
+  r.d_pad = round_up(c->hidden, 128);
+  r.V_pad = round_up(c->vocab, 128);
+  r.mt_gu = r.I_pad / 64;
+  r.mt_dn = r.d_pad / 128;
+  r.T_max = c->max_batch * (c->max_k + 1);
+  r.rows_max = r.T_max * r.kS;
+  // chunks per layer are at most T*k/16 + E (routed) plus S*(T/16 + 1) (shared)
+  const int chunks = r.T_max * c->top_k / 16 + c->n_experts + c->n_shared * (r.T_max / 16 + 1);
+  const int mt = r.mt_gu > r.mt_dn ? r.mt_gu : r.mt_dn;
+  r.items_cap = chunks * mt;
+  return r;
+}
+
+struct Sizes {
+  uint64_t w_gu, w_dn, w_lm, embed, router, gain, final_gain, bias;
+  uint64_t h, y, xhat, xperm, abuf, xf, topk_idx, topk_w, bad, perm, expert_off, items, keys, io;
+};
+
+Sizes sizes(const moe_verify_config* c, const Derived& r) {
+  Sizes s;
+  const uint64_t L = c->n_layers, d = c->hidden, E = c->n_experts, V = c->vocab;
+  s.w_gu = L * r.nE * r.mt_gu * 128ull * d * 2;
+  s.w_dn = L * r.nE * r.mt_dn * 128ull * r.I_pad * 2;
+  s.w_lm = (uint64_t)r.V_pad * d * 2;
+  s.embed = V * d * 2;
+  s.router = L * E * d * 2;
+  s.gain = L * d * 4;
+  s.final_gain = d * 4;
+  s.bias = L * E * 4;
+  s.h = (uint64_t)r.T_max * d * 4;
+  s.y = (uint64_t)r.T_max * r.kS * d * 4;
+  s.xhat = (uint64_t)r.T_max * d * 2;
+  s.xperm = (uint64_t)r.rows_max * d * 2;
+  s.abuf = (uint64_t)r.rows_max * r.I_pad * 2;
+  s.xf = (uint64_t)round_up(r.T_max, 16) * d * 2;
+  s.topk_idx = (uint64_t)r.T_max * c->top_k * 4;
+  s.topk_w = s.topk_idx;
+  s.bad = (uint64_t)r.T_max * 4;
+  s.perm = (uint64_t)r.rows_max * 4;
+  s.expert_off = (uint64_t)(r.nE + 1) * 4;
+  s.items = (uint64_t)r.items_cap * sizeof(Item);
+  s.keys = (uint64_t)r.T_max * 8;
+  s.io = (uint64_t)r.T_max * 4;
+  return s;
+}
+
+uint64_t total_bytes(const Sizes& s) {
+  return s.w_gu + s.w_dn + s.w_lm + s.embed + s.router + s.gain + s.final_gain + s.bias + s.h +
+         s.y + s.xhat + s.xperm + s.abuf + s.xf + s.topk_idx + s.topk_w + s.bad + 3 * s.perm +
+         s.expert_off + 2 * s.items + s.keys + 5 * s.io + 64;
+}
+
+template <typename T>
+int dalloc(moe_verify_ctx* c, T** p, uint64_t bytes) {
+  void* v = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&v, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? MOE_VERIFY_ERR_OOM : MOE_VERIFY_ERR_CUDA;
+  }
+  c->allocs.push_back(v);
+  *p = static_cast<T*>(v);
+  return MOE_VERIFY_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (row-major), boxes of 64 x box_rows with the
+// 128-byte swizzle that the tcgen05 shared-memory descriptors expect.
+int encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = get_encode();
+  if (!fn) return MOE_VERIFY_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_VERIFY_OK : MOE_VERIFY_ERR_CUDA;
+}
+
+void free_all(moe_verify_ctx* c) {
+  for (void* p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+  for (auto& tp : c->pending) {
+    (void)tp;
+  }
+  for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+  c->event_pool.clear();
+  c->pending.clear();
+}
+
+// ------------------------------------------------------------- profiling
+
+cudaEvent_t take_event(moe_verify_ctx* c) {
+  if (!c->event_pool.empty()) {
+    cudaEvent_t e = c->event_pool.back();
+    c->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct Timed {
+  moe_verify_ctx* c;
+  int family;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  Timed(moe_verify_ctx* c_, int f, cudaStream_t s_) : c(c_), family(f), s(s_) {
+    if (c->timing) {
+      a = take_event(c);
+      cudaEventRecord(a, s);
+    }
+  }
+  ~Timed() {
+    if (c->timing && a) {
+      cudaEvent_t b = take_event(c);
+      cudaEventRecord(b, s);
+      c->pending.push_back({family, a, b});
+    }
+  }
+};
+
+// --------------------------------------------------------------- launches
+
+struct StepShape {
+  int T, tpb, grid_route, nch_r, nch_s, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
+  size_t route_smem;
+};
+
+StepShape shape_for(const moe_verify_ctx* c, int T) {
+  StepShape s;
+  s.T = T;
+  s.tpb = (T + c->num_sms - 1) / c->num_sms;
+  if (s.tpb < 1) s.tpb = 1;
+  if (s.tpb > 8) s.tpb = 8;
+  s.grid_route = (T + s.tpb - 1) / s.tpb;
+  // routed experts see about T*k/E rows each; leave headroom for uneven load
+  int avg = (int)((3LL * T * c->k + 2LL * c->E - 1) / (2LL * c->E));
+  s.nch_r = round_up(avg < 16 ? 16 : avg, 16);
+  if (s.nch_r > 256) s.nch_r = 256;
+  s.nch_s = round_up(T, 16);
+  if (s.nch_s > 256) s.nch_s = 256;
+  s.nch = s.nch_r > s.nch_s ? s.nch_r : s.nch_s;
+  if (c->S == 0) s.nch = s.nch_r;
+  s.stages = mv::gemm_max_stages(s.nch);
+  s.n_chunks_lm = (T + 255) / 256;
+  s.nch_lm = round_up((T + s.n_chunks_lm - 1) / s.n_chunks_lm, 16);
+  int need = 2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm);
+  s.tmem_cols = pow2_at_least(need);
+  s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, T, c->k);
+  return s;
+}
+
+int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int32_t* context_ids,
+              const int32_t* draft_ids, int B, int K, const void* h_in,
+              const moe_verify_probe* probe, int probe_layer, cudaStream_t s, bool pdl) {
+  const int T = sh.T;
+  mv::RouteParams rp = {};
+  rp.T = T;
+  rp.B = B;
+  rp.K = K;
+  rp.d = c->d;
+  rp.E = c->E;
+  rp.k = c->k;
+  rp.S = c->S;
+  rp.V = c->V;
+  rp.tpb = sh.tpb;
+  rp.eps = c->cfg.rms_eps;
+  rp.src = src;
+  rp.context_ids = context_ids;
+  rp.draft_ids = draft_ids;
+  rp.embed = c->embed;
+  rp.h_in = static_cast<const __nv_bfloat16*>(h_in);
+  rp.h = c->h;
+  rp.y = c->y;
+  rp.gain = c->gain + (size_t)l * c->d;
+  rp.Wr = c->router + (size_t)l * c->E * c->d;
+  rp.bias = c->has_bias ? c->bias + (size_t)l * c->E : nullptr;
+  rp.xhat = c->xhat;
+  rp.topk_idx = c->topk_idx;
+  rp.topk_w = c->topk_w;
+  rp.bad = c->bad;
+  rp.status = c->status;
+  if (probe) {
+    if (probe->topk_idx) rp.probe_idx = probe->topk_idx + (size_t)probe_layer * T * c->k;
+    if (probe->topk_w) rp.probe_w = probe->topk_w + (size_t)probe_layer * T * c->k;
+    if (probe->hidden) rp.probe_hidden = probe->hidden + (size_t)probe_layer * T * c->d;
+  }
+  rp.perm_token = c->perm_token;
+  rp.perm_slot = c->perm_slot;
+  rp.perm_w = c->perm_w;
+  rp.expert_off = c->expert_off;
+  rp.items_gu = c->items_gu;
+  rp.items_dn = c->items_dn;
+  rp.n_items = c->n_items;
+  rp.nch_r = sh.nch_r;
+  rp.nch_s = sh.nch_s;
+  rp.mt_gu = c->mt_gu;
+  rp.mt_dn = c->mt_dn;
+  rp.a_base_gu = l * c->nE * c->mt_gu * 128;
+  rp.a_base_dn = l * c->nE * c->mt_dn * 128;
+  rp.done = c->done_route;
+  {
+    Timed tm(c, 3, s);
+    CK(mv::launch_route(rp, sh.grid_route, sh.route_smem, s, pdl));
+    CK(mv::launch_scatter(c->perm_token, c->xhat, c->xperm, T * c->kS, c->d, s, pdl));
+  }
+  mv::GemmParams gp = {};
+  gp.items = c->items_gu;
+  gp.n_items = c->n_items;
+  gp.kblocks = c->d / 64;
+  gp.nch = sh.nch;
+  gp.stages = sh.stages;
+  gp.tmem_cols = sh.tmem_cols;
+  gp.status = c->status;
+  gp.a_out = c->abuf;
+  gp.I_pad = c->I_pad;
+  {
+    Timed tm(c, 0, s);
+    CK(mv::launch_gemm(mv::kGateUp, c->map_gu, c->map_x, gp, c->num_sms, s, pdl));
+  }
+  mv::GemmParams gd = {};
+  gd.items = c->items_dn;
+  gd.n_items = c->n_items + 1;
+  gd.kblocks = c->I_pad / 64;
+  gd.nch = sh.nch;
+  gd.stages = sh.stages;
+  gd.tmem_cols = sh.tmem_cols;
+  gd.status = c->status;
+  gd.perm_token = c->perm_token;
+  gd.perm_slot = c->perm_slot;
+  gd.perm_w = c->perm_w;
+  gd.y = c->y;
+  gd.d = c->d;
+  gd.kS = c->kS;
+  {
+    Timed tm(c, 1, s);
+    CK(mv::launch_gemm(mv::kDown, c->map_dn, c->map_a, gd, c->num_sms, s, pdl));
+  }
+  return MOE_VERIFY_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_verify_strerror(int status) {
+  switch (status) {
+    case MOE_VERIFY_OK: return "ok";
+    case MOE_VERIFY_ERR_ARG: return "invalid argument";
+    case MOE_VERIFY_ERR_CUDA: return "CUDA call failed";
+    case MOE_VERIFY_ERR_OOM: return "out of device memory";
+    case MOE_VERIFY_ERR_ID_RANGE: return "token id outside [0, vocab)";
+    case MOE_VERIFY_ERR_TIMEOUT: return "bounded device wait ran out";
+    case MOE_VERIFY_ERR_UNSUPPORTED: return "unsupported shape or device";
+    default: return "unknown status";
+  }
+}
+
+int moe_verify_check_config(const moe_verify_config* config) { return check(config); }
+
+uint64_t moe_verify_device_bytes(const moe_verify_config* config) {
+  if (check(config) != MOE_VERIFY_OK) return 0;
+  Derived r = derive(config);
+  return total_bytes(sizes(config, r));
+}
+
+int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w,
+                    void* cuda_stream, moe_verify_ctx** out) {
+  if (!out) return MOE_VERIFY_ERR_ARG;
+  *out = nullptr;
+  int rc = check(config);
+  if (rc != MOE_VERIFY_OK) return rc;
+  if (!w || !w->embed || !w->final_norm || !w->lm_head || !w->norm || !w->router || !w->w_gate ||
+      !w->w_up || !w->w_down)
+    return MOE_VERIFY_ERR_ARG;
+  if (config->n_shared > 0 && (!w->s_gate || !w->s_up || !w->s_down)) return MOE_VERIFY_ERR_ARG;
+  for (int l = 0; l < config->n_layers; ++l) {
+    if (!w->norm[l] || !w->router[l] || !w->w_gate[l] || !w->w_up[l] || !w->w_down[l])
+      return MOE_VERIFY_ERR_ARG;
+    if (config->n_shared > 0 && (!w->s_gate[l] || !w->s_up[l] || !w->s_down[l]))
+      return MOE_VERIFY_ERR_ARG;
+  }
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_VERIFY_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_VERIFY_ERR_UNSUPPORTED;
+  if (!get_encode()) return MOE_VERIFY_ERR_CUDA;
+
+  moe_verify_ctx* c = new (std::nothrow) moe_verify_ctx();
+  if (!c) return MOE_VERIFY_ERR_OOM;
+  c->cfg = *config;
+  c->device = dev;
+  c->num_sms = sms;
+  c->L = config->n_layers;
+  c->d = config->hidden;
+  c->E = config->n_experts;
+  c->k = config->top_k;
+  c->S = config->n_shared;
+  c->I = config->expert_inter;
+  c->Is = config->shared_inter;
+  c->V = config->vocab;
+  Derived r = derive(config);
+  c->nE = r.nE;
+  c->kS = r.kS;
+  c->I_pad = r.I_pad;
+  c->d_pad = r.d_pad;
+  c->V_pad = r.V_pad;
+  c->mt_gu = r.mt_gu;
+  c->mt_dn = r.mt_dn;
+  c->T_max = r.T_max;
+  c->rows_max = r.rows_max;
+  c->items_cap = r.items_cap;
+  Sizes z = sizes(config, r);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  auto fail = [&](int code) {
+    cudaStreamSynchronize(s);
+    free_all(c);
+    delete c;
+    return code;
+  };
+#define AL(ptr, bytes)                       \
+  do {                                       \
+    int _r = dalloc(c, &(ptr), (bytes));     \
+    if (_r != MOE_VERIFY_OK) return fail(_r); \
+  } while (0)
+#define CKF(x)                                                 \
+  do {                                                         \
+    if ((x) != cudaSuccess) return fail(MOE_VERIFY_ERR_CUDA);  \
+  } while (0)
+
+  AL(c->w_gu, z.w_gu);
+  AL(c->w_dn, z.w_dn);
+  AL(c->w_lm, z.w_lm);
+  AL(c->embed, z.embed);
+  AL(c->router, z.router);
+  AL(c->gain, z.gain);
+  AL(c->final_gain, z.final_gain);
+  AL(c->bias, z.bias);
+  AL(c->h, z.h);
+  AL(c->y, z.y);
+  AL(c->xhat, z.xhat);
+  AL(c->xperm, z.xperm);
+  AL(c->abuf, z.abuf);
+  AL(c->xf, z.xf);
+  AL(c->topk_idx, z.topk_idx);
+  AL(c->topk_w, z.topk_w);
+  AL(c->bad, z.bad);
+  AL(c->perm_token, z.perm);
+  AL(c->perm_slot, z.perm);
+  AL(c->perm_w, z.perm);
+  AL(c->expert_off, z.expert_off);
+  AL(c->items_gu, z.items);
+  AL(c->items_dn, z.items);
+  AL(c->n_items, 16);
+  AL(c->done_route, 16);
+  AL(c->done_lm, 16);
+  AL(c->keys, z.keys);
+  AL(c->status, 16);
+  AL(c->io_ctx, z.io);
+  AL(c->io_drafts, z.io);
+  AL(c->io_targets, z.io);
+  AL(c->io_committed, z.io);
+  AL(c->io_alen, z.io);
+
+  // zero the workspace so that padding rows read by the MMAs are finite
+  CKF(cudaMemsetAsync(c->y, 0, z.y, s));
+  CKF(cudaMemsetAsync(c->xperm, 0, z.xperm, s));
+  CKF(cudaMemsetAsync(c->abuf, 0, z.abuf, s));
+  CKF(cudaMemsetAsync(c->xf, 0, z.xf, s));
+  CKF(cudaMemsetAsync(c->n_items, 0, 16, s));
+  CKF(cudaMemsetAsync(c->done_route, 0, 16, s));
+  CKF(cudaMemsetAsync(c->done_lm, 0, 16, s));
+  CKF(cudaMemsetAsync(c->status, 0, 16, s));
+  CKF(cudaMemsetAsync(c->bias, 0, z.bias, s));
+
+  // weights: copy and repack
+  const int d = c->d, E = c->E, L = c->L;
+  CKF(cudaMemcpyAsync(c->embed, w->embed, z.embed, cudaMemcpyDeviceToDevice, s));
+  CKF(cudaMemsetAsync(c->w_lm, 0, z.w_lm, s));
+  CKF(cudaMemcpyAsync(c->w_lm, w->lm_head, (size_t)c->V * d * 2, cudaMemcpyDeviceToDevice, s));
+  CKF(mv::launch_bf16_to_f32(c->final_gain, static_cast<const __nv_bfloat16*>(w->final_norm), d, s));
+  const size_t gu_layer = (size_t)c->nE * c->mt_gu * 128 * d;
+  const size_t dn_layer = (size_t)c->nE * c->mt_dn * 128 * c->I_pad;
+  for (int l = 0; l < L; ++l) {
+    CKF(cudaMemcpyAsync(c->router + (size_t)l * E * d, w->router[l], (size_t)E * d * 2,
+                        cudaMemcpyDeviceToDevice, s));
+    CKF(mv::launch_bf16_to_f32(c->gain + (size_t)l * d,
+                               static_cast<const __nv_bfloat16*>(w->norm[l]), d, s));
+    if (w->router_bias && w->router_bias[l]) {
+      c->has_bias = true;
+      CKF(cudaMemcpyAsync(c->bias + (size_t)l * E, w->router_bias[l], (size_t)E * 4,
+                          cudaMemcpyDeviceToDevice, s));
+    }
+    const __nv_bfloat16* sg = c->S ? static_cast<const __nv_bfloat16*>(w->s_gate[l]) : nullptr;
+    const __nv_bfloat16* su = c->S ? static_cast<const __nv_bfloat16*>(w->s_up[l]) : nullptr;
+    const __nv_bfloat16* sd = c->S ? static_cast<const __nv_bfloat16*>(w->s_down[l]) : nullptr;
+    CKF(mv::launch_repack_gateup(c->w_gu + gu_layer * l,
+                                 static_cast<const __nv_bfloat16*>(w->w_gate[l]),
+                                 static_cast<const __nv_bfloat16*>(w->w_up[l]), sg, su, E, c->S,
+                                 c->I, c->Is, d, c->mt_gu, s));
+    CKF(mv::launch_repack_down(c->w_dn + dn_layer * l,
+                               static_cast<const __nv_bfloat16*>(w->w_down[l]), sd, E, c->S, c->I,
+                               c->Is, d, c->I_pad, c->mt_dn, s));
+  }
+  CKF(cudaStreamSynchronize(s));
+
+  int e1 = encode_map(&c->map_gu, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 128);
+  int e2 = encode_map(&c->map_dn, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 128);
+  int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
+  int e4 = encode_map(&c->map_x, c->xperm, d, c->rows_max, 16);
+  int e5 = encode_map(&c->map_a, c->abuf, c->I_pad, c->rows_max, 16);
+  int e6 = encode_map(&c->map_f, c->xf, d, round_up(c->T_max, 16), 16);
+  if (e1 || e2 || e3 || e4 || e5 || e6) return fail(MOE_VERIFY_ERR_CUDA);
+#undef AL
+#undef CKF
+  *out = c;
+  return MOE_VERIFY_OK;
+}
+
+static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
+                        int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
+                        cudaStream_t s) {
+  const int T = B * (K + 1);
+  StepShape sh = shape_for(ctx, T);
+  const bool pdl = false;
+  for (int l = 0; l < ctx->L; ++l) {
+    int rc = run_layer(ctx, l, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
+                       draft_ids, B, K, nullptr, probe, l, s, pdl);
+    if (rc != MOE_VERIFY_OK) return rc;
+  }
+  mv::FinalParams fp = {};
+  fp.T = T;
+  fp.d = ctx->d;
+  fp.kS = ctx->kS;
+  fp.eps = ctx->cfg.rms_eps;
+  fp.mode = 0;
+  fp.h = ctx->h;
+  fp.y = ctx->y;
+  fp.gain = ctx->final_gain;
+  fp.out = ctx->xf;
+  fp.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
+  fp.keys = ctx->keys;
+  {
+    Timed tm(ctx, 3, s);
+    CK(mv::launch_final(fp, s, pdl));
+  }
+  mv::GemmParams gp = {};
+  gp.n_items_static = (ctx->V_pad / 128) * sh.n_chunks_lm;
+  gp.kblocks = ctx->d / 64;
+  gp.nch = sh.nch_lm;
+  gp.stages = mv::gemm_max_stages(sh.nch_lm);
+  gp.tmem_cols = pow2_at_least(2 * sh.nch_lm);
+  gp.status = ctx->status;
+  gp.T = T;
+  gp.V = ctx->V;
+  gp.n_chunks = sh.n_chunks_lm;
+  gp.nch_lm = sh.nch_lm;
+  gp.keys = ctx->keys;
+  gp.logits = probe ? probe->logits : nullptr;
+  gp.targets = target_ids;
+  gp.bad = ctx->bad;
+  gp.done = ctx->done_lm;
+  {
+    Timed tm(ctx, 2, s);
+    CK(mv::launch_gemm(mv::kLmHead, ctx->map_lm, ctx->map_f, gp, ctx->num_sms, s, pdl));
+  }
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
+                    int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
+                    void* cuda_stream) {
+  if (!ctx || !context_ids || !target_ids) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
+  if (K > 0 && !draft_ids) return MOE_VERIFY_ERR_ARG;
+  return enqueue_step(ctx, context_ids, draft_ids, B, K, target_ids, probe,
+                      static_cast<cudaStream_t>(cuda_stream));
+}
+
+int moe_verify_accept(moe_verify_ctx* ctx, const int32_t* draft_ids, const int32_t* target_ids,
+                      int32_t B, int32_t K, int32_t* committed, int32_t* accept_len,
+                      void* cuda_stream) {
+  if (!ctx || !target_ids || !committed || !accept_len) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || K < 0 || K > 15) return MOE_VERIFY_ERR_ARG;
+  if (K > 0 && !draft_ids) return MOE_VERIFY_ERR_ARG;
+  mv::AcceptParams ap;
+  ap.B = B;
+  ap.K = K;
+  ap.V = ctx->V;
+  ap.drafts = draft_ids;
+  ap.targets = target_ids;
+  ap.committed = committed;
+  ap.accept_len = accept_len;
+  ap.status = ctx->status;
+  CK(mv::launch_accept(ap, static_cast<cudaStream_t>(cuda_stream)));
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32_t T, void* h_out,
+                     const moe_verify_probe* probe, void* cuda_stream) {
+  if (!ctx || !h_in || !h_out) return MOE_VERIFY_ERR_ARG;
+  if (layer < 0 || layer >= ctx->L || T < 1 || T > ctx->T_max) return MOE_VERIFY_ERR_ARG;
+  if (!aligned16(h_in) || !aligned16(h_out)) return MOE_VERIFY_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  StepShape sh = shape_for(ctx, T);
+  int rc = run_layer(ctx, layer, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
+                     false);
+  if (rc != MOE_VERIFY_OK) return rc;
+  mv::FinalParams fp = {};
+  fp.T = T;
+  fp.d = ctx->d;
+  fp.kS = ctx->kS;
+  fp.eps = ctx->cfg.rms_eps;
+  fp.mode = 1;
+  fp.h = ctx->h;
+  fp.y = ctx->y;
+  fp.gain = ctx->final_gain;
+  fp.out = static_cast<__nv_bfloat16*>(h_out);
+  fp.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)T * ctx->d : nullptr;
+  fp.keys = ctx->keys;
+  {
+    Timed tm(ctx, 3, s);
+    CK(mv::launch_final(fp, s, false));
+  }
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
+                           const int32_t* host_draft_ids, int32_t B, int32_t K,
+                           int32_t* host_committed, int32_t* host_accept_len, void* cuda_stream) {
+  if (!ctx || !host_context_ids || !host_committed || !host_accept_len) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
+  if (K > 0 && !host_draft_ids) return MOE_VERIFY_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  CK(cudaMemcpyAsync(ctx->io_ctx, host_context_ids, (size_t)B * 4, cudaMemcpyHostToDevice, s));
+  if (K > 0)
+    CK(cudaMemcpyAsync(ctx->io_drafts, host_draft_ids, (size_t)B * K * 4, cudaMemcpyHostToDevice,
+                       s));
+  int rc = enqueue_step(ctx, ctx->io_ctx, ctx->io_drafts, B, K, ctx->io_targets, nullptr, s);
+  if (rc != MOE_VERIFY_OK) return rc;
+  rc = moe_verify_accept(ctx, ctx->io_drafts, ctx->io_targets, B, K, ctx->io_committed,
+                         ctx->io_alen, s);
+  if (rc != MOE_VERIFY_OK) return rc;
+  CK(cudaMemcpyAsync(host_committed, ctx->io_committed, (size_t)B * (K + 1) * 4,
+                     cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(host_accept_len, ctx->io_alen, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_sync_status(moe_verify_ctx* ctx) {
+  if (!ctx) return MOE_VERIFY_ERR_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
+  uint32_t st = 0;
+  if (cudaMemcpy(&st, ctx->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_VERIFY_ERR_CUDA;
+  if (cudaMemset(ctx->status, 0, 4) != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
+  if (st & mv::kErrTimeout) return MOE_VERIFY_ERR_TIMEOUT;
+  if (st & mv::kErrIdRange) return MOE_VERIFY_ERR_ID_RANGE;
+  if (st) return MOE_VERIFY_ERR_CUDA;
+  return MOE_VERIFY_OK;
+}
+
+void moe_verify_destroy(moe_verify_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  free_all(ctx);
+  delete ctx;
+}
+
+int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable) {
+  if (!ctx) return MOE_VERIFY_ERR_ARG;
+  ctx->timing = enable != 0;
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms, int64_t* n, int32_t reset) {
+  if (!ctx || !ms || !n) return MOE_VERIFY_ERR_ARG;
+  for (auto& tp : ctx->pending) {
+    if (cudaEventSynchronize(tp.b) != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, tp.a, tp.b) != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
+    ctx->ms[tp.family] += t;
+    ctx->launches[tp.family] += 1;
+    ctx->event_pool.push_back(tp.a);
+    ctx->event_pool.push_back(tp.b);
+  }
+  ctx->pending.clear();
+  for (int i = 0; i < 4; ++i) {
+    ms[i] = ctx->ms[i];
+    n[i] = ctx->launches[i];
+    if (reset) {
+      ctx->ms[i] = 0;
+      ctx->launches[i] = 0;
+    }
+  }
+  return MOE_VERIFY_OK;
+}
+
+}  // extern "C"

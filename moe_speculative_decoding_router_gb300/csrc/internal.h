@@ -1,0 +1,140 @@
+// Internal interface between the host API (api.cu) and the kernels
+// (route.cu, gemm.cu, misc.cu).  Not part of the C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mv {
+
+// Bits of the device status word.
+constexpr uint32_t kErrIdRange = 1u;
+constexpr uint32_t kErrTimeout = 2u;
+constexpr uint32_t kErrInternal = 4u;
+
+// One unit of grouped-GEMM work: a 128-row tile of one weight matrix times
+// up to `n` activation rows.  a_row: first row of the tile in the weight
+// tensor map; b_row: first activation row; aux: tile index inside the expert.
+struct Item {
+  int32_t a_row;
+  int32_t b_row;
+  int32_t n;
+  int32_t aux;
+};
+
+// Sources of the residual stream entering a routing kernel.
+enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2 };
+
+struct RouteParams {
+  int T, B, K;          // verify tokens, sequences, drafts per sequence
+  int d, E, k, S, V;
+  int tpb;              // tokens per block (1..8)
+  float eps;
+  int src;              // RouteSrc
+  const int32_t* context_ids;
+  const int32_t* draft_ids;
+  const __nv_bfloat16* embed;  // [V, d]
+  const __nv_bfloat16* h_in;   // [T, d] (kSrcBf16)
+  float* h;                    // [T, d] residual stream (fp32)
+  const float* y;              // [T, k+S, d] expert outputs of the previous block
+  const float* gain;           // [d]
+  const __nv_bfloat16* Wr;     // [E, d]
+  const float* bias;           // [E] or nullptr
+  __nv_bfloat16* xhat;         // [T, d]
+  int32_t* topk_idx;           // [T, k]
+  float* topk_w;               // [T, k]
+  int32_t* bad;                // [T]
+  uint32_t* status;
+  int32_t* probe_idx;          // [T, k] or nullptr
+  float* probe_w;              // [T, k] or nullptr
+  float* probe_hidden;         // [T, d] or nullptr
+  // grouping (done by the last block to finish)
+  int32_t* perm_token;         // [rows]
+  int32_t* perm_slot;          // [rows]
+  float* perm_w;               // [rows]
+  int32_t* expert_off;         // [E+S+1]
+  Item* items_gu;
+  Item* items_dn;
+  int32_t* n_items;            // [2]
+  int nch_r, nch_s;            // activation rows per item: routed / shared experts
+  int mt_gu, mt_dn;            // 128-row tiles per expert: gate/up, down
+  int a_base_gu, a_base_dn;    // first weight row of this layer in the tensor maps
+  unsigned int* done;
+};
+
+struct FinalParams {
+  int T, d, kS;                // kS = k + S slots per token
+  float eps;
+  int mode;                    // 0: final RMSNorm -> xf;  1: h_out = bf16(h)
+  float* h;                    // [T, d]
+  const float* y;              // [T, kS, d]
+  const float* gain;           // [d]
+  __nv_bfloat16* out;          // mode 0: xf [T, d]; mode 1: h_out [T, d]
+  float* probe_hidden;         // [T, d] or nullptr
+  unsigned long long* keys;    // [T] argmax keys, cleared in mode 0
+};
+
+enum GemmMode : int { kGateUp = 0, kDown = 1, kLmHead = 2 };
+
+struct GemmParams {
+  const Item* items;           // kGateUp, kDown
+  const int32_t* n_items;      // device count
+  int n_items_static;          // kLmHead
+  int kblocks;                 // K / 64
+  int nch;                     // largest activation row count of an item (multiple of 16)
+  int stages;
+  int tmem_cols;
+  uint32_t* status;
+  // kGateUp
+  __nv_bfloat16* a_out;        // [rows, I_pad]
+  int I_pad;
+  // kDown
+  const int32_t* perm_token;
+  const int32_t* perm_slot;
+  const float* perm_w;
+  float* y;                    // [T, kS, d]
+  int d, kS;
+  // kLmHead
+  int T, V, n_chunks, nch_lm;
+  unsigned long long* keys;    // [T]
+  float* logits;               // [T, V] or nullptr
+  int32_t* targets;            // [T]
+  const int32_t* bad;          // [T]
+  unsigned int* done;
+};
+
+struct AcceptParams {
+  int B, K, V;
+  const int32_t* drafts;
+  const int32_t* targets;
+  int32_t* committed;
+  int32_t* accept_len;
+  uint32_t* status;
+};
+
+// Shared memory the GEMM kernel needs for a given item width and stage count.
+size_t gemm_smem_bytes(int nch, int stages);
+int gemm_max_stages(int nch);
+size_t route_smem_bytes(int tpb, int d, int E, int T, int k);
+
+// Launchers (enqueue only).  `pdl` requests programmatic dependent launch.
+cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_scatter(const int32_t* perm_token, const __nv_bfloat16* xhat,
+                           __nv_bfloat16* xperm, int rows, int d, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm(int mode, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                        const GemmParams& p, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
+
+// Weight repacking (init only).
+cudaError_t launch_repack_gateup(__nv_bfloat16* dst, const __nv_bfloat16* gate,
+                                 const __nv_bfloat16* up, const __nv_bfloat16* s_gate,
+                                 const __nv_bfloat16* s_up, int E, int S, int I, int Is, int d,
+                                 int mt_gu, cudaStream_t s);
+cudaError_t launch_repack_down(__nv_bfloat16* dst, const __nv_bfloat16* down,
+                               const __nv_bfloat16* s_down, int E, int S, int I, int Is, int d,
+                               int I_pad, int mt_dn, cudaStream_t s);
+cudaError_t launch_bf16_to_f32(float* dst, const __nv_bfloat16* src, int64_t n, cudaStream_t s);
+
+}  // namespace mv

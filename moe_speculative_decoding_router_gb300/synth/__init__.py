@@ -144,8 +144,10 @@ class ModelConfig:
 # Tiny correctness instance: 2 layers, d=64, 8 experts of 32, top-2, one
 # shared expert, vocab 512, weights N(0, 0.05).
 TINY = ModelConfig(2, 64, 8, 2, 1, 32, 32, 512, sigma=0.05, name="tiny")
-# One layer at the decoder's expert layout (hidden 1280, 64 x 896, top-6, 2 shared).
-LAYER = ModelConfig(1, 1280, 64, 6, 2, 896, 896, 129280, name="layer")
+# One layer at the decoder's expert layout (hidden 1280, 64 x 896, top-6, 2
+# shared).  The single-block entry point never touches the vocabulary, so a
+# small one keeps the embedding and lm_head cheap.
+LAYER = ModelConfig(1, 1280, 64, 6, 2, 896, 896, 512, name="layer")
 # The full 12-layer stack with the 129,280-token vocabulary.
 FULL = ModelConfig(12, 1280, 64, 6, 2, 896, 896, 129280, name="full")
 # The full stack with Zipf(s=1.2)-skewed routing.

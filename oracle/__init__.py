@@ -77,6 +77,8 @@ def lib():
         L.oracle_verify_step.argtypes = [_P, _P, _P, _P, _i32, _i32, _P]
         L.oracle_accept.restype = _i32
         L.oracle_accept.argtypes = [_P, _P, _i32, _i32, _i32, _P, _P]
+        L.oracle_head.restype = _i32
+        L.oracle_head.argtypes = [_P, _P, _P, _P, _P]
         L.oracle_layer_bf16.restype = None
         L.oracle_layer_bf16.argtypes = [_P, _P, _i32, _P, _P, _P, _P, _P, _P, _P]
         _lib = L
@@ -228,6 +230,15 @@ class Oracle:
         lib().oracle_layer(self._cp, self._wp, int(l), _ptr(hh), _ptr(fs), _ptr(sel), _ptr(wts),
                            _ptr(gap), _ptr(xh))
         return hh, sel, wts, float(gap[0]), xh
+
+    def head(self, h: np.ndarray, logits: bool = False):
+        """Final RMSNorm + lm_head argmax on residual h [d].  Returns
+        (target, top-2 logit gap, logits or None)."""
+        hh = np.ascontiguousarray(h, dtype=np.float64)
+        lg = np.empty(self.cfg.vocab) if logits else None
+        gap = np.empty(1)
+        y = lib().oracle_head(self._cp, self._wp, _ptr(hh), _ptr(lg), _ptr(gap))
+        return int(y), float(gap[0]), lg
 
     def layer_bf16(self, l: int, h_in: np.ndarray, force_sel: Optional[np.ndarray] = None):
         """The bf16-in/bf16-out block on one token.  Returns

@@ -170,8 +170,9 @@ ORACLE_API void oracle_swiglu_expert(const uint16_t* xhat, const uint16_t* Wg, c
  * (routed slots in selection order, then shared experts in index order).
  * force_sel (k ids, or NULL) replaces the selected set, keeping the softmax
  * weights of the forced experts: used to follow a different but equally valid
- * choice at a near tie.  Diagnostics (each may be NULL): sel_out[k],
- * w_out[k], gap_out (z_(k) - z_(k+1)), xhat_out[d]. */
+ * choice at a near tie.  Diagnostics (each may be NULL): sel_out[k] (the
+ * block's own top-k choice, before any forcing), w_out[k] (the weights
+ * applied), gap_out (z_(k) - z_(k+1)), xhat_out[d]. */
 ORACLE_API void oracle_layer(const oracle_config* c, const oracle_weights* w, int32_t l, double* h,
                              const int32_t* force_sel, int32_t* sel_out, double* w_out,
                              double* gap_out, uint16_t* xhat_out) {
@@ -189,6 +190,7 @@ ORACLE_API void oracle_layer(const oracle_config* c, const oracle_weights* w, in
   oracle_rmsnorm_bf16(h, w->norm[l], d, c->rms_eps, xhat);
   oracle_router(xhat, w->router[l], w->router_bias ? w->router_bias[l] : NULL, E, d, k, z, p, sel,
                 psel, &gap);
+  if (sel_out) memcpy(sel_out, sel, sizeof(int32_t) * (size_t)k); /* the block's own choice */
   if (force_sel) {
     for (int j = 0; j < k; ++j) {
       sel[j] = force_sel[j];
@@ -210,7 +212,6 @@ ORACLE_API void oracle_layer(const oracle_config* c, const oracle_weights* w, in
   }
   for (int m = 0; m < d; ++m) h[m] += acc[m];
 
-  if (sel_out) memcpy(sel_out, sel, sizeof(int32_t) * (size_t)k);
   if (w_out) memcpy(w_out, psel, sizeof(double) * (size_t)k);
   if (gap_out) *gap_out = gap;
   if (xhat_out) memcpy(xhat_out, xhat, sizeof(uint16_t) * (size_t)d);
@@ -238,6 +239,18 @@ static int32_t lm_head_argmax(const oracle_config* c, const oracle_weights* w, c
   }
   if (top2_gap) *top2_gap = best - second;
   return arg;
+}
+
+/* Final RMSNorm and greedy choice on a given residual stream h [d]:
+ * xhat_f = bf16(RMSNorm(h) * g_f);  returns argmax_v xhat_f . W_lm[v]
+ * (lowest v on ties).  logits [V] and logit_gap (top-2 gap) may be NULL. */
+ORACLE_API int32_t oracle_head(const oracle_config* c, const oracle_weights* w, const double* h,
+                               double* logits, double* logit_gap) {
+  uint16_t* xf = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)c->hidden);
+  oracle_rmsnorm_bf16(h, w->final_norm, c->hidden, c->rms_eps, xf);
+  int32_t y = lm_head_argmax(c, w, xf, logits, logit_gap);
+  free(xf);
+  return y;
 }
 
 /* Target stack on one verify token id x:

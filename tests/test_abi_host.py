@@ -1,0 +1,81 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and its host-only checks behave."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from moe_speculative_decoding_router_gb300 import binding as B
+from moe_speculative_decoding_router_gb300 import build as build_mod
+from moe_speculative_decoding_router_gb300 import synth as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            names |= set(re.findall(r"^MOE_VERIFY_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    path = build_mod.build()
+    names = declared_entry_points()
+    assert {"moe_verify_init", "moe_verify_step", "moe_verify_accept"} <= names
+    lib = ctypes.CDLL(path)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert names == exported, (names ^ exported)
+    assert set(B.EXPORTED) == names
+
+
+def test_library_links_no_torch_and_no_oracle():
+    out = subprocess.run(["ldd", build_mod.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in out and "oracle" not in out and "synth" not in out
+
+
+def test_strerror_covers_every_status():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert B.strerror(code) and B.strerror(code) != "unknown status"
+    assert B.strerror(-99) == "unknown status"
+
+
+def test_check_config():
+    assert B.check_config(S.FULL, 32, 3) == B.OK
+    assert B.check_config(S.TINY, 4, 3) == B.OK
+    assert B.check_config(S.FULL, 0, 3) == B.ERR_ARG
+    assert B.check_config(S.FULL, 32, 16) == B.ERR_ARG
+    assert B.check_config(S.FULL, 4096, 3) == B.ERR_UNSUPPORTED     # T = 16384 tokens
+    import dataclasses
+    assert B.check_config(dataclasses.replace(S.FULL, hidden=1000), 32, 3) == B.ERR_UNSUPPORTED
+    assert B.check_config(dataclasses.replace(S.FULL, top_k=65), 32, 3) == B.ERR_ARG
+    assert B.check_config(dataclasses.replace(S.FULL, rms_eps=0.0), 32, 3) == B.ERR_ARG
+    assert B.device_bytes(S.FULL, 0, 3) == 0
+
+
+def test_device_bytes_is_weights_plus_workspace():
+    n = B.device_bytes(S.FULL, 32, 3)
+    per_expert = 3 * 896 * 1280 * 2
+    weights = 12 * 66 * per_expert + 2 * 129280 * 1280 * 2
+    assert weights < n < weights * 1.05
+
+
+def test_null_arguments_fail_on_the_host():
+    lib = B.load()
+    assert lib.moe_verify_step(None, None, None, 1, 0, None, None, None) == B.ERR_ARG
+    assert lib.moe_verify_accept(None, None, None, 1, 0, None, None, None) == B.ERR_ARG
+    assert lib.moe_verify_layer(None, 0, None, 1, None, None, None) == B.ERR_ARG
+    assert lib.moe_verify_sync_status(None) == B.ERR_ARG
+    assert lib.moe_verify_check_config(None) == B.ERR_ARG
+    h = ctypes.c_void_p()
+    assert lib.moe_verify_init(None, None, None, ctypes.byref(h)) == B.ERR_ARG
+    assert h.value is None
+    lib.moe_verify_destroy(None)
