@@ -200,7 +200,7 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    cfg = S.FULL
+    cfg = S.FULL if not args.layers else __import__("dataclasses").replace(S.FULL, n_layers=args.layers)
     t_setup = time.perf_counter()
     w_host = S.make_weights(cfg)
     w_dev = BND.weights_to_device(w_host, device=dev)
@@ -210,11 +210,14 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream()
 
     # greedy table g over the whole vocabulary, 4,096 verify tokens per call
+    # (profiling runs use a random table instead: same kernels, same shapes)
     V = cfg.vocab
     g = np.empty(V, dtype=np.int32)
+    if args.profile:
+        g[:] = S.uniform_ids(V, 99, 0, V)
     chunk = 1024 * (K_DRAFT + 1)
     all_ids = torch.arange(V, dtype=torch.int32, device=dev)
-    for s0 in range(0, V, chunk):
+    for s0 in (range(0, V, chunk) if not args.profile else ()):
         n = min(chunk, V - s0)
         Bn = (n + K_DRAFT) // (K_DRAFT + 1)
         ids = torch.zeros(Bn * (K_DRAFT + 1), dtype=torch.int32, device=dev)
@@ -303,6 +306,13 @@ def run_ours(args, rank, world, local):
     clocks.stop()
     ms = ev0.elapsed_time(ev1)
     clk = clocks.summary(w0, w1)
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "layers": cfg.n_layers, "steps": args.steps,
+                              "ms_per_step": round(ms / args.steps, 4), "clocks": clk}), flush=True)
+        ctx.close()
+        return
 
     # every timed step committed exactly what the planned trajectory says
     got_com = d_com[args.warmup:].cpu().numpy()
@@ -501,9 +511,15 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="timing loop only (random greedy table; no e2e, roofline or CPU legs)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: a shorter stack (same per-layer shapes)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.layers and not args.profile:
+        ap.error("--layers is for profiling runs only (--profile)")
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
