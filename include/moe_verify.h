@@ -206,6 +206,43 @@ MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
 MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] host*/, int64_t* n /*[4] host*/,
                           int32_t reset);
 
+/* ----------------------------------------------------------------------
+ * Greedy head without allocation.  The pages have no counterpart of this
+ * entry point: it exists for callers that cannot allocate device memory,
+ * such as code whose device memory belongs to another allocator with a fixed
+ * budget, code that must not stall other streams (cudaMalloc and cudaFree
+ * can synchronise the device), or code running where CUDA allocation calls
+ * are not allowed.
+ *
+ * It computes, for T residual-stream rows h [T, d] (fp32, device):
+ *   target_ids[t] = argmax_v bf16(RMSNorm(h[t]) * g) . W_lm[v]   (lowest v on ties)
+ * with final_norm g [d] and lm_head W_lm [V, d] as bf16 device arrays
+ * (h and lm_head 16-byte aligned), the same kernels as moe_verify_step's
+ * last stage.
+ * target_ids [T] int32 (device) is written; -1 marks a row whose device-side
+ * work gave up after a bounded wait.
+ *
+ * Its scratch (normalised rows, argmax keys, a completion counter) is a
+ * fixed array of about 1 MB in the library's device memory; every GPU that
+ * loads the library holds it until the process exits.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine) and
+ * enqueues two kernels on cuda_stream.  Limits: 1 <= T <= 256 and
+ * 64 <= d <= 2048 with d a multiple of 64; larger sizes are rejected with
+ * MOE_VERIFY_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     the call clears what must start at zero.  Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it and give wrong results.
+ * -------------------------------------------------------------------- */
+#define MOE_VERIFY_NOALLOC_MAX_TOKENS 256
+#define MOE_VERIFY_NOALLOC_MAX_HIDDEN 2048
+MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h, const void* final_norm,
+                                                  const void* lm_head, int32_t T, int32_t d,
+                                                  int32_t V, float rms_eps, int32_t* target_ids,
+                                                  void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

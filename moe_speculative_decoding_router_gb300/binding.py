@@ -29,7 +29,7 @@ ERR_UNSUPPORTED = -6
 EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_verify_layer",
             "moe_verify_decode_host", "moe_verify_sync_status", "moe_verify_destroy",
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
-            "moe_verify_set_timing", "moe_verify_get_timing")
+            "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc")
 
 
 class Config(ctypes.Structure):
@@ -93,6 +93,9 @@ def load(build_if_missing: bool = True):
     L.moe_verify_set_timing.argtypes = [_P, _i32]
     L.moe_verify_get_timing.restype = _i32
     L.moe_verify_get_timing.argtypes = [_P, _P, _P, _i32]
+    L.moe_verify_greedy_head_noalloc.restype = _i32
+    L.moe_verify_greedy_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P,
+                                                 _P]
     _lib = L
     return L
 
@@ -268,6 +271,23 @@ class MoeVerify:
             self.close()
         except Exception:
             pass
+
+
+def greedy_head_noalloc(h, final_norm, lm_head, rms_eps: float, target_ids=None, stream=None):
+    """moe_verify_greedy_head_noalloc: argmax of lm_head . bf16(RMSNorm(h) * g)
+    for each row of h [T, d] (fp32 CUDA tensor), with no device allocation
+    inside the call (target_ids may be passed preallocated)."""
+    import torch
+    T, d = h.shape
+    V = lm_head.shape[0]
+    if target_ids is None:
+        target_ids = torch.empty((T,), dtype=torch.int32, device=h.device)
+    rc = load().moe_verify_greedy_head_noalloc(_ptr(h), _ptr(final_norm), _ptr(lm_head), T, d, V,
+                                                float(rms_eps), _ptr(target_ids),
+                                                _stream_handle(stream))
+    if rc != OK:
+        raise MoeVerifyError(rc, "moe_verify_greedy_head_noalloc")
+    return target_ids
 
 
 def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logits: bool = False,
