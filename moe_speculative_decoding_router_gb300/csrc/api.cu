@@ -86,7 +86,9 @@ int check(const moe_verify_config* c) {
   if (c->hidden % 64 != 0) return MOE_VERIFY_ERR_UNSUPPORTED;
   const int64_t T_max = (int64_t)c->max_batch * (c->max_k + 1);
   if (T_max > 4096) return MOE_VERIFY_ERR_UNSUPPORTED;
-  if (T_max * c->top_k > 32768) return MOE_VERIFY_ERR_UNSUPPORTED;
+  // the grouping step keeps every (token, slot) pair in one block's shared memory
+  if (mv::route_group_smem_bytes((int)T_max, c->top_k, c->n_experts) > 227 * 1024)
+    return MOE_VERIFY_ERR_UNSUPPORTED;
   return MOE_VERIFY_OK;
 }
 
@@ -238,30 +240,33 @@ struct Timed {
 
 struct StepShape {
   int T, tpb, grid_route, nch_r, nch_s, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
+  bool wr_smem;
   size_t route_smem;
 };
 
 StepShape shape_for(const moe_verify_ctx* c, int T) {
   StepShape s;
   s.T = T;
-  s.tpb = (T + c->num_sms - 1) / c->num_sms;
-  if (s.tpb < 1) s.tpb = 1;
-  if (s.tpb > 8) s.tpb = 8;
+  // tokens per routing block: 1, 2, 4 or 8, enough blocks to cover the SMs
+  const int want = (T + c->num_sms - 1) / c->num_sms;
+  s.tpb = want <= 1 ? 1 : want <= 2 ? 2 : want <= 4 ? 4 : 8;
   s.grid_route = (T + s.tpb - 1) / s.tpb;
   // routed experts see about T*k/E rows each; leave headroom for uneven load
   int avg = (int)((3LL * T * c->k + 2LL * c->E - 1) / (2LL * c->E));
   s.nch_r = round_up(avg < 16 ? 16 : avg, 16);
   if (s.nch_r > 256) s.nch_r = 256;
-  s.nch_s = round_up(T, 16);
-  if (s.nch_s > 256) s.nch_s = 256;
-  s.nch = s.nch_r > s.nch_s ? s.nch_r : s.nch_s;
-  if (c->S == 0) s.nch = s.nch_r;
+  // Shared experts see every token; they are cut into chunks of the same
+  // width, so that the shared-memory stages stay small and many of them fit
+  // (bytes in flight per SM are what keep HBM busy).
+  s.nch_s = s.nch_r;
+  s.nch = s.nch_r;
   s.stages = mv::gemm_max_stages(s.nch);
   s.n_chunks_lm = (T + 255) / 256;
   s.nch_lm = round_up((T + s.n_chunks_lm - 1) / s.n_chunks_lm, 16);
   int need = 2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm);
   s.tmem_cols = pow2_at_least(need);
-  s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, T, c->k);
+  s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E);
+  s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, T, c->k, s.wr_smem);
   return s;
 }
 
@@ -279,6 +284,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   rp.S = c->S;
   rp.V = c->V;
   rp.tpb = sh.tpb;
+  rp.wr_smem = sh.wr_smem ? 1 : 0;
   rp.eps = c->cfg.rms_eps;
   rp.src = src;
   rp.context_ids = context_ids;
@@ -543,7 +549,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
                         cudaStream_t s) {
   const int T = B * (K + 1);
   StepShape sh = shape_for(ctx, T);
-  const bool pdl = false;
+  const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
     int rc = run_layer(ctx, l, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
                        draft_ids, B, K, nullptr, probe, l, s, pdl);
@@ -625,7 +631,7 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   StepShape sh = shape_for(ctx, T);
   int rc = run_layer(ctx, layer, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
-                     false);
+                     true);
   if (rc != MOE_VERIFY_OK) return rc;
   mv::FinalParams fp = {};
   fp.T = T;
@@ -641,7 +647,7 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   fp.keys = ctx->keys;
   {
     Timed tm(ctx, 3, s);
-    CK(mv::launch_final(fp, s, false));
+    CK(mv::launch_final(fp, s, true));
   }
   return MOE_VERIFY_OK;
 }

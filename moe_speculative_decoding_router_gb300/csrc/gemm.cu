@@ -113,7 +113,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
   }
-  // everything above is independent of the previous kernel's output
+  // everything above is independent of the previous kernel's output; all
+  // global writes of this grid come after pdl_wait
+  pdl_launch_dependents();
   pdl_wait();
   const int n_items = (MODE == kLmHead) ? p.n_items_static : __ldcg(p.n_items);
   const bool has_work = (int)blockIdx.x < n_items;
@@ -396,7 +398,7 @@ size_t gemm_smem_bytes(int nch, int stages) {
 
 int gemm_max_stages(int nch) {
   const size_t budget = 227 * 1024;
-  int s = 12;
+  int s = 16;
   while (s > 2 && gemm_smem_bytes(nch, s) > budget) --s;
   return s;
 }

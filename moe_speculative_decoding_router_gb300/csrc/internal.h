@@ -29,7 +29,8 @@ enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2 };
 struct RouteParams {
   int T, B, K;          // verify tokens, sequences, drafts per sequence
   int d, E, k, S, V;
-  int tpb;              // tokens per block (1..8)
+  int tpb;              // tokens per block: 1, 2, 4 or 8
+  int wr_smem;          // 1: router weights staged in shared memory
   float eps;
   int src;              // RouteSrc
   const int32_t* context_ids;
@@ -116,7 +117,9 @@ struct AcceptParams {
 // Shared memory the GEMM kernel needs for a given item width and stage count.
 size_t gemm_smem_bytes(int nch, int stages);
 int gemm_max_stages(int nch);
-size_t route_smem_bytes(int tpb, int d, int E, int T, int k);
+size_t route_smem_bytes(int tpb, int d, int E, int T, int k, bool wr_smem);
+size_t route_group_smem_bytes(int T, int k, int E);  // the grouping step's share
+bool route_wr_fits(int tpb, int d, int E);
 
 // Launchers (enqueue only).  `pdl` requests programmatic dependent launch.
 cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl);

@@ -56,33 +56,40 @@ int scratch_address(int dev, unsigned char** out) {
   return MOE_VERIFY_OK;
 }
 
-// One warp per token: xf = bf16(h * rsqrt(mean(h^2) + eps) * g); clears the
-// argmax key and the invalid-token flag of the token, and the completion
-// counter, which must all start at zero.
+// One block of 256 threads per token: xf = bf16(h * rsqrt(mean(h^2) + eps) * g),
+// with the sum of squares reduced in the same order as the verify step's
+// final RMSNorm (per thread over 4-float chunks c = tid, tid + 256, ..., then
+// per warp, then over the warps in order), so both give the same bits.  Also
+// clears the token's argmax key and invalid flag, and the completion counter:
+// they must start at zero.
 __global__ void __launch_bounds__(256) noalloc_norm_kernel(const float* __restrict__ h,
                                                            const __nv_bfloat16* __restrict__ gain,
                                                            int T, int d, float eps,
                                                            unsigned char* scratch) {
+  __shared__ float red[8];
   __nv_bfloat16* xf = reinterpret_cast<__nv_bfloat16*>(scratch);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(scratch + kKeysOff);
   int32_t* bad = reinterpret_cast<int32_t*>(scratch + kBadOff);
   unsigned int* done = reinterpret_cast<unsigned int*>(scratch + kDoneOff);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *done = 0u;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  // same summation order as the step's final RMSNorm: float4 chunks per lane
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x;
+  if (t == 0 && tid == 0) *done = 0u;
   const float4* row = reinterpret_cast<const float4*>(h + (size_t)t * d);
   const int nc = d / 4;
   float ss = 0.f;
-  for (int c = lane; c < nc; c += 32) {
+  for (int c = tid; c < nc; c += 256) {
     const float4 v = row[c];
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float r = rsqrtf(ss / (float)d + eps);
-  for (int c = lane; c < nc; c += 32) {
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float r = rsqrtf(tot / (float)d + eps);
+  for (int c = tid; c < nc; c += 256) {
     const float4 v = row[c];
     const int i = 4 * c;
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r * __bfloat162float(gain[i]),
@@ -94,7 +101,7 @@ __global__ void __launch_bounds__(256) noalloc_norm_kernel(const float* __restri
     packed.y = *reinterpret_cast<uint32_t*>(&hi);
     reinterpret_cast<uint2*>(xf + (size_t)t * d)[c] = packed;
   }
-  if (lane == 0) {
+  if (tid == 0) {
     keys[t] = 0ull;
     bad[t] = 0;
   }
@@ -149,8 +156,8 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
     return MOE_VERIFY_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  noalloc_norm_kernel<<<(T + 7) / 8, 256, 0, s>>>(h, static_cast<const __nv_bfloat16*>(final_norm),
-                                                   T, d, rms_eps, scratch);
+  noalloc_norm_kernel<<<T, 256, 0, s>>>(h, static_cast<const __nv_bfloat16*>(final_norm), T, d,
+                                         rms_eps, scratch);
   if (cudaGetLastError() != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
 
   const int nch = (T + 15) / 16 * 16;

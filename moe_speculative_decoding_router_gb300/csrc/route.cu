@@ -46,265 +46,342 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
   return make_float4(a.x, a.y, c.x, c.y);
 }
 
-// Stage 1 for one token (one warp): build h, normalise, write xhat.
+// Residual stream entering the block for chunk c (4 floats) of token t.
 template <int SRC>
-__device__ void token_norm(const RouteParams& p, int t, float* xs) {
-  const int lane = threadIdx.x & 31;
-  const int d = p.d;
-  const int nc = d / 4;
-  float* hrow = p.h + (size_t)t * d;
-  const __nv_bfloat16* erow = nullptr;
-  if (SRC == kSrcEmbed) {
-    const int b = t / (p.K + 1), i = t % (p.K + 1);
-    int id = (i == 0) ? p.context_ids[b] : p.draft_ids[(size_t)b * p.K + (i - 1)];
-    const bool ok = (id >= 0 && id < p.V);
-    if (lane == 0) {
-      p.bad[t] = ok ? 0 : 1;
-      if (!ok) atomicOr(p.status, kErrIdRange);
-    }
-    erow = p.embed + (size_t)(ok ? id : 0) * d;
+__device__ __forceinline__ float4 residual_chunk(const RouteParams& p, int t, int c,
+                                                 const __nv_bfloat16* erow) {
+  const int d = p.d, nc = d / 4;
+  if (SRC == kSrcEmbed) return bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(erow) + c));
+  if (SRC == kSrcBf16)
+    return bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(p.h_in + (size_t)t * d) + c));
+  const int kS = p.k + p.S;
+  float4 v = reinterpret_cast<const float4*>(p.h + (size_t)t * d)[c];
+  const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * kS * d) + c;
+  // routed slots in selection order, then shared experts, summed first
+  float4 acc = yr[0];
+#pragma unroll 8
+  for (int s = 1; s < kS; ++s) {
+    const float4 u = yr[(size_t)s * nc];
+    acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
   }
-  float ss = 0.f;
-  for (int c = lane; c < nc; c += 32) {
-    float4 v;
+  v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
+  return v;
+}
+
+// Stage 1 for the block's tokens t0 .. t0+ntok-1, all threads: build h (and
+// write it back), RMSNorm, write xhat (bf16, global) and its widened values
+// to xs [ntok, d] in shared memory.
+template <int SRC, int TPB>
+__device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, float* red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = p.d, nc = d / 4;
+  float ss[TPB];
+#pragma unroll
+  for (int i = 0; i < TPB; ++i) ss[i] = 0.f;
+#pragma unroll
+  for (int tt = 0; tt < TPB; ++tt) {
+    if (tt >= ntok) break;
+    const int t = t0 + tt;
+    const __nv_bfloat16* erow = nullptr;
     if (SRC == kSrcEmbed) {
-      v = bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(erow) + c));
-    } else if (SRC == kSrcBf16) {
-      v = bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(p.h_in + (size_t)t * d) + c));
-    } else {
-      v = reinterpret_cast<const float4*>(hrow)[c];
-      const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * (p.k + p.S) * d);
-      float4 acc = yr[c];
-      for (int s = 1; s < p.k + p.S; ++s) {
-        float4 u = yr[(size_t)s * nc + c];
-        acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
+      const int b = t / (p.K + 1), i = t % (p.K + 1);
+      const int id = (i == 0) ? p.context_ids[b] : p.draft_ids[(size_t)b * p.K + (i - 1)];
+      const bool ok = (id >= 0 && id < p.V);
+      if (tid == 0) {
+        p.bad[t] = ok ? 0 : 1;
+        if (!ok) atomicOr(p.status, kErrIdRange);
       }
-      v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
+      erow = p.embed + (size_t)(ok ? id : 0) * d;
     }
-    reinterpret_cast<float4*>(hrow)[c] = v;
-    if (p.probe_hidden) reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d)[c] = v;
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    for (int c = tid; c < nc; c += kRouteThreads) {
+      const float4 v = residual_chunk<SRC>(p, t, c, erow);
+      reinterpret_cast<float4*>(p.h + (size_t)t * d)[c] = v;
+      if (p.probe_hidden) reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d)[c] = v;
+      reinterpret_cast<float4*>(xs + tt * d)[c] = v;
+      ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
   }
-  ss = warp_sum(ss);
-  const float r = rsqrtf(ss / (float)d + p.eps);
-  for (int c = lane; c < nc; c += 32) {
-    float4 v = reinterpret_cast<const float4*>(hrow)[c];
-    float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
-    __nv_bfloat16 q0 = __float2bfloat16_rn(v.x * r * g.x);
-    __nv_bfloat16 q1 = __float2bfloat16_rn(v.y * r * g.y);
-    __nv_bfloat16 q2 = __float2bfloat16_rn(v.z * r * g.z);
-    __nv_bfloat16 q3 = __float2bfloat16_rn(v.w * r * g.w);
-    __nv_bfloat162 lo = __halves2bfloat162(q0, q1), hi = __halves2bfloat162(q2, q3);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(p.xhat + (size_t)t * d)[c] = packed;
-    float4 f = make_float4(__bfloat162float(q0), __bfloat162float(q1), __bfloat162float(q2),
-                           __bfloat162float(q3));
-    reinterpret_cast<float4*>(xs)[c] = f;
+#pragma unroll
+  for (int tt = 0; tt < TPB; ++tt) {
+    if (tt >= ntok) break;
+    const float w = warp_sum(ss[tt]);
+    if (lane == 0) red[warp * 8 + tt] = w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int tt = 0; tt < TPB; ++tt) {
+    if (tt >= ntok) break;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; ++w) tot += red[w * 8 + tt];
+    const float r = rsqrtf(tot / (float)d + p.eps);
+    const int t = t0 + tt;
+    for (int c = tid; c < nc; c += kRouteThreads) {
+      float4 v = reinterpret_cast<const float4*>(xs + tt * d)[c];
+      const float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
+      __nv_bfloat16 q0 = __float2bfloat16_rn(v.x * r * g.x);
+      __nv_bfloat16 q1 = __float2bfloat16_rn(v.y * r * g.y);
+      __nv_bfloat16 q2 = __float2bfloat16_rn(v.z * r * g.z);
+      __nv_bfloat16 q3 = __float2bfloat16_rn(v.w * r * g.w);
+      __nv_bfloat162 lo = __halves2bfloat162(q0, q1), hi = __halves2bfloat162(q2, q3);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(p.xhat + (size_t)t * d)[c] = packed;
+      v = make_float4(__bfloat162float(q0), __bfloat162float(q1), __bfloat162float(q2),
+                      __bfloat162float(q3));
+      reinterpret_cast<float4*>(xs + tt * d)[c] = v;
+    }
   }
 }
 
 // Grouping by expert, run by the last block of the grid.  Expert-major rows:
 // routed expert e owns rows [off[e], off[e+1]) with its tokens in increasing
 // token order; shared expert s owns rows off[E+s] + t for every token t.
+// Shared memory: idx [T*k], per-expert token bitmasks and their prefix
+// popcounts [E][T/32], counts and offsets [E+S+1] x 3.
 __device__ void group_by_expert(const RouteParams& p, int* sm) {
   const int T = p.T, k = p.k, E = p.E, S = p.S, nE = E + S;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int* idx_s = sm;              // [T*k]
-  int* cnt_s = idx_s + T * k;   // [nE]
-  int* off_s = cnt_s + nE;      // [nE+1]
-  int* igu_s = off_s + nE + 1;  // [nE+1] item offsets, gate/up
-  int* idn_s = igu_s + nE + 1;  // [nE+1] item offsets, down
+  const int nw = (T + 31) / 32;  // bitmask words per expert
+  int* idx_s = sm;                                             // [T*k]
+  unsigned* mask = reinterpret_cast<unsigned*>(idx_s + T * k);  // [E*nw]
+  int* pre = reinterpret_cast<int*>(mask + E * nw);       // [E*nw]
+  int* cnt_s = pre + E * nw;                              // [nE]
+  int* off_s = cnt_s + nE;                                // [nE+1]
+  int* igu_s = off_s + nE + 1;                            // [nE+1] item offsets, gate/up
+  int* idn_s = igu_s + nE + 1;                            // [nE+1] item offsets, down
 
+  for (int i = tid; i < E * nw; i += kRouteThreads) mask[i] = 0u;
   for (int i = tid; i < T * k; i += kRouteThreads) {
     const int e = __ldcg(p.topk_idx + i);
     idx_s[i] = (e >= 0 && e < E) ? e : 0;
   }
-  for (int e = tid; e < nE; e += kRouteThreads) cnt_s[e] = (e < E) ? 0 : T;
   __syncthreads();
-  for (int i = tid; i < T * k; i += kRouteThreads) atomicAdd(&cnt_s[idx_s[i]], 1);
+  for (int i = tid; i < T * k; i += kRouteThreads) {
+    const int t = i / k;
+    atomicOr(&mask[idx_s[i] * nw + (t >> 5)], 1u << (t & 31));
+  }
   __syncthreads();
-  if (tid == 0) {
-    int o = 0, ig = 0, id = 0;
-    for (int e = 0; e < nE; ++e) {
-      off_s[e] = o;
-      igu_s[e] = ig;
-      idn_s[e] = id;
-      const int c = cnt_s[e];
-      const int nch = (e < E) ? p.nch_r : p.nch_s;
-      const int chunks = (c + nch - 1) / nch;
-      o += c;
-      ig += chunks * p.mt_gu;
-      id += chunks * p.mt_dn;
+  // per expert: prefix popcounts over the bitmask words, and the count
+  for (int e = tid; e < nE; e += kRouteThreads) {
+    if (e < E) {
+      int run = 0;
+      for (int w = 0; w < nw; ++w) {
+        pre[e * nw + w] = run;
+        run += __popc(mask[e * nw + w]);
+      }
+      cnt_s[e] = run;
+    } else {
+      cnt_s[e] = T;
     }
-    off_s[nE] = o;
-    igu_s[nE] = ig;
-    idn_s[nE] = id;
-    p.n_items[0] = ig;
-    p.n_items[1] = id;
+  }
+  __syncthreads();
+  // exclusive scans over experts of rows, gate/up items and down items: one
+  // warp, 32 experts per round, shuffle scans with a running carry
+  if (warp == 0) {
+    int co = 0, cg = 0, cd = 0;
+    for (int e0 = 0; e0 < nE; e0 += 32) {
+      const int e = e0 + lane;
+      int c = 0, ng = 0, nd = 0;
+      if (e < nE) {
+        c = cnt_s[e];
+        const int nch = (e < E) ? p.nch_r : p.nch_s;
+        const int chunks = (c + nch - 1) / nch;
+        ng = chunks * p.mt_gu;
+        nd = chunks * p.mt_dn;
+      }
+      int ic = c, ig = ng, id = nd;  // inclusive scans
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ic, o);
+        const int b = __shfl_up_sync(0xffffffffu, ig, o);
+        const int f = __shfl_up_sync(0xffffffffu, id, o);
+        if (lane >= o) {
+          ic += a;
+          ig += b;
+          id += f;
+        }
+      }
+      if (e < nE) {
+        off_s[e] = co + ic - c;
+        igu_s[e] = cg + ig - ng;
+        idn_s[e] = cd + id - nd;
+      }
+      co += __shfl_sync(0xffffffffu, ic, 31);
+      cg += __shfl_sync(0xffffffffu, ig, 31);
+      cd += __shfl_sync(0xffffffffu, id, 31);
+    }
+    if (lane == 0) {
+      off_s[nE] = co;
+      igu_s[nE] = cg;
+      idn_s[nE] = cd;
+      p.n_items[0] = cg;
+      p.n_items[1] = cd;
+    }
   }
   __syncthreads();
   for (int e = tid; e <= nE; e += kRouteThreads) p.expert_off[e] = off_s[e];
 
-  // stable positions of routed (token, slot) pairs
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int e = warp; e < E; e += kRouteWarps) {
-    int running = off_s[e];
-    for (int c0 = 0; c0 < T; c0 += 32) {
-      const int t = c0 + lane;
-      int jf = -1;
-      if (t < T) {
-        for (int j = 0; j < k; ++j)
-          if (idx_s[t * k + j] == e) jf = j;
-      }
-      const unsigned ballot = __ballot_sync(0xffffffffu, jf >= 0);
-      if (jf >= 0) {
-        const int pos = running + __popc(ballot & lt_mask);
-        p.perm_token[pos] = t;
-        p.perm_slot[pos] = jf;
-        p.perm_w[pos] = __ldcg(p.topk_w + (size_t)t * k + jf);
-      }
-      running += __popc(ballot);
-    }
+  // row of each routed (token, slot): the expert's offset plus the number of
+  // its tokens before t (prefix popcount of its bitmask)
+  for (int i = tid; i < T * k; i += kRouteThreads) {
+    const int t = i / k, j = i - t * k;
+    const int e = idx_s[i];
+    const int w = t >> 5;
+    const int pos = off_s[e] + pre[e * nw + w] +
+                    __popc(mask[e * nw + w] & ((1u << (t & 31)) - 1u));
+    p.perm_token[pos] = t;
+    p.perm_slot[pos] = j;
+    p.perm_w[pos] = __ldcg(p.topk_w + i);
   }
   for (int i = tid; i < S * T; i += kRouteThreads) {
-    const int s = i / T, t = i % T;
+    const int s = i / T, t = i - s * T;
     const int pos = off_s[E + s] + t;
     p.perm_token[pos] = t;
     p.perm_slot[pos] = k + s;
     p.perm_w[pos] = 1.0f;
   }
-  // work items, expert-major; the tiles of one expert sit next to each other
-  for (int e = tid; e < nE; e += kRouteThreads) {
-    const int c = cnt_s[e];
-    const int nch = (e < E) ? p.nch_r : p.nch_s;
-    const int chunks = (c + nch - 1) / nch;
-    for (int ch = 0; ch < chunks; ++ch) {
-      const int n = min(nch, c - ch * nch);
-      const int brow = off_s[e] + ch * nch;
-      for (int mt = 0; mt < p.mt_gu; ++mt) {
-        Item it;
-        it.a_row = p.a_base_gu + (e * p.mt_gu + mt) * 128;
-        it.b_row = brow;
-        it.n = n;
-        it.aux = mt;
-        p.items_gu[igu_s[e] + ch * p.mt_gu + mt] = it;
-      }
-      for (int mt = 0; mt < p.mt_dn; ++mt) {
-        Item it;
-        it.a_row = p.a_base_dn + (e * p.mt_dn + mt) * 128;
-        it.b_row = brow;
-        it.n = n;
-        it.aux = mt;
-        p.items_dn[idn_s[e] + ch * p.mt_dn + mt] = it;
-      }
+  // work items, one thread each; expert-major, so the tiles of one expert
+  // sit next to each other
+  const int n_gu = igu_s[nE], n_all = n_gu + idn_s[nE];
+  for (int i = tid; i < n_all; i += kRouteThreads) {
+    const bool gu = i < n_gu;
+    const int r = gu ? i : i - n_gu;
+    const int* io = gu ? igu_s : idn_s;
+    int lo = 0, hi = nE - 1;  // last expert with io[e] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (io[mid] <= r) lo = mid; else hi = mid - 1;
     }
+    const int e = lo;
+    const int mt_n = gu ? p.mt_gu : p.mt_dn;
+    const int q = r - io[e];
+    const int ch = q / mt_n, mt = q - ch * mt_n;
+    const int nch = (e < E) ? p.nch_r : p.nch_s;
+    Item it;
+    it.a_row = (gu ? p.a_base_gu : p.a_base_dn) + (e * mt_n + mt) * 128;
+    it.b_row = off_s[e] + ch * nch;
+    it.n = min(nch, cnt_s[e] - ch * nch);
+    it.aux = mt;
+    (gu ? p.items_gu : p.items_dn)[r] = it;
   }
 }
 
-template <int SRC>
+template <int SRC, int TPB>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
-  extern __shared__ __align__(16) float rsm[];
+  extern __shared__ __align__(128) float rsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = p.d, E = p.E, tpb = p.tpb;
+  const int d = p.d, E = p.E, tpb = TPB;
   const int t0 = blockIdx.x * tpb;
-  float* xs = rsm;              // [tpb, d]  normalised input, bf16 values widened
-  float* zs = rsm + tpb * d;    // [tpb, E]  router logits
+  const int ntok = min(tpb, p.T - t0);
+  // shared memory: [router weights E x d bf16, when staged] [xs tpb x d] [zs tpb x E] [red 64]
+  const size_t wr_bytes = p.wr_smem ? (size_t)E * d * 2 : 0;
+  __nv_bfloat16* wr_s = reinterpret_cast<__nv_bfloat16*>(rsm);
+  float* xs = reinterpret_cast<float*>(reinterpret_cast<char*>(rsm) + wr_bytes);
+  float* zs = xs + tpb * d;
+  float* red = zs + tpb * E;
+  __shared__ __align__(8) uint64_t wr_bar;
+  __shared__ int abort_flag;
 
+  // The router weights do not depend on earlier kernels: start their copy
+  // into shared memory before waiting for the previous kernel.
+  if (p.wr_smem && threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&wr_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&wr_bar, (uint32_t)wr_bytes);
+    const char* src = reinterpret_cast<const char*>(p.Wr);
+    char* dst = reinterpret_cast<char*>(wr_s);
+    for (size_t off = 0; off < wr_bytes; off += 16384) {
+      const uint32_t n = (uint32_t)min((size_t)16384, wr_bytes - off);
+      bulk_load(dst + off, src + off, n, &wr_bar);
+    }
+  }
+  // dependents may start their own prologue now; every global write below
+  // comes after pdl_wait, so they cannot disturb what this grid still reads
+  pdl_launch_dependents();
   pdl_wait();
-  if (warp < tpb && t0 + warp < p.T) token_norm<SRC>(p, t0 + warp, xs + warp * d);
+  block_norm<SRC, TPB>(p, t0, ntok, xs, red);
   __syncthreads();
+  bool wr_ok = true;
+  if (p.wr_smem) wr_ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
 
-  // router logits: warp w computes experts w, w+8, ... for every token of the block
-  for (int e = warp; e < E; e += kRouteWarps) {
-    const uint4* wrow = reinterpret_cast<const uint4*>(p.Wr + (size_t)e * d);
-    float acc[8];
+  // router logits: warp w computes experts 8w .. 8w+7 (then + 64, ...) for
+  // every token of the block, eight independent accumulation chains per lane
+  const __nv_bfloat16* wsrc = p.wr_smem ? wr_s : p.Wr;
+  for (int e0 = warp * 8; e0 < E && wr_ok; e0 += kRouteWarps * 8) {
+    float acc[8][TPB];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int tt = 0; tt < TPB; ++tt) acc[j][tt] = 0.f;
     for (int c = lane; c < d / 8; c += 32) {
-      float w8[8];
-      unpack8(__ldg(wrow + c), w8);
+      float4 xa[TPB], xb[TPB];
 #pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        if (tt < tpb) {
-          const float4* x4 = reinterpret_cast<const float4*>(xs + tt * d + c * 8);
-          const float4 xa = x4[0], xb = x4[1];
-          float a = acc[tt];
-          a = fmaf(w8[0], xa.x, a);
-          a = fmaf(w8[1], xa.y, a);
-          a = fmaf(w8[2], xa.z, a);
-          a = fmaf(w8[3], xa.w, a);
-          a = fmaf(w8[4], xb.x, a);
-          a = fmaf(w8[5], xb.y, a);
-          a = fmaf(w8[6], xb.z, a);
-          a = fmaf(w8[7], xb.w, a);
-          acc[tt] = a;
+      for (int tt = 0; tt < TPB; ++tt) {
+        const float4* x4 = reinterpret_cast<const float4*>(xs + tt * d + c * 8);
+        xa[tt] = x4[0];
+        xb[tt] = x4[1];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = min(e0 + j, E - 1);
+        const uint4* wrow = reinterpret_cast<const uint4*>(wsrc + (size_t)e * d);
+        float w8[8];
+        unpack8(p.wr_smem ? wrow[c] : __ldg(wrow + c), w8);
+#pragma unroll
+        for (int tt = 0; tt < TPB; ++tt) {
+          float a = acc[j][tt];
+          a = fmaf(w8[0], xa[tt].x, a);
+          a = fmaf(w8[1], xa[tt].y, a);
+          a = fmaf(w8[2], xa[tt].z, a);
+          a = fmaf(w8[3], xa[tt].w, a);
+          a = fmaf(w8[4], xb[tt].x, a);
+          a = fmaf(w8[5], xb[tt].y, a);
+          a = fmaf(w8[6], xb[tt].z, a);
+          a = fmaf(w8[7], xb[tt].w, a);
+          acc[j][tt] = a;
         }
       }
     }
-    const float b = p.bias ? __ldg(p.bias + e) : 0.f;
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
-      if (tt < tpb) {
-        const float z = warp_sum(acc[tt]);
-        if (lane == 0) zs[tt * E + e] = z + b;
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + j;
+#pragma unroll
+      for (int tt = 0; tt < TPB; ++tt) {
+        const float z = warp_sum(acc[j][tt]);
+        if (lane == 0 && e < E) zs[tt * E + e] = z + (p.bias ? __ldg(p.bias + e) : 0.f);
       }
     }
   }
   __syncthreads();
 
-  // softmax and top-k: one warp per token, lane holds experts lane + 32 j
-  if (warp < tpb && t0 + warp < p.T) {
+  // softmax and top-k, one warp per token.  Rank of expert e = number of
+  // experts ordered before it by (z desc, index asc); the experts of rank < k
+  // are the selection, written in rank order.
+  if (warp < ntok && wr_ok) {
     const int t = t0 + warp;
     const float* z = zs + warp * E;
-    float zl[8];
     float m = -FLT_MAX;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane + 32 * j;
-      zl[j] = (e < E) ? z[e] : -FLT_MAX;
-      m = fmaxf(m, zl[j]);
-    }
+    for (int e = lane; e < E; e += 32) m = fmaxf(m, z[e]);
     m = warp_max(m);
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (lane + 32 * j < E) s += __expf(zl[j] - m);
-    s = warp_sum(s);
-    unsigned taken = 0;
-    for (int r = 0; r < p.k; ++r) {
-      float bv = -FLT_MAX;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (zl[j] > bv || (zl[j] == bv && e < be))) {
-          bv = zl[j];
-          be = e;
-        }
+    float sum = 0.f;
+    for (int e = lane; e < E; e += 32) sum += __expf(z[e] - m);
+    sum = warp_sum(sum);
+    for (int e = lane; e < E; e += 32) {
+      const float ze = z[e];
+      int rank = 0;
+      for (int f = 0; f < E; ++f) {
+        const float zf = z[f];
+        rank += (zf > ze || (zf == ze && f < e)) ? 1 : 0;
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be < 0 || be >= E) {  // only reachable with non-finite logits
-        if (lane == 0) atomicOr(p.status, kErrInternal);
-        be = r;
-        bv = zl[0];
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) {
-        const float w = __expf(bv - m) / s;
-        p.topk_idx[(size_t)t * p.k + r] = be;
-        p.topk_w[(size_t)t * p.k + r] = w;
-        if (p.probe_idx) p.probe_idx[(size_t)t * p.k + r] = be;
-        if (p.probe_w) p.probe_w[(size_t)t * p.k + r] = w;
+      if (rank < p.k) {
+        const float w = __expf(ze - m) / sum;
+        p.topk_idx[(size_t)t * p.k + rank] = e;
+        p.topk_w[(size_t)t * p.k + rank] = w;
+        if (p.probe_idx) p.probe_idx[(size_t)t * p.k + rank] = e;
+        if (p.probe_w) p.probe_w[(size_t)t * p.k + rank] = w;
       }
     }
   }
@@ -325,6 +402,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
                                                       const __nv_bfloat16* __restrict__ xhat,
                                                       __nv_bfloat16* __restrict__ xperm, int rows,
                                                       int d) {
+  pdl_launch_dependents();
   pdl_wait();
   const int cpr = d / 8;  // 16-byte chunks per row
   const int64_t total = (int64_t)rows * cpr;
@@ -338,21 +416,26 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
 }
 
 // Residual update after the last block, then either the final RMSNorm (the
-// lm_head input) or the bf16 output of the single-block entry point.
+// lm_head input) or the bf16 output of the single-block entry point.  One
+// token per block; the sum of squares is reduced per thread over its 4-float
+// chunks (c = tid, tid + 256, ...), then per warp, then over the warps in
+// order (the allocation-free greedy head reduces in the same order).
 __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
+  pdl_launch_dependents();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= p.T) return;
+  __shared__ float red[8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x;
   const int d = p.d, nc = d / 4;
   float* hrow = p.h + (size_t)t * d;
   const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * p.kS * d);
   float ss = 0.f;
-  for (int c = lane; c < nc; c += 32) {
+  for (int c = tid; c < nc; c += 256) {
     float4 v = reinterpret_cast<const float4*>(hrow)[c];
     float4 acc = yr[c];
+#pragma unroll 8
     for (int s = 1; s < p.kS; ++s) {
-      float4 u = yr[(size_t)s * nc + c];
+      const float4 u = yr[(size_t)s * nc + c];
       acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
     }
     v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
@@ -369,10 +452,15 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
   }
   if (p.mode == 1) return;
   ss = warp_sum(ss);
-  const float r = rsqrtf(ss / (float)d + p.eps);
-  for (int c = lane; c < nc; c += 32) {
-    float4 v = reinterpret_cast<const float4*>(hrow)[c];
-    float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float r = rsqrtf(tot / (float)d + p.eps);
+  for (int c = tid; c < nc; c += 256) {
+    const float4 v = reinterpret_cast<const float4*>(hrow)[c];
+    const float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r * g.x, v.y * r * g.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * r * g.z, v.w * r * g.w);
     uint2 packed;
@@ -380,7 +468,7 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
     packed.y = *reinterpret_cast<uint32_t*>(&hi);
     reinterpret_cast<uint2*>(p.out + (size_t)t * d)[c] = packed;
   }
-  if (lane == 0) p.keys[t] = 0ull;
+  if (tid == 0) p.keys[t] = 0ull;
 }
 
 template <typename Kern, typename... Args>
@@ -401,29 +489,45 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStrea
 
 }  // namespace
 
-size_t route_smem_bytes(int tpb, int d, int E, int T, int k) {
-  const size_t a = (size_t)tpb * (d + E) * sizeof(float);
-  const size_t b = ((size_t)T * k + 4 * 300) * sizeof(int);
+size_t route_group_smem_bytes(int T, int k, int E) {
+  const size_t nw = ((size_t)T + 31) / 32;
+  return ((size_t)T * k + 2 * (size_t)E * nw + 4 * 300) * sizeof(int);
+}
+
+size_t route_smem_bytes(int tpb, int d, int E, int T, int k, bool wr_smem) {
+  const size_t a = (wr_smem ? (size_t)E * d * 2 : 0) + ((size_t)tpb * (d + E) + 64) * sizeof(float);
+  const size_t b = route_group_smem_bytes(T, k, E);
   return a > b ? a : b;
+}
+
+bool route_wr_fits(int tpb, int d, int E) {
+  return (size_t)E * d * 2 + ((size_t)tpb * (d + E) + 64) * sizeof(float) <= 220 * 1024;
+}
+
+template <int SRC, int TPB>
+cudaError_t launch_route_t(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  auto k = route_kernel<SRC, TPB>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, p);
+}
+
+template <int SRC>
+cudaError_t launch_route_src(const RouteParams& p, int grid, size_t smem, cudaStream_t s,
+                             bool pdl) {
+  switch (p.tpb) {
+    case 1: return launch_route_t<SRC, 1>(p, grid, smem, s, pdl);
+    case 2: return launch_route_t<SRC, 2>(p, grid, smem, s, pdl);
+    case 4: return launch_route_t<SRC, 4>(p, grid, smem, s, pdl);
+    default: return launch_route_t<SRC, 8>(p, grid, smem, s, pdl);
+  }
 }
 
 cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
   switch (p.src) {
-    case kSrcEmbed: {
-      auto k = route_kernel<kSrcEmbed>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, p);
-    }
-    case kSrcBf16: {
-      auto k = route_kernel<kSrcBf16>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, p);
-    }
-    default: {
-      auto k = route_kernel<kSrcCombine>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, p);
-    }
+    case kSrcEmbed: return launch_route_src<kSrcEmbed>(p, grid, smem, s, pdl);
+    case kSrcBf16: return launch_route_src<kSrcBf16>(p, grid, smem, s, pdl);
+    default: return launch_route_src<kSrcCombine>(p, grid, smem, s, pdl);
   }
 }
 
@@ -438,7 +542,7 @@ cudaError_t launch_scatter(const int32_t* perm_token, const __nv_bfloat16* xhat,
 }
 
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl) {
-  const int grid = (p.T + 7) / 8;
+  const int grid = p.T;
   return launch_ex(final_kernel, dim3(grid), dim3(256), 0, s, pdl, p);
 }
 
