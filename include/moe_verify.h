@@ -195,12 +195,14 @@ MOE_VERIFY_API uint64_t moe_verify_device_bytes(const moe_verify_config* config)
 
 /* Per-launch time of the library's kernel families, for profiling.
  * moe_verify_set_timing(ctx, 1) makes later steps record CUDA events around
- * each launch of the grouped expert GEMMs and of the lm_head kernel on the
- * step's stream (this breaks graph capture: use it outside capture only).
- * moe_verify_get_timing synchronises and reports the sums since the last
- * reset, in milliseconds, and the launch counts:
- *   ms[0], n[0]: gate/up + SwiGLU GEMM   ms[1], n[1]: down + combine GEMM
- *   ms[2], n[2]: lm_head + argmax        ms[3], n[3]: routing kernels
+ * each launch of the library's kernels on the step's stream (this breaks
+ * graph capture and the overlap of consecutive kernels: use it outside
+ * capture, for per-kernel times only).  moe_verify_get_timing synchronises
+ * and reports the sums since the last reset, in milliseconds, and the launch
+ * counts:
+ *   ms[0], n[0]: expert FFN (gate/up + SwiGLU + down + weighted combine)
+ *   ms[1], n[1]: unused (0)
+ *   ms[2], n[2]: lm_head + argmax        ms[3], n[3]: routing + final RMSNorm
  * reset != 0 clears the sums afterwards. */
 MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
 MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] host*/, int64_t* n /*[4] host*/,

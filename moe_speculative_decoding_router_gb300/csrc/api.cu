@@ -2,6 +2,7 @@
 // library-owned weights and workspace, TMA descriptors and the launch order
 // of one verify step.
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <new>
@@ -10,7 +11,6 @@
 #include "../../include/moe_verify.h"
 #include "internal.h"
 
-using mv::Item;
 
 struct TimingPair {
   int family;
@@ -22,7 +22,7 @@ struct moe_verify_ctx {
   int device = 0, num_sms = 0;
   int L = 0, d = 0, E = 0, k = 0, S = 0, I = 0, Is = 0, V = 0;
   int nE = 0, kS = 0, I_pad = 0, d_pad = 0, V_pad = 0, mt_gu = 0, mt_dn = 0;
-  int T_max = 0, rows_max = 0, items_cap = 0;
+  int T_max = 0, rows_max = 0, chunks_cap = 0;
   // library-owned weights
   __nv_bfloat16 *w_gu = nullptr, *w_dn = nullptr, *w_lm = nullptr, *embed = nullptr,
                 *router = nullptr;
@@ -31,12 +31,11 @@ struct moe_verify_ctx {
   // workspace
   float* h = nullptr;
   float* y = nullptr;
-  __nv_bfloat16 *xhat = nullptr, *xperm = nullptr, *abuf = nullptr, *xf = nullptr;
-  int32_t *topk_idx = nullptr, *bad = nullptr, *perm_token = nullptr, *perm_slot = nullptr,
-          *expert_off = nullptr, *n_items = nullptr;
-  float *topk_w = nullptr, *perm_w = nullptr;
-  Item *items_gu = nullptr, *items_dn = nullptr;
-  unsigned int *done_route = nullptr, *done_lm = nullptr;
+  __nv_bfloat16 *xperm = nullptr, *abuf = nullptr, *xf = nullptr;
+  int32_t *bad = nullptr, *perm_token = nullptr, *perm_slot = nullptr, *cnt = nullptr,
+          *dep = nullptr;
+  float* perm_w = nullptr;
+  unsigned int *done_ffn = nullptr, *done_lm = nullptr;
   unsigned long long* keys = nullptr;
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
@@ -68,7 +67,7 @@ int pow2_at_least(int x) {
 }
 
 struct Derived {
-  int nE, kS, I_pad, d_pad, V_pad, mt_gu, mt_dn, T_max, rows_max, items_cap;
+  int nE, kS, I_pad, d_pad, V_pad, mt_gu, mt_dn, T_max, rows_max, chunks_cap;
 };
 
 int check(const moe_verify_config* c) {
@@ -86,8 +85,10 @@ int check(const moe_verify_config* c) {
   if (c->hidden % 64 != 0) return MOE_VERIFY_ERR_UNSUPPORTED;
   const int64_t T_max = (int64_t)c->max_batch * (c->max_k + 1);
   if (T_max > 4096) return MOE_VERIFY_ERR_UNSUPPORTED;
-  // the grouping step keeps every (token, slot) pair in one block's shared memory
-  if (mv::route_group_smem_bytes((int)T_max, c->top_k, c->n_experts) > 227 * 1024)
+  // a routing block must hold eight tokens' rows when the router weights do
+  // not fit in shared memory
+  if (mv::route_smem_bytes(8, c->hidden, c->n_experts, c->top_k, c->n_shared, false) >
+      227 * 1024)
     return MOE_VERIFY_ERR_UNSUPPORTED;
   return MOE_VERIFY_OK;
 }
@@ -103,17 +104,16 @@ Derived derive(const moe_verify_config* c) {
   r.mt_gu = r.I_pad / 64;
   r.mt_dn = r.d_pad / 128;
   r.T_max = c->max_batch * (c->max_k + 1);
-  r.rows_max = r.T_max * r.kS;
+  r.rows_max = r.T_max * r.nE;  // expert e owns rows [e*T, e*T + count_e)
   // chunks per layer are at most T*k/16 + E (routed) plus S*(T/16 + 1) (shared)
   const int chunks = r.T_max * c->top_k / 16 + c->n_experts + c->n_shared * (r.T_max / 16 + 1);
-  const int mt = r.mt_gu > r.mt_dn ? r.mt_gu : r.mt_dn;
-  r.items_cap = chunks * mt;
+  r.chunks_cap = chunks;
   return r;
 }
 
 struct Sizes {
   uint64_t w_gu, w_dn, w_lm, embed, router, gain, final_gain, bias;
-  uint64_t h, y, xhat, xperm, abuf, xf, topk_idx, topk_w, bad, perm, expert_off, items, keys, io;
+  uint64_t h, y, xperm, abuf, xf, bad, perm, cnt, dep, keys, io;
 };
 
 Sizes sizes(const moe_verify_config* c, const Derived& r) {
@@ -129,16 +129,13 @@ Sizes sizes(const moe_verify_config* c, const Derived& r) {
   s.bias = L * E * 4;
   s.h = (uint64_t)r.T_max * d * 4;
   s.y = (uint64_t)r.T_max * r.kS * d * 4;
-  s.xhat = (uint64_t)r.T_max * d * 2;
   s.xperm = (uint64_t)r.rows_max * d * 2;
   s.abuf = (uint64_t)r.rows_max * r.I_pad * 2;
   s.xf = (uint64_t)round_up(r.T_max, 16) * d * 2;
-  s.topk_idx = (uint64_t)r.T_max * c->top_k * 4;
-  s.topk_w = s.topk_idx;
   s.bad = (uint64_t)r.T_max * 4;
   s.perm = (uint64_t)r.rows_max * 4;
-  s.expert_off = (uint64_t)(r.nE + 1) * 4;
-  s.items = (uint64_t)r.items_cap * sizeof(Item);
+  s.cnt = (uint64_t)c->n_experts * 4;
+  s.dep = (uint64_t)r.chunks_cap * 4;
   s.keys = (uint64_t)r.T_max * 8;
   s.io = (uint64_t)r.T_max * 4;
   return s;
@@ -146,8 +143,8 @@ Sizes sizes(const moe_verify_config* c, const Derived& r) {
 
 uint64_t total_bytes(const Sizes& s) {
   return s.w_gu + s.w_dn + s.w_lm + s.embed + s.router + s.gain + s.final_gain + s.bias + s.h +
-         s.y + s.xhat + s.xperm + s.abuf + s.xf + s.topk_idx + s.topk_w + s.bad + 3 * s.perm +
-         s.expert_off + 2 * s.items + s.keys + 5 * s.io + 64;
+         s.y + s.xperm + s.abuf + s.xf + s.bad + 3 * s.perm + s.cnt + s.dep + s.keys + 5 * s.io +
+         64;
 }
 
 template <typename T>
@@ -239,7 +236,7 @@ struct Timed {
 // --------------------------------------------------------------- launches
 
 struct StepShape {
-  int T, tpb, grid_route, nch_r, nch_s, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
+  int T, tpb, grid_route, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
   bool wr_smem;
   size_t route_smem;
 };
@@ -251,22 +248,20 @@ StepShape shape_for(const moe_verify_ctx* c, int T) {
   const int want = (T + c->num_sms - 1) / c->num_sms;
   s.tpb = want <= 1 ? 1 : want <= 2 ? 2 : want <= 4 ? 4 : 8;
   s.grid_route = (T + s.tpb - 1) / s.tpb;
-  // routed experts see about T*k/E rows each; leave headroom for uneven load
+  // routed experts see about T*k/E rows each; leave headroom for uneven load.
+  // Shared experts (every token) are cut into chunks of the same width, so
+  // that the shared-memory stages stay small and many of them fit (bytes in
+  // flight per SM are what keep HBM busy).
   int avg = (int)((3LL * T * c->k + 2LL * c->E - 1) / (2LL * c->E));
-  s.nch_r = round_up(avg < 16 ? 16 : avg, 16);
-  if (s.nch_r > 256) s.nch_r = 256;
-  // Shared experts see every token; they are cut into chunks of the same
-  // width, so that the shared-memory stages stay small and many of them fit
-  // (bytes in flight per SM are what keep HBM busy).
-  s.nch_s = s.nch_r;
-  s.nch = s.nch_r;
+  s.nch = round_up(avg < 16 ? 16 : avg, 16);
+  if (s.nch > 256) s.nch = 256;
   s.stages = mv::gemm_max_stages(s.nch);
   s.n_chunks_lm = (T + 255) / 256;
   s.nch_lm = round_up((T + s.n_chunks_lm - 1) / s.n_chunks_lm, 16);
   int need = 2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm);
   s.tmem_cols = pow2_at_least(need);
-  s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E);
-  s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, T, c->k, s.wr_smem);
+  s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E, c->k, c->S);
+  s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, c->k, c->S, s.wr_smem);
   return s;
 }
 
@@ -296,9 +291,6 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   rp.gain = c->gain + (size_t)l * c->d;
   rp.Wr = c->router + (size_t)l * c->E * c->d;
   rp.bias = c->has_bias ? c->bias + (size_t)l * c->E : nullptr;
-  rp.xhat = c->xhat;
-  rp.topk_idx = c->topk_idx;
-  rp.topk_w = c->topk_w;
   rp.bad = c->bad;
   rp.status = c->status;
   if (probe) {
@@ -306,56 +298,44 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
     if (probe->topk_w) rp.probe_w = probe->topk_w + (size_t)probe_layer * T * c->k;
     if (probe->hidden) rp.probe_hidden = probe->hidden + (size_t)probe_layer * T * c->d;
   }
+  rp.cnt = c->cnt;
+  rp.xperm = c->xperm;
   rp.perm_token = c->perm_token;
   rp.perm_slot = c->perm_slot;
   rp.perm_w = c->perm_w;
-  rp.expert_off = c->expert_off;
-  rp.items_gu = c->items_gu;
-  rp.items_dn = c->items_dn;
-  rp.n_items = c->n_items;
-  rp.nch_r = sh.nch_r;
-  rp.nch_s = sh.nch_s;
-  rp.mt_gu = c->mt_gu;
-  rp.mt_dn = c->mt_dn;
-  rp.a_base_gu = l * c->nE * c->mt_gu * 128;
-  rp.a_base_dn = l * c->nE * c->mt_dn * 128;
-  rp.done = c->done_route;
   {
     Timed tm(c, 3, s);
     CK(mv::launch_route(rp, sh.grid_route, sh.route_smem, s, pdl));
-    CK(mv::launch_scatter(c->perm_token, c->xhat, c->xperm, T * c->kS, c->d, s, pdl));
   }
-  mv::GemmParams gp = {};
-  gp.items = c->items_gu;
-  gp.n_items = c->n_items;
-  gp.kblocks = c->d / 64;
-  gp.nch = sh.nch;
-  gp.stages = sh.stages;
-  gp.tmem_cols = sh.tmem_cols;
-  gp.status = c->status;
-  gp.a_out = c->abuf;
-  gp.I_pad = c->I_pad;
+  mv::FfnParams fp = {};
+  fp.cnt = c->cnt;
+  fp.cnt_clear = c->cnt;
+  fp.dep = c->dep;
+  fp.E = c->E;
+  fp.S = c->S;
+  fp.T = T;
+  fp.nch = sh.nch;
+  fp.mt_gu = c->mt_gu;
+  fp.mt_dn = c->mt_dn;
+  fp.kb_gu = c->d / 64;
+  fp.kb_dn = c->I_pad / 64;
+  fp.a_base_gu = l * c->nE * c->mt_gu * 128;
+  fp.a_base_dn = l * c->nE * c->mt_dn * 128;
+  fp.stages = sh.stages;
+  fp.tmem_cols = sh.tmem_cols;
+  fp.a_out = c->abuf;
+  fp.I_pad = c->I_pad;
+  fp.perm_token = c->perm_token;
+  fp.perm_slot = c->perm_slot;
+  fp.perm_w = c->perm_w;
+  fp.y = c->y;
+  fp.d = c->d;
+  fp.kS = c->kS;
+  fp.status = c->status;
+  fp.done = c->done_ffn;
   {
     Timed tm(c, 0, s);
-    CK(mv::launch_gemm(mv::kGateUp, c->map_gu, c->map_x, gp, c->num_sms, s, pdl));
-  }
-  mv::GemmParams gd = {};
-  gd.items = c->items_dn;
-  gd.n_items = c->n_items + 1;
-  gd.kblocks = c->I_pad / 64;
-  gd.nch = sh.nch;
-  gd.stages = sh.stages;
-  gd.tmem_cols = sh.tmem_cols;
-  gd.status = c->status;
-  gd.perm_token = c->perm_token;
-  gd.perm_slot = c->perm_slot;
-  gd.perm_w = c->perm_w;
-  gd.y = c->y;
-  gd.d = c->d;
-  gd.kS = c->kS;
-  {
-    Timed tm(c, 1, s);
-    CK(mv::launch_gemm(mv::kDown, c->map_dn, c->map_a, gd, c->num_sms, s, pdl));
+    CK(mv::launch_ffn(c->map_gu, c->map_x, c->map_dn, c->map_a, fp, c->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -435,7 +415,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   c->mt_dn = r.mt_dn;
   c->T_max = r.T_max;
   c->rows_max = r.rows_max;
-  c->items_cap = r.items_cap;
+  c->chunks_cap = r.chunks_cap;
   Sizes z = sizes(config, r);
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
 
@@ -465,21 +445,16 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   AL(c->bias, z.bias);
   AL(c->h, z.h);
   AL(c->y, z.y);
-  AL(c->xhat, z.xhat);
   AL(c->xperm, z.xperm);
   AL(c->abuf, z.abuf);
   AL(c->xf, z.xf);
-  AL(c->topk_idx, z.topk_idx);
-  AL(c->topk_w, z.topk_w);
   AL(c->bad, z.bad);
   AL(c->perm_token, z.perm);
   AL(c->perm_slot, z.perm);
   AL(c->perm_w, z.perm);
-  AL(c->expert_off, z.expert_off);
-  AL(c->items_gu, z.items);
-  AL(c->items_dn, z.items);
-  AL(c->n_items, 16);
-  AL(c->done_route, 16);
+  AL(c->cnt, z.cnt);
+  AL(c->dep, z.dep);
+  AL(c->done_ffn, 16);
   AL(c->done_lm, 16);
   AL(c->keys, z.keys);
   AL(c->status, 16);
@@ -494,8 +469,9 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   CKF(cudaMemsetAsync(c->xperm, 0, z.xperm, s));
   CKF(cudaMemsetAsync(c->abuf, 0, z.abuf, s));
   CKF(cudaMemsetAsync(c->xf, 0, z.xf, s));
-  CKF(cudaMemsetAsync(c->n_items, 0, 16, s));
-  CKF(cudaMemsetAsync(c->done_route, 0, 16, s));
+  CKF(cudaMemsetAsync(c->cnt, 0, z.cnt, s));
+  CKF(cudaMemsetAsync(c->dep, 0, z.dep, s));
+  CKF(cudaMemsetAsync(c->done_ffn, 0, 16, s));
   CKF(cudaMemsetAsync(c->done_lm, 0, 16, s));
   CKF(cudaMemsetAsync(c->status, 0, 16, s));
   CKF(cudaMemsetAsync(c->bias, 0, z.bias, s));
@@ -589,7 +565,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   gp.done = ctx->done_lm;
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_gemm(mv::kLmHead, ctx->map_lm, ctx->map_f, gp, ctx->num_sms, s, pdl));
+    CK(mv::launch_lmhead(ctx->map_lm, ctx->map_f, gp, ctx->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }

@@ -1,20 +1,23 @@
 // Grouped GEMMs of the verify step on the 5th-generation tensor cores.
 //
-// One persistent kernel shape serves three products:
-//   kGateUp  [tile of 64 gate rows + 64 up rows of one expert] x [its tokens]
-//            epilogue: a = bf16(silu(g) * u)                (SwiGLU)
-//   kDown    [128 rows of one expert's down projection] x [its tokens' a]
-//            epilogue: y[token, slot] = p * (a W_d^T)        (weighted combine)
-//   kLmHead  [128 vocabulary rows] x [all verify tokens]
-//            epilogue: running argmax over the vocabulary     (greedy choice)
+// ffn_kernel: one layer's expert FFN in one persistent launch.  Work items:
+//   gate/up  [64 gate rows + 64 up rows of one expert] x [<= nch of its rows]
+//            epilogue a = bf16(silu(g) * u)                  (SwiGLU)
+//   down     [128 rows of one expert's down projection] x [the same rows' a]
+//            epilogue y[token, slot] = p * (a W_d^T)         (weighted combine)
+// All gate/up items come first, then all down items; item i runs on CTA
+// i mod gridDim.  A down item waits (bounded) until both SwiGLU halves of
+// every gate/up tile of its chunk of rows are written.
+// lmhead_kernel: [128 vocabulary rows] x [all verify tokens], epilogue the
+// running greedy argmax over the vocabulary.
+//
 // The weight rows sit on the MMA's M side (128) and the few tokens of an
 // expert on its N side (16..256), so every weight byte is streamed from HBM
 // once per item while the tensor pipe stays legal at small batch.
 //
 // Per CTA: warp 0 issues TMA loads into a ring of shared-memory stages, one
 // thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
-// accumulator, and warps 2..5 drain TMEM through tcgen05.ld.  Items are
-// taken round-robin: item i runs on CTA i mod gridDim.
+// accumulator, and warps 2..5 drain TMEM through tcgen05.ld.
 #include <float.h>
 
 #include "internal.h"
@@ -27,31 +30,17 @@ namespace {
 constexpr int kGemmThreads = 192;
 constexpr int kStageA = 128 * 128;  // 128 weight rows x 64 bf16
 constexpr int kXbufBytes = 2 * 16 * 64 * 4;
-constexpr int kBarBytes = 1024;
+constexpr int kCtrlBytes = 1024;
+constexpr int kListBytes = 6144;  // per-expert counts and prefix sums (<= 264 experts)
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int MODE>
-__device__ __forceinline__ Item get_item(const GemmParams& p, int i) {
-  if (MODE == kLmHead) {
-    Item it;
-    const int vt = i / p.n_chunks, c = i % p.n_chunks;
-    it.a_row = vt * 128;
-    it.b_row = c * p.nch_lm;
-    it.n = min(p.nch_lm, p.T - c * p.nch_lm);
-    it.aux = vt;
-    return it;
-  } else {
-    const int4 v = __ldg(reinterpret_cast<const int4*>(p.items) + i);
-    Item it;
-    it.a_row = v.x;
-    it.b_row = v.y;
-    it.n = v.z;
-    it.aux = v.w;
-    return it;
-  }
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Orderable key of (logit, vocabulary id): larger logit first, then lower id.
@@ -68,279 +57,638 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
   return ((unsigned long long)hi << 32) | lo;
 }
 
-template <int MODE>
+// Barriers and flags at the start of the control area.
+struct Ctrl {
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;
+  uint64_t* drain;
+  uint64_t* xfull;
+  uint64_t* xempty;
+  uint64_t* spec;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ Ctrl ctrl_at(uint8_t* base, int stages) {
+  Ctrl c;
+  c.full = reinterpret_cast<uint64_t*>(base);
+  c.empty = c.full + stages;
+  c.tfull = c.empty + stages;
+  c.tempty = c.tfull + 2;
+  c.drain = c.tempty + 2;
+  c.xfull = c.drain + 1;
+  c.xempty = c.xfull + 2;
+  c.spec = c.xempty + 2;
+  c.tmem_slot = reinterpret_cast<uint32_t*>(c.spec + 1);
+  c.abort_flag = reinterpret_cast<volatile int*>(c.tmem_slot + 1);
+  return c;
+}
+
+__device__ __forceinline__ void init_ctrl(const Ctrl& c, int stages, uint32_t xfull_n,
+                                          uint32_t xempty_n) {
+  for (int s = 0; s < stages; ++s) {
+    mbar_init(&c.full[s], 1);
+    mbar_init(&c.empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&c.tfull[b], 1);
+    mbar_init(&c.tempty[b], 4);
+    mbar_init(&c.xfull[b], xfull_n);
+    mbar_init(&c.xempty[b], xempty_n);
+  }
+  mbar_init(c.drain, 1);
+  mbar_init(c.spec, 1);
+  *c.abort_flag = 0;
+  fence_mbar_init();
+}
+
+// The MMA issuer's wind-down: everything it issued completes before TMEM is
+// released.
+__device__ __forceinline__ void mma_drain(const Ctrl& c) {
+  umma_commit(c.drain);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(c.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// The producer's wind-down after an abort: let every load already issued land.
+__device__ __forceinline__ void producer_drain(const Ctrl& c, int issued, int stages) {
+  for (int r = (issued > stages ? issued - stages : 0); r < issued; ++r) {
+    const int s = r % stages;
+    const uint32_t par = (uint32_t)((r / stages) & 1);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&c.full[s], par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    }
+  }
+}
+
+// Issues the MMAs of one item (kblocks stages) into TMEM columns tmem_d.
+// Returns false if a wait gave up.
+__device__ __forceinline__ bool mma_item(const Ctrl& c, uint8_t* stages, int stage_bytes,
+                                         int n_stages, int& stage, uint32_t& phase, int kblocks,
+                                         uint32_t tmem_d, uint32_t idesc, uint32_t* status) {
+  for (int kb = 0; kb < kblocks; ++kb) {
+    if (!mbar_wait(&c.full[stage], phase, c.abort_flag, status)) return false;
+    tc_fence_after();
+    const uint32_t sa = smem_u32(stages + (size_t)stage * stage_bytes);
+    const uint32_t sb = sa + kStageA;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_bf16(tmem_d, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sb + kk * 32), idesc,
+                (kb | kk) != 0 ? 1u : 0u);
+    umma_commit(&c.empty[stage]);
+    if (++stage == n_stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+// ----------------------------------------------------------------- FFN
+
+struct FItem {
+  int down;     // 0: gate/up, 1: down
+  int e, mt;    // expert, 128-row tile inside it
+  int n;        // rows (tokens) of this chunk
+  int row0;     // first expert-major row
+  int chunk;    // global chunk id
+  int a_row;    // first weight row in the tensor map
+  int kblocks;
+};
+
+struct Lists {
+  int* cnt;  // [nE] rows per expert
+  int* cb;   // [nE+1] first chunk id per expert
+  int* igu;  // [nE+1] first gate/up item per expert
+  int* idn;  // [nE+1] first down item per expert
+};
+
+__device__ __forceinline__ FItem decode(const FfnParams& p, const Lists& L, int nE, int n_gu,
+                                        int i) {
+  FItem it;
+  it.down = i >= n_gu ? 1 : 0;
+  const int r = it.down ? i - n_gu : i;
+  const int* io = it.down ? L.idn : L.igu;
+  const int mt_n = it.down ? p.mt_dn : p.mt_gu;
+  // the last expert whose first item is <= r (empty experts share the start
+  // of the next non-empty one and come before it)
+  int lo = 0, hi = nE - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (io[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  it.e = lo;
+  const int q = r - io[lo];
+  const int ch = q / mt_n;
+  it.mt = q - ch * mt_n;
+  it.n = min(p.nch, L.cnt[lo] - ch * p.nch);
+  it.row0 = lo * p.T + ch * p.nch;
+  it.chunk = L.cb[lo] + ch;
+  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (lo * mt_n + it.mt) * 128;
+  it.kblocks = it.down ? p.kb_dn : p.kb_gu;
+  return it;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                const GemmParams p) {
+    ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
+               const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
+               const FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stage_bytes = kStageA + p.nch * 128;
   uint8_t* stages = smem;
-  uint8_t* ctrl = smem + (size_t)p.stages * stage_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + p.stages;
-  uint64_t* tfull = empty + p.stages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint64_t* xfull = drain + 1;   // epilogue exchange buffer filled [2]
-  uint64_t* xempty = xfull + 2;  // epilogue exchange buffer free [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* xbuf = reinterpret_cast<float*>(ctrl + kBarBytes);
+  uint8_t* ctrl_base = smem + (size_t)p.stages * stage_bytes;
+  const Ctrl C = ctrl_at(ctrl_base, p.stages);
+  int* list_base = reinterpret_cast<int*>(ctrl_base + kCtrlBytes);
+  float* xbuf = reinterpret_cast<float*>(ctrl_base + kCtrlBytes + kListBytes);
+  __shared__ int s_totals[3];  // gate/up items, down items, chunks
+  __shared__ int is_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, nE = p.E + p.S;
+  Lists L;
+  L.cnt = list_base;
+  L.cb = L.cnt + nE;
+  L.igu = L.cb + nE + 1;
+  L.idn = L.igu + nE + 1;
+
+  // Speculation: when every expert holds one chunk, the first item of CTA c
+  // is gate/up tile c of this layer.  Its weight tiles do not depend on the
+  // routing, so they start streaming before waiting for it.
+  const int guess_row = p.a_base_gu + blockIdx.x * 128;
+  const bool guess_valid = (int)blockIdx.x < nE * p.mt_gu;
+  const int pre = guess_valid ? min(p.stages, p.kb_gu) : 0;
+  if (threadIdx.x == 0) {
+    init_ctrl(C, p.stages, 2, 2);
+    tma_prefetch_desc(&map_gu);
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_dn);
+    tma_prefetch_desc(&map_a);
+    if (pre > 0) {
+      const uint64_t pol_w = policy_evict_first();
+      mbar_arrive_expect_tx(C.spec, (uint32_t)(pre * kStageA));
+      for (int s = 0; s < pre; ++s)
+        tma_load_2d(stages + (size_t)s * stage_bytes, &map_gu, C.spec, s * 64, guess_row, pol_w);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  // The routing kernel (the predecessor) must be complete before the counts
+  // and rows are read; dependents may start once this grid is past its wait.
+  pdl_wait();
+  pdl_launch_dependents();
+  if (warp == 0) {
+    // per-expert rows, chunk and item prefix sums: one warp, 32 experts per
+    // round, shuffle scans with a running carry
+    int cc = 0, cg = 0, cd = 0;
+    for (int e0 = 0; e0 < nE; e0 += 32) {
+      const int e = e0 + lane;
+      int c = 0, ch = 0;
+      if (e < nE) {
+        c = (e < E) ? min(__ldcg(p.cnt + e), p.T) : p.T;
+        ch = (c + p.nch - 1) / p.nch;
+        L.cnt[e] = c;
+      }
+      int ich = ch;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ich, o);
+        if (lane >= o) ich += a;
+      }
+      if (e < nE) {
+        const int before = ich - ch;
+        L.cb[e] = cc + before;
+        L.igu[e] = cg + before * p.mt_gu;
+        L.idn[e] = cd + before * p.mt_dn;
+      }
+      const int tot = __shfl_sync(0xffffffffu, ich, 31);
+      cc += tot;
+      cg += tot * p.mt_gu;
+      cd += tot * p.mt_dn;
+    }
+    if (lane == 0) {
+      L.cb[nE] = cc;
+      L.igu[nE] = cg;
+      L.idn[nE] = cd;
+      s_totals[0] = cg;
+      s_totals[1] = cd;
+      s_totals[2] = cc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *C.tmem_slot;
+  const int n_gu = s_totals[0];
+  const int n_items = n_gu + s_totals[1];
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int i = blockIdx.x, kb = 0;
+      FItem it = {};
+      if (i < n_items) it = decode(p, L, nE, n_gu, i);
+      bool ok = true;
+      if (pre > 0) ok = mbar_wait(C.spec, 0, C.abort_flag, p.status);  // speculative tiles landed
+      const bool hit = ok && pre > 0 && i < n_items && !it.down && it.a_row == guess_row;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      if (hit) {
+        // the weight tiles are already in place: add the activation tiles
+        const int npad = (it.n + 15) & ~15;
+        for (int s = 0; s < pre; ++s) {
+          uint8_t* sb = stages + (size_t)s * stage_bytes + kStageA;
+          mbar_arrive_expect_tx(&C.full[s], (uint32_t)(npad * 128));
+          for (int j = 0; j < npad; j += 16)
+            tma_load_2d(sb + j * 128, &map_x, &C.full[s], s * 64, it.row0 + j, pol_x);
+        }
+        issued = pre;
+        stage = pre;
+        kb = pre;
+        if (kb == it.kblocks) {
+          kb = 0;
+          i += gridDim.x;
+          if (i < n_items) it = decode(p, L, nE, n_gu, i);
+        }
+        if (stage == p.stages) {
+          stage = 0;
+          phase = 1;
+        }
+      }
+      while (ok && i < n_items) {
+        const int npad = (it.n + 15) & ~15;
+        if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = stages + (size_t)stage * stage_bytes;
+        uint8_t* sb = sa + kStageA;
+        mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + npad * 128));
+        tma_load_2d(sa, it.down ? &map_dn : &map_gu, &C.full[stage], kb * 64, it.a_row, pol_w);
+        if (it.down && kb == 0) {
+          // both SwiGLU halves of every gate/up tile of this chunk are written
+          const int want = 2 * p.mt_gu;
+          const uint64_t t0 = globaltimer_ns();
+          uint32_t n = 0;
+          while (ld_acquire(p.dep + it.chunk) < want) {
+            if ((++n & 63u) == 0 && (*C.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+              if (!*C.abort_flag) {
+                *C.abort_flag = 1;
+                atomicOr(p.status, kErrTimeout);
+              }
+              ok = false;
+              break;
+            }
+          }
+          fence_proxy_async_global();
+        }
+        // on a failed wait the activation tiles are still loaded (stale rows),
+        // so that the stage's byte count completes and the drain ends
+        for (int j = 0; j < npad; j += 16)
+          tma_load_2d(sb + j * 128, it.down ? &map_a : &map_x, &C.full[stage], kb * 64,
+                      it.row0 + j, pol_x);
+        ++issued;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++kb == it.kblocks) {
+          kb = 0;
+          i += gridDim.x;
+          if (i < n_items) it = decode(p, L, nE, n_gu, i);
+        }
+      }
+      if (!ok) producer_drain(C, issued, p.stages);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+        const FItem it = decode(p, L, nE, n_gu, i);
+        const int npad = (it.n + 15) & ~15;
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        if (!mma_item(C, stages, stage_bytes, p.stages, stage, phase, it.kblocks,
+                      tmem_base + (uint32_t)(buf * p.nch), umma_idesc_bf16(128, (uint32_t)npad),
+                      p.status))
+          break;
+        umma_commit(&C.tfull[buf]);
+      }
+      mma_drain(C);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int local = 0;
+    uint32_t chunk_seq = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+      const FItem it = decode(p, L, nE, n_gu, i);
+      const int npad = (it.n + 15) & ~15;
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.nch);
+      bool ok = true;
+      if (!it.down) {
+        // rows 0..63: gate, rows 64..127: up, intermediate columns mt*64 + r;
+        // the "up" warps hand their values to the "gate" warps
+        for (int c0 = 0; c0 < npad && ok; c0 += 16, ++chunk_seq) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+          const uint32_t xb = chunk_seq & 1u, xu = chunk_seq >> 1;
+          float* U = xbuf + xb * (16 * 64);
+          if (q >= 2) {
+            ok = mbar_wait(&C.xempty[xb], (xu & 1u) ^ 1u, C.abort_flag, p.status);
+            if (ok) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) U[j * 64 + (row - 64)] = __uint_as_float(v[j]);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&C.xfull[xb]);
+            }
+          } else {
+            ok = mbar_wait(&C.xfull[xb], xu & 1u, C.abort_flag, p.status);
+            if (ok) {
+              __nv_bfloat16* out = p.a_out + (size_t)it.mt * 64 + row;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = c0 + j;
+                if (n < it.n) {
+                  const float g = __uint_as_float(v[j]);
+                  const float u = U[j * 64 + row];
+                  const float a = g / (1.0f + __expf(-g)) * u;
+                  out[(size_t)(it.row0 + n) * p.I_pad] = __float2bfloat16_rn(a);
+                }
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&C.xempty[xb]);
+            }
+          }
+        }
+        if (ok && q < 2) {
+          // publish this half of the tile to the chunk's down items
+          __threadfence();
+          fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) atomicAdd(p.dep + it.chunk, 1);
+        }
+      } else {
+        const int m = it.mt * 128 + row;  // output dimension
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+          if (m < p.d) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = c0 + j;
+              if (n < it.n) {
+                const int r = it.row0 + n;
+                const int tok = __ldg(p.perm_token + r);
+                const int slot = __ldg(p.perm_slot + r);
+                const float w = __ldg(p.perm_w + r);
+                p.y[((size_t)tok * p.kS + slot) * p.d + m] = w * __uint_as_float(v[j]);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.tempty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+  }
+  // the last CTA clears the counters for the next layer
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (is_last) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) p.cnt_clear[e] = 0;
+    for (int c = threadIdx.x; c < s_totals[2]; c += blockDim.x) p.dep[c] = 0;
+    if (threadIdx.x == 0) *p.done = 0u;
+  }
+}
+
+// ------------------------------------------------------------- lm_head
+
+struct LmItem {
+  int a_row, b_row, n;
+};
+
+__device__ __forceinline__ LmItem lm_item(const GemmParams& p, int i) {
+  LmItem it;
+  const int vt = i / p.n_chunks, c = i % p.n_chunks;
+  it.a_row = vt * 128;
+  it.b_row = c * p.nch_lm;
+  it.n = min(p.nch_lm, p.T - c * p.nch_lm);
+  return it;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap mapA,
+                  const __grid_constant__ CUtensorMap mapB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int stage_bytes = kStageA + p.nch * 128;
+  uint8_t* stages = smem;
+  uint8_t* ctrl_base = smem + (size_t)p.stages * stage_bytes;
+  const Ctrl C = ctrl_at(ctrl_base, p.stages);
+  float* xbuf = reinterpret_cast<float*>(ctrl_base + kCtrlBytes + kListBytes);
+  __shared__ int is_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.n_items_static;
+  const bool has_work = (int)blockIdx.x < n_items;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-    }
-    mbar_init(drain, 1);
-    // gate/up: the two "up" warps fill, the two "gate" warps drain;
-    // lm_head: all four warps fill, warp 2 drains.
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&xfull[b], MODE == kLmHead ? 4 : 2);
-      mbar_init(&xempty[b], MODE == kLmHead ? 1 : 2);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
+    init_ctrl(C, p.stages, 4, 1);
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
   }
-  // everything above is independent of the previous kernel's output; all
-  // global writes of this grid come after pdl_wait
-  pdl_launch_dependents();
-  pdl_wait();
-  const int n_items = (MODE == kLmHead) ? p.n_items_static : __ldcg(p.n_items);
-  const bool has_work = (int)blockIdx.x < n_items;
   if (has_work && warp == 1) {
-    tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = has_work ? *tmem_slot : 0u;
+  const uint32_t tmem_base = has_work ? *C.tmem_slot : 0u;
 
-  if (has_work) {
-    if (warp == 0) {
-      // ------------------------------------------------ TMA producer
-      if (lane == 0) {
-        const uint64_t pol_w = policy_evict_first();
-        const uint64_t pol_x = policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued_rounds = 0;
-        bool ok = true;
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-          const Item it = get_item<MODE>(p, i);
-          const int npad = (it.n + 15) & ~15;
-          const uint32_t bytes = (uint32_t)(kStageA + npad * 128);
-          for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* sa = stages + (size_t)stage * stage_bytes;
-            uint8_t* sb = sa + kStageA;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            tma_load_2d(sa, &mapA, &full[stage], kb * 64, it.a_row, pol_w);
-            for (int j = 0; j < npad; j += 16)
-              tma_load_2d(sb + j * 128, &mapB, &full[stage], kb * 64, it.b_row + j, pol_x);
-            ++issued_rounds;
-            if (++stage == p.stages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        if (!ok) {
-          // wind down: let every load already issued land before the CTA exits
-          const int last = issued_rounds;
-          for (int r = (last > p.stages ? last - p.stages : 0); r < last; ++r) {
-            const int s = r % p.stages;
-            const uint32_t par = (uint32_t)((r / p.stages) & 1);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[s], par) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-          }
+  if (has_work && warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    // The first ring of weight tiles does not depend on earlier kernels:
+    // issue it before waiting for the final RMSNorm.
+    int i = blockIdx.x, kb = 0;
+    LmItem it = lm_item(p, i);
+    int pre = 0;
+    {
+      int pi = i, pk = kb;
+      LmItem pt = it;
+      while (pre < p.stages && pi < n_items) {
+        const int npad = (pt.n + 15) & ~15;
+        mbar_arrive_expect_tx(&C.full[pre], (uint32_t)(kStageA + npad * 128));
+        tma_load_2d(stages + (size_t)pre * stage_bytes, &mapA, &C.full[pre], pk * 64, pt.a_row,
+                    pol_w);
+        ++pre;
+        if (++pk == p.kblocks) {
+          pk = 0;
+          pi += gridDim.x;
+          if (pi < n_items) pt = lm_item(p, pi);
         }
       }
-    } else if (warp == 1) {
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int s = 0; s < pre; ++s) {
+      const int npad = (it.n + 15) & ~15;
+      uint8_t* sb = stages + (size_t)s * stage_bytes + kStageA;
+      for (int j = 0; j < npad; j += 16)
+        tma_load_2d(sb + j * 128, &mapB, &C.full[s], kb * 64, it.b_row + j, pol_x);
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = lm_item(p, i);
+      }
+    }
+    int stage = pre, issued = pre;
+    uint32_t phase = 0;
+    if (stage == p.stages) {
+      stage = 0;
+      phase = 1;
+    }
+    bool ok = true;
+    while (i < n_items) {
+      const int npad = (it.n + 15) & ~15;
+      if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + (size_t)stage * stage_bytes;
+      mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + npad * 128));
+      tma_load_2d(sa, &mapA, &C.full[stage], kb * 64, it.a_row, pol_w);
+      for (int j = 0; j < npad; j += 16)
+        tma_load_2d(sa + kStageA + j * 128, &mapB, &C.full[stage], kb * 64, it.b_row + j, pol_x);
+      ++issued;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = lm_item(p, i);
+      }
+    }
+    if (!ok) producer_drain(C, issued, p.stages);
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (has_work && warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int local = 0;
-        bool ok = true;
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++local) {
-          const Item it = get_item<MODE>(p, i);
-          const int npad = (it.n + 15) & ~15;
-          const uint32_t idesc = umma_idesc_bf16(128, (uint32_t)npad);
-          const int buf = local & 1;
-          const uint32_t use = (uint32_t)(local >> 1);
-          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tmem_d = tmem_base + (uint32_t)(buf * p.nch);
-          for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(stages + (size_t)stage * stage_bytes);
-            const uint32_t sb = sa + kStageA;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              umma_bf16(tmem_d, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sb + kk * 32),
-                        idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
-            umma_commit(&empty[stage]);
-            if (++stage == p.stages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (ok) umma_commit(&tfull[buf]);
-        }
-        // all MMAs issued by this thread complete before TMEM is released
-        umma_commit(drain);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-        }
-      }
-    } else {
-      // ------------------------------------------------ epilogue warps 2..5
-      const int q = warp & 3;  // TMEM lane quarter this warp may access
-      const int row = q * 32 + lane;
-      int local = 0;
-      uint32_t chunk_seq = 0;
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
       for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
-        const Item it = get_item<MODE>(p, i);
+        const LmItem it = lm_item(p, i);
         const int npad = (it.n + 15) & ~15;
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!mbar_wait(&tfull[buf], use & 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        if (!mma_item(C, stages, stage_bytes, p.stages, stage, phase, p.kblocks,
+                      tmem_base + (uint32_t)(buf * p.nch), umma_idesc_bf16(128, (uint32_t)npad),
+                      p.status))
+          break;
+        umma_commit(&C.tfull[buf]);
+      }
+      mma_drain(C);
+    } else if (has_work && warp >= 2) {
+      // ------------------------------------------------ epilogue warps 2..5
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      int local = 0;
+      uint32_t chunk_seq = 0;
+      unsigned long long* red = reinterpret_cast<unsigned long long*>(xbuf);
+      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+        const LmItem it = lm_item(p, i);
+        const int npad = (it.n + 15) & ~15;
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.nch);
-
+        // greedy argmax over this tile's 128 vocabulary rows, per token column
+        const int vid = it.a_row + row;
+        const bool valid = vid < p.V;
         bool ok = true;
-        if (MODE == kGateUp) {
-          // rows 0..63: gate, rows 64..127: up, for intermediate columns aux*64 + r
-          for (int c0 = 0; c0 < npad && ok; c0 += 16, ++chunk_seq) {
-            uint32_t v[16];
-            tmem_ld16(tb + (uint32_t)c0, v);
-            tmem_ld_wait();
-            const uint32_t xb = chunk_seq & 1u, xu = chunk_seq >> 1;
-            float* U = xbuf + xb * (16 * 64);
-            if (q >= 2) {
-              ok = mbar_wait(&xempty[xb], (xu & 1u) ^ 1u, abort_flag, p.status);
-              if (ok) {
+        for (int c0 = 0; c0 < npad && ok; c0 += 16, ++chunk_seq) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+          const uint32_t xb = chunk_seq & 1u, xu = chunk_seq >> 1;
+          unsigned long long* R = red + xb * 64;
+          unsigned long long keys[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) U[j * 64 + (row - 64)] = __uint_as_float(v[j]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xfull[xb]);
-              }
-            } else {
-              ok = mbar_wait(&xfull[xb], xu & 1u, abort_flag, p.status);
-              if (ok) {
-                __nv_bfloat16* out = p.a_out + (size_t)it.aux * 64 + row;
+          for (int j = 0; j < 16; ++j) {
+            const float lv = __uint_as_float(v[j]);
+            unsigned long long key = valid ? argmax_key(lv, vid) : 0ull;
+            if (p.logits && valid && c0 + j < it.n)
+              p.logits[(size_t)(it.b_row + c0 + j) * p.V + vid] = lv;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const int n = c0 + j;
-                  if (n < it.n) {
-                    const float g = __uint_as_float(v[j]);
-                    const float u = U[j * 64 + row];
-                    const float a = g / (1.0f + __expf(-g)) * u;
-                    out[(size_t)(it.b_row + n) * p.I_pad] = __float2bfloat16_rn(a);
-                  }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xempty[xb]);
-              }
+            for (int o = 16; o > 0; o >>= 1) {
+              const unsigned long long other = shfl_xor_u64(key, o);
+              key = other > key ? other : key;
             }
+            keys[j] = key;
           }
-        } else if (MODE == kDown) {
-          const int m = it.aux * 128 + row;  // output dimension
-          for (int c0 = 0; c0 < npad; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tb + (uint32_t)c0, v);
-            tmem_ld_wait();
-            if (m < p.d) {
+          ok = mbar_wait(&C.xempty[xb], (xu & 1u) ^ 1u, C.abort_flag, p.status);
+          if (!ok) break;
+          if (lane == 0) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int n = c0 + j;
-                if (n < it.n) {
-                  const int r = it.b_row + n;
-                  const int tok = __ldg(p.perm_token + r);
-                  const int slot = __ldg(p.perm_slot + r);
-                  const float w = __ldg(p.perm_w + r);
-                  p.y[((size_t)tok * p.kS + slot) * p.d + m] = w * __uint_as_float(v[j]);
-                }
-              }
-            }
+            for (int j = 0; j < 16; ++j) R[(warp - 2) * 16 + j] = keys[j];
+            mbar_arrive(&C.xfull[xb]);
           }
-        } else {
-          // greedy argmax over this tile's 128 vocabulary rows, per token column
-          const int vid = it.a_row + row;
-          const bool valid = vid < p.V;
-          unsigned long long* red = reinterpret_cast<unsigned long long*>(xbuf);
-          for (int c0 = 0; c0 < npad && ok; c0 += 16, ++chunk_seq) {
-            uint32_t v[16];
-            tmem_ld16(tb + (uint32_t)c0, v);
-            tmem_ld_wait();
-            const uint32_t xb = chunk_seq & 1u, xu = chunk_seq >> 1;
-            unsigned long long* R = red + xb * 64;
-            unsigned long long keys[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float lv = __uint_as_float(v[j]);
-              unsigned long long key = valid ? argmax_key(lv, vid) : 0ull;
-              if (p.logits && valid && c0 + j < it.n)
-                p.logits[(size_t)(it.b_row + c0 + j) * p.V + vid] = lv;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long other = shfl_xor_u64(key, o);
-                key = other > key ? other : key;
-              }
-              keys[j] = key;
-            }
-            ok = mbar_wait(&xempty[xb], (xu & 1u) ^ 1u, abort_flag, p.status);
+          if (warp == 2) {
+            ok = mbar_wait(&C.xfull[xb], xu & 1u, C.abort_flag, p.status);
             if (!ok) break;
-            if (lane == 0) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) R[(warp - 2) * 16 + j] = keys[j];
-              mbar_arrive(&xfull[xb]);
+            if (lane < 16 && c0 + lane < it.n) {
+              unsigned long long k0 = R[lane], k1 = R[16 + lane], k2 = R[32 + lane],
+                                 k3 = R[48 + lane];
+              k0 = k1 > k0 ? k1 : k0;
+              k2 = k3 > k2 ? k3 : k2;
+              k0 = k2 > k0 ? k2 : k0;
+              atomicMax(p.keys + it.b_row + c0 + lane, k0);
             }
-            if (warp == 2) {
-              ok = mbar_wait(&xfull[xb], xu & 1u, abort_flag, p.status);
-              if (!ok) break;
-              if (lane < 16 && c0 + lane < it.n) {
-                unsigned long long k0 = R[lane], k1 = R[16 + lane], k2 = R[32 + lane],
-                                   k3 = R[48 + lane];
-                k0 = k1 > k0 ? k1 : k0;
-                k2 = k3 > k2 ? k3 : k2;
-                k0 = k2 > k0 ? k2 : k0;
-                atomicMax(p.keys + it.b_row + c0 + lane, k0);
-              }
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&xempty[xb]);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&C.xempty[xb]);
           }
         }
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) mbar_arrive(&C.tempty[buf]);
       }
     }
   }
@@ -350,30 +698,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
-  if (MODE == kLmHead) {
-    // the last CTA turns the argmax keys into token ids
+  // the last CTA turns the argmax keys into token ids
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (is_last) {
     __threadfence();
-    __syncthreads();
-    __shared__ int is_last;
-    if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-    __syncthreads();
-    if (is_last) {
-      __threadfence();
-      for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
-        const unsigned long long key = __ldcg(p.keys + t);
-        const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-        p.targets[t] = (__ldg(p.bad + t) || key == 0ull) ? -1 : id;
-      }
-      if (threadIdx.x == 0) *p.done = 0u;
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+      const unsigned long long key = __ldcg(p.keys + t);
+      const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+      p.targets[t] = (__ldg(p.bad + t) || key == 0ull) ? -1 : id;
     }
+    if (threadIdx.x == 0) *p.done = 0u;
   }
 }
 
-template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
-                        int grid, cudaStream_t s, bool pdl) {
-  const size_t smem = gemm_smem_bytes(p.nch, p.stages);
-  auto kern = gemm_kernel<MODE>;
+template <typename Kern, typename... Args>
+cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, bool pdl,
+                           Args... args) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -386,14 +729,14 @@ cudaError_t launch_mode(const CUtensorMap& mapA, const CUtensorMap& mapB, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, mapA, mapB, p);
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes(int nch, int stages) {
-  return 1024 /* alignment slack */ + (size_t)stages * (kStageA + (size_t)nch * 128) + kBarBytes +
-         kXbufBytes;
+  return 1024 /* alignment slack */ + (size_t)stages * (kStageA + (size_t)nch * 128) + kCtrlBytes +
+         kListBytes + kXbufBytes;
 }
 
 int gemm_max_stages(int nch) {
@@ -403,13 +746,17 @@ int gemm_max_stages(int nch) {
   return s;
 }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                        const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
-  switch (mode) {
-    case kGateUp: return launch_mode<kGateUp>(mapA, mapB, p, grid, s, pdl);
-    case kDown: return launch_mode<kDown>(mapA, mapB, p, grid, s, pdl);
-    default: return launch_mode<kLmHead>(mapA, mapB, p, grid, s, pdl);
-  }
+cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
+                       const CUtensorMap& map_dn, const CUtensorMap& map_a, const FfnParams& p,
+                       int grid, cudaStream_t s, bool pdl) {
+  return launch_gemm_ex(ffn_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu, map_x,
+                        map_dn, map_a, p);
+}
+
+cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                          int grid, cudaStream_t s, bool pdl) {
+  return launch_gemm_ex(lmhead_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, mapA, mapB,
+                        p);
 }
 
 }  // namespace mv

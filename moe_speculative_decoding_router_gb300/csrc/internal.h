@@ -13,16 +13,6 @@ constexpr uint32_t kErrIdRange = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 constexpr uint32_t kErrInternal = 4u;
 
-// One unit of grouped-GEMM work: a 128-row tile of one weight matrix times
-// up to `n` activation rows.  a_row: first row of the tile in the weight
-// tensor map; b_row: first activation row; aux: tile index inside the expert.
-struct Item {
-  int32_t a_row;
-  int32_t b_row;
-  int32_t n;
-  int32_t aux;
-};
-
 // Sources of the residual stream entering a routing kernel.
 enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2 };
 
@@ -42,25 +32,38 @@ struct RouteParams {
   const float* gain;           // [d]
   const __nv_bfloat16* Wr;     // [E, d]
   const float* bias;           // [E] or nullptr
-  __nv_bfloat16* xhat;         // [T, d]
-  int32_t* topk_idx;           // [T, k]
-  float* topk_w;               // [T, k]
   int32_t* bad;                // [T]
   uint32_t* status;
   int32_t* probe_idx;          // [T, k] or nullptr
   float* probe_w;              // [T, k] or nullptr
   float* probe_hidden;         // [T, d] or nullptr
-  // grouping (done by the last block to finish)
-  int32_t* perm_token;         // [rows]
-  int32_t* perm_slot;          // [rows]
-  float* perm_w;               // [rows]
-  int32_t* expert_off;         // [E+S+1]
-  Item* items_gu;
-  Item* items_dn;
-  int32_t* n_items;            // [2]
-  int nch_r, nch_s;            // activation rows per item: routed / shared experts
-  int mt_gu, mt_dn;            // 128-row tiles per expert: gate/up, down
+  // expert-major rows: expert e owns rows [e*T, e*T + cnt[e])
+  int32_t* cnt;                // [E] rows claimed per routed expert (zero on entry)
+  __nv_bfloat16* xperm;        // [(E+S)*T, d] normalised inputs
+  int32_t* perm_token;         // [(E+S)*T] token of each row
+  int32_t* perm_slot;          // [(E+S)*T] its slot: routed rank, or k + s
+  float* perm_w;               // [(E+S)*T] combine weight (1 for shared)
+};
+
+// The layer's expert FFN in one persistent kernel: gate/up + SwiGLU items for
+// every (expert, 128-row tile, chunk of <= nch rows), then the down items.
+struct FfnParams {
+  const int32_t* cnt;          // [E] routed rows per expert (shared experts: T)
+  int32_t* cnt_clear;          // the same counters, cleared by the last CTA
+  int32_t* dep;                // [chunks] finished gate/up halves per chunk
+  int E, S, T, nch;
+  int mt_gu, mt_dn;            // 128-row tiles per expert
+  int kb_gu, kb_dn;            // 64-wide K blocks: d/64 and I_pad/64
   int a_base_gu, a_base_dn;    // first weight row of this layer in the tensor maps
+  int stages, tmem_cols;
+  __nv_bfloat16* a_out;        // [(E+S)*T, I_pad] SwiGLU rows
+  int I_pad;
+  const int32_t* perm_token;
+  const int32_t* perm_slot;
+  const float* perm_w;
+  float* y;                    // [T, kS, d]
+  int d, kS;
+  uint32_t* status;
   unsigned int* done;
 };
 
@@ -76,27 +79,14 @@ struct FinalParams {
   unsigned long long* keys;    // [T] argmax keys, cleared in mode 0
 };
 
-enum GemmMode : int { kGateUp = 0, kDown = 1, kLmHead = 2 };
-
+// The lm_head GEMM with its argmax epilogue.
 struct GemmParams {
-  const Item* items;           // kGateUp, kDown
-  const int32_t* n_items;      // device count
-  int n_items_static;          // kLmHead
-  int kblocks;                 // K / 64
-  int nch;                     // largest activation row count of an item (multiple of 16)
+  int n_items_static;          // vocabulary tiles x token chunks
+  int kblocks;                 // d / 64
+  int nch;                     // tokens per item (multiple of 16)
   int stages;
   int tmem_cols;
   uint32_t* status;
-  // kGateUp
-  __nv_bfloat16* a_out;        // [rows, I_pad]
-  int I_pad;
-  // kDown
-  const int32_t* perm_token;
-  const int32_t* perm_slot;
-  const float* perm_w;
-  float* y;                    // [T, kS, d]
-  int d, kS;
-  // kLmHead
   int T, V, n_chunks, nch_lm;
   unsigned long long* keys;    // [T]
   float* logits;               // [T, V] or nullptr
@@ -114,19 +104,19 @@ struct AcceptParams {
   uint32_t* status;
 };
 
-// Shared memory the GEMM kernel needs for a given item width and stage count.
+// Shared memory the GEMM kernels need for a given item width and stage count.
 size_t gemm_smem_bytes(int nch, int stages);
 int gemm_max_stages(int nch);
-size_t route_smem_bytes(int tpb, int d, int E, int T, int k, bool wr_smem);
-size_t route_group_smem_bytes(int T, int k, int E);  // the grouping step's share
-bool route_wr_fits(int tpb, int d, int E);
+size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem);
+bool route_wr_fits(int tpb, int d, int E, int k, int S);
 
 // Launchers (enqueue only).  `pdl` requests programmatic dependent launch.
 cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl);
-cudaError_t launch_scatter(const int32_t* perm_token, const __nv_bfloat16* xhat,
-                           __nv_bfloat16* xperm, int rows, int d, cudaStream_t s, bool pdl);
-cudaError_t launch_gemm(int mode, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                        const GemmParams& p, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
+                       const CUtensorMap& map_dn, const CUtensorMap& map_a, const FfnParams& p,
+                       int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
+                          int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
 

@@ -179,7 +179,7 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
   gp.targets = target_ids;
   gp.bad = reinterpret_cast<const int32_t*>(scratch + kBadOff);
   gp.done = reinterpret_cast<unsigned int*>(scratch + kDoneOff);
-  if (mv::launch_gemm(mv::kLmHead, map_lm, map_xf, gp, sms, s, false) != cudaSuccess)
+  if (mv::launch_lmhead(map_lm, map_xf, gp, sms, s, false) != cudaSuccess)
     return MOE_VERIFY_ERR_CUDA;
   return MOE_VERIFY_OK;
 }

@@ -126,6 +126,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (no completion tracking).
+// Address 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Orders this thread's earlier generic-proxy global accesses against its
 // later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

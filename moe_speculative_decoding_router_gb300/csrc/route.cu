@@ -1,11 +1,20 @@
 // Per-layer routing: residual update, RMSNorm, softmax router with top-k
-// selection, and the grouping of (token, slot) pairs by expert.
+// selection, and the placement of each token's normalised row in the rows of
+// the experts it selected.
 //
 // Decoder block of "Jina AI Releases jina-ocr-v1, a 3.4B MoE Document Parser
 // With Built-In Speculative Decoding", architecture paragraph: 64 routed
 // experts, top-6 routing, two shared experts.  Top-k is taken on the router
 // logits (ties: lower expert index); the weights are the softmax over all
 // experts, not renormalised.
+//
+// Expert-major rows: expert e (shared experts are E .. E+S-1) owns rows
+// [e*T, e*T + count_e) of the normalised-input and SwiGLU buffers.  A routed
+// token claims its row in expert e with an atomic counter, so the order of
+// tokens inside an expert varies from run to run; every token's result is
+// independent of its row (each row is a separate column of the expert's GEMM,
+// reduced in a fixed order), so the outputs do not.  Shared expert s holds
+// token t in row (E+s)*T + t.
 #include <float.h>
 
 #include "internal.h"
@@ -69,10 +78,11 @@ __device__ __forceinline__ float4 residual_chunk(const RouteParams& p, int t, in
 }
 
 // Stage 1 for the block's tokens t0 .. t0+ntok-1, all threads: build h (and
-// write it back), RMSNorm, write xhat (bf16, global) and its widened values
-// to xs [ntok, d] in shared memory.
+// write it back), RMSNorm; the normalised row goes to xs [TPB, d] (widened
+// bf16 values, for the router) and xb [TPB, d] (bf16, for the expert rows).
 template <int SRC, int TPB>
-__device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, float* red) {
+__device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs,
+                           __nv_bfloat16* xb, float* red) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = p.d, nc = d / 4;
   float ss[TPB];
@@ -115,7 +125,6 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, fl
 #pragma unroll
     for (int w = 0; w < kRouteWarps; ++w) tot += red[w * 8 + tt];
     const float r = rsqrtf(tot / (float)d + p.eps);
-    const int t = t0 + tt;
     for (int c = tid; c < nc; c += kRouteThreads) {
       float4 v = reinterpret_cast<const float4*>(xs + tt * d)[c];
       const float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
@@ -127,7 +136,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, fl
       uint2 packed;
       packed.x = *reinterpret_cast<uint32_t*>(&lo);
       packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(p.xhat + (size_t)t * d)[c] = packed;
+      reinterpret_cast<uint2*>(xb + tt * d)[c] = packed;
       v = make_float4(__bfloat162float(q0), __bfloat162float(q1), __bfloat162float(q2),
                       __bfloat162float(q3));
       reinterpret_cast<float4*>(xs + tt * d)[c] = v;
@@ -135,158 +144,28 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, fl
   }
 }
 
-// Grouping by expert, run by the last block of the grid.  Expert-major rows:
-// routed expert e owns rows [off[e], off[e+1]) with its tokens in increasing
-// token order; shared expert s owns rows off[E+s] + t for every token t.
-// Shared memory: idx [T*k], per-expert token bitmasks and their prefix
-// popcounts [E][T/32], counts and offsets [E+S+1] x 3.
-__device__ void group_by_expert(const RouteParams& p, int* sm) {
-  const int T = p.T, k = p.k, E = p.E, S = p.S, nE = E + S;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nw = (T + 31) / 32;  // bitmask words per expert
-  int* idx_s = sm;                                             // [T*k]
-  unsigned* mask = reinterpret_cast<unsigned*>(idx_s + T * k);  // [E*nw]
-  int* pre = reinterpret_cast<int*>(mask + E * nw);       // [E*nw]
-  int* cnt_s = pre + E * nw;                              // [nE]
-  int* off_s = cnt_s + nE;                                // [nE+1]
-  int* igu_s = off_s + nE + 1;                            // [nE+1] item offsets, gate/up
-  int* idn_s = igu_s + nE + 1;                            // [nE+1] item offsets, down
-
-  for (int i = tid; i < E * nw; i += kRouteThreads) mask[i] = 0u;
-  for (int i = tid; i < T * k; i += kRouteThreads) {
-    const int e = __ldcg(p.topk_idx + i);
-    idx_s[i] = (e >= 0 && e < E) ? e : 0;
-  }
-  __syncthreads();
-  for (int i = tid; i < T * k; i += kRouteThreads) {
-    const int t = i / k;
-    atomicOr(&mask[idx_s[i] * nw + (t >> 5)], 1u << (t & 31));
-  }
-  __syncthreads();
-  // per expert: prefix popcounts over the bitmask words, and the count
-  for (int e = tid; e < nE; e += kRouteThreads) {
-    if (e < E) {
-      int run = 0;
-      for (int w = 0; w < nw; ++w) {
-        pre[e * nw + w] = run;
-        run += __popc(mask[e * nw + w]);
-      }
-      cnt_s[e] = run;
-    } else {
-      cnt_s[e] = T;
-    }
-  }
-  __syncthreads();
-  // exclusive scans over experts of rows, gate/up items and down items: one
-  // warp, 32 experts per round, shuffle scans with a running carry
-  if (warp == 0) {
-    int co = 0, cg = 0, cd = 0;
-    for (int e0 = 0; e0 < nE; e0 += 32) {
-      const int e = e0 + lane;
-      int c = 0, ng = 0, nd = 0;
-      if (e < nE) {
-        c = cnt_s[e];
-        const int nch = (e < E) ? p.nch_r : p.nch_s;
-        const int chunks = (c + nch - 1) / nch;
-        ng = chunks * p.mt_gu;
-        nd = chunks * p.mt_dn;
-      }
-      int ic = c, ig = ng, id = nd;  // inclusive scans
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, ic, o);
-        const int b = __shfl_up_sync(0xffffffffu, ig, o);
-        const int f = __shfl_up_sync(0xffffffffu, id, o);
-        if (lane >= o) {
-          ic += a;
-          ig += b;
-          id += f;
-        }
-      }
-      if (e < nE) {
-        off_s[e] = co + ic - c;
-        igu_s[e] = cg + ig - ng;
-        idn_s[e] = cd + id - nd;
-      }
-      co += __shfl_sync(0xffffffffu, ic, 31);
-      cg += __shfl_sync(0xffffffffu, ig, 31);
-      cd += __shfl_sync(0xffffffffu, id, 31);
-    }
-    if (lane == 0) {
-      off_s[nE] = co;
-      igu_s[nE] = cg;
-      idn_s[nE] = cd;
-      p.n_items[0] = cg;
-      p.n_items[1] = cd;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e <= nE; e += kRouteThreads) p.expert_off[e] = off_s[e];
-
-  // row of each routed (token, slot): the expert's offset plus the number of
-  // its tokens before t (prefix popcount of its bitmask)
-  for (int i = tid; i < T * k; i += kRouteThreads) {
-    const int t = i / k, j = i - t * k;
-    const int e = idx_s[i];
-    const int w = t >> 5;
-    const int pos = off_s[e] + pre[e * nw + w] +
-                    __popc(mask[e * nw + w] & ((1u << (t & 31)) - 1u));
-    p.perm_token[pos] = t;
-    p.perm_slot[pos] = j;
-    p.perm_w[pos] = __ldcg(p.topk_w + i);
-  }
-  for (int i = tid; i < S * T; i += kRouteThreads) {
-    const int s = i / T, t = i - s * T;
-    const int pos = off_s[E + s] + t;
-    p.perm_token[pos] = t;
-    p.perm_slot[pos] = k + s;
-    p.perm_w[pos] = 1.0f;
-  }
-  // work items, one thread each; expert-major, so the tiles of one expert
-  // sit next to each other
-  const int n_gu = igu_s[nE], n_all = n_gu + idn_s[nE];
-  for (int i = tid; i < n_all; i += kRouteThreads) {
-    const bool gu = i < n_gu;
-    const int r = gu ? i : i - n_gu;
-    const int* io = gu ? igu_s : idn_s;
-    int lo = 0, hi = nE - 1;  // last expert with io[e] <= r
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (io[mid] <= r) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo;
-    const int mt_n = gu ? p.mt_gu : p.mt_dn;
-    const int q = r - io[e];
-    const int ch = q / mt_n, mt = q - ch * mt_n;
-    const int nch = (e < E) ? p.nch_r : p.nch_s;
-    Item it;
-    it.a_row = (gu ? p.a_base_gu : p.a_base_dn) + (e * mt_n + mt) * 128;
-    it.b_row = off_s[e] + ch * nch;
-    it.n = min(nch, cnt_s[e] - ch * nch);
-    it.aux = mt;
-    (gu ? p.items_gu : p.items_dn)[r] = it;
-  }
-}
-
 template <int SRC, int TPB>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   extern __shared__ __align__(128) float rsm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = p.d, E = p.E, tpb = TPB;
-  const int t0 = blockIdx.x * tpb;
-  const int ntok = min(tpb, p.T - t0);
-  // shared memory: [router weights E x d bf16, when staged] [xs tpb x d] [zs tpb x E] [red 64]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = p.d, E = p.E, k = p.k, S = p.S;
+  const int t0 = blockIdx.x * TPB;
+  const int ntok = min(TPB, p.T - t0);
+  // shared memory: [router weights E x d bf16, when staged] [xs TPB x d fp32]
+  // [xb TPB x d bf16] [zs TPB x E] [red 64] [rows TPB x (k+S) ints]
   const size_t wr_bytes = p.wr_smem ? (size_t)E * d * 2 : 0;
   __nv_bfloat16* wr_s = reinterpret_cast<__nv_bfloat16*>(rsm);
   float* xs = reinterpret_cast<float*>(reinterpret_cast<char*>(rsm) + wr_bytes);
-  float* zs = xs + tpb * d;
-  float* red = zs + tpb * E;
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + TPB * d);
+  float* zs = reinterpret_cast<float*>(xb + TPB * d);
+  float* red = zs + TPB * E;
+  int* rows = reinterpret_cast<int*>(red + 64);
   __shared__ __align__(8) uint64_t wr_bar;
   __shared__ int abort_flag;
 
   // The router weights do not depend on earlier kernels: start their copy
   // into shared memory before waiting for the previous kernel.
-  if (p.wr_smem && threadIdx.x == 0) {
+  if (p.wr_smem && tid == 0) {
     abort_flag = 0;
     mbar_init(&wr_bar, 1);
     fence_mbar_init();
@@ -298,14 +177,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
       bulk_load(dst + off, src + off, n, &wr_bar);
     }
   }
-  // dependents may start their own prologue now; every global write below
-  // comes after pdl_wait, so they cannot disturb what this grid still reads
-  pdl_launch_dependents();
+  // Wait for the previous kernel, then let dependents start: a kernel two
+  // launches later may then read what the kernel before this one wrote.
   pdl_wait();
-  block_norm<SRC, TPB>(p, t0, ntok, xs, red);
+  pdl_launch_dependents();
+  block_norm<SRC, TPB>(p, t0, ntok, xs, xb, red);
   __syncthreads();
   bool wr_ok = true;
   if (p.wr_smem) wr_ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
+  for (int i = tid; i < TPB * (k + S); i += kRouteThreads) rows[i] = -1;
 
   // router logits: warp w computes experts 8w .. 8w+7 (then + 64, ...) for
   // every token of the block, eight independent accumulation chains per lane
@@ -317,12 +197,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
 #pragma unroll
       for (int tt = 0; tt < TPB; ++tt) acc[j][tt] = 0.f;
     for (int c = lane; c < d / 8; c += 32) {
-      float4 xa[TPB], xb[TPB];
+      float4 xa[TPB], xv[TPB];
 #pragma unroll
       for (int tt = 0; tt < TPB; ++tt) {
         const float4* x4 = reinterpret_cast<const float4*>(xs + tt * d + c * 8);
         xa[tt] = x4[0];
-        xb[tt] = x4[1];
+        xv[tt] = x4[1];
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -337,10 +217,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
           a = fmaf(w8[1], xa[tt].y, a);
           a = fmaf(w8[2], xa[tt].z, a);
           a = fmaf(w8[3], xa[tt].w, a);
-          a = fmaf(w8[4], xb[tt].x, a);
-          a = fmaf(w8[5], xb[tt].y, a);
-          a = fmaf(w8[6], xb[tt].z, a);
-          a = fmaf(w8[7], xb[tt].w, a);
+          a = fmaf(w8[4], xv[tt].x, a);
+          a = fmaf(w8[5], xv[tt].y, a);
+          a = fmaf(w8[6], xv[tt].z, a);
+          a = fmaf(w8[7], xv[tt].w, a);
           acc[j][tt] = a;
         }
       }
@@ -359,10 +239,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
 
   // softmax and top-k, one warp per token.  Rank of expert e = number of
   // experts ordered before it by (z desc, index asc); the experts of rank < k
-  // are the selection, written in rank order.
+  // are the selection, in rank order.  Each selected expert's row is claimed
+  // with its counter; shared experts take the token's own row.
   if (warp < ntok && wr_ok) {
-    const int t = t0 + warp;
-    const float* z = zs + warp * E;
+    const int tt = warp, t = t0 + tt;
+    const float* z = zs + tt * E;
     float m = -FLT_MAX;
     for (int e = lane; e < E; e += 32) m = fmaxf(m, z[e]);
     m = warp_max(m);
@@ -376,42 +257,44 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
         const float zf = z[f];
         rank += (zf > ze || (zf == ze && f < e)) ? 1 : 0;
       }
-      if (rank < p.k) {
+      if (rank < k) {
         const float w = __expf(ze - m) / sum;
-        p.topk_idx[(size_t)t * p.k + rank] = e;
-        p.topk_w[(size_t)t * p.k + rank] = w;
-        if (p.probe_idx) p.probe_idx[(size_t)t * p.k + rank] = e;
-        if (p.probe_w) p.probe_w[(size_t)t * p.k + rank] = w;
+        int slot = atomicAdd(p.cnt + e, 1);
+        if (slot >= p.T) {  // only reachable if the counters were not cleared
+          atomicOr(p.status, kErrInternal);
+          slot = p.T - 1;
+        }
+        const int row = e * p.T + slot;
+        rows[tt * (k + S) + rank] = row;
+        p.perm_token[row] = t;
+        p.perm_slot[row] = rank;
+        p.perm_w[row] = w;
+        if (p.probe_idx) p.probe_idx[(size_t)t * k + rank] = e;
+        if (p.probe_w) p.probe_w[(size_t)t * k + rank] = w;
       }
     }
+    for (int s = lane; s < S; s += 32) {
+      const int row = (E + s) * p.T + t;
+      rows[tt * (k + S) + k + s] = row;
+      p.perm_token[row] = t;
+      p.perm_slot[row] = k + s;
+      p.perm_w[row] = 1.0f;
+    }
   }
-
-  // the last block to finish groups the whole batch by expert
-  __threadfence();
   __syncthreads();
-  __shared__ int is_last;
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  group_by_expert(p, reinterpret_cast<int*>(rsm));
-  if (threadIdx.x == 0) *p.done = 0u;
-}
 
-__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ perm_token,
-                                                      const __nv_bfloat16* __restrict__ xhat,
-                                                      __nv_bfloat16* __restrict__ xperm, int rows,
-                                                      int d) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int cpr = d / 8;  // 16-byte chunks per row
-  const int64_t total = (int64_t)rows * cpr;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / cpr), c = (int)(i % cpr);
-    const int t = __ldg(perm_token + r);
-    reinterpret_cast<uint4*>(xperm + (size_t)r * d)[c] =
-        __ldg(reinterpret_cast<const uint4*>(xhat + (size_t)t * d) + c);
+  // copy each token's normalised row into its k + S expert rows
+  if (wr_ok) {
+    const int cpr = d / 8;  // 16-byte chunks per row
+    const int nslots = ntok * (k + S);
+    for (int i = tid; i < nslots * cpr; i += kRouteThreads) {
+      const int q = i / cpr, c = i - q * cpr;
+      const int tt = q / (k + S);
+      const int row = rows[q];
+      if (row >= 0)
+        reinterpret_cast<uint4*>(p.xperm + (size_t)row * d)[c] =
+            reinterpret_cast<const uint4*>(xb + tt * d)[c];
+    }
   }
 }
 
@@ -421,8 +304,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
 // chunks (c = tid, tid + 256, ...), then per warp, then over the warps in
 // order (the allocation-free greedy head reduces in the same order).
 __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;
@@ -487,23 +370,6 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStrea
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-}  // namespace
-
-size_t route_group_smem_bytes(int T, int k, int E) {
-  const size_t nw = ((size_t)T + 31) / 32;
-  return ((size_t)T * k + 2 * (size_t)E * nw + 4 * 300) * sizeof(int);
-}
-
-size_t route_smem_bytes(int tpb, int d, int E, int T, int k, bool wr_smem) {
-  const size_t a = (wr_smem ? (size_t)E * d * 2 : 0) + ((size_t)tpb * (d + E) + 64) * sizeof(float);
-  const size_t b = route_group_smem_bytes(T, k, E);
-  return a > b ? a : b;
-}
-
-bool route_wr_fits(int tpb, int d, int E) {
-  return (size_t)E * d * 2 + ((size_t)tpb * (d + E) + 64) * sizeof(float) <= 220 * 1024;
-}
-
 template <int SRC, int TPB>
 cudaError_t launch_route_t(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
   auto k = route_kernel<SRC, TPB>;
@@ -523,6 +389,17 @@ cudaError_t launch_route_src(const RouteParams& p, int grid, size_t smem, cudaSt
   }
 }
 
+}  // namespace
+
+size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem) {
+  return (wr_smem ? (size_t)E * d * 2 : 0) + (size_t)tpb * d * (4 + 2) +
+         ((size_t)tpb * E + 64) * sizeof(float) + (size_t)tpb * (k + S) * sizeof(int);
+}
+
+bool route_wr_fits(int tpb, int d, int E, int k, int S) {
+  return route_smem_bytes(tpb, d, E, k, S, true) <= 220 * 1024;
+}
+
 cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
   switch (p.src) {
     case kSrcEmbed: return launch_route_src<kSrcEmbed>(p, grid, smem, s, pdl);
@@ -531,19 +408,8 @@ cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream
   }
 }
 
-cudaError_t launch_scatter(const int32_t* perm_token, const __nv_bfloat16* xhat,
-                           __nv_bfloat16* xperm, int rows, int d, cudaStream_t s, bool pdl) {
-  const int64_t total = (int64_t)rows * (d / 8);
-  int grid = (int)((total + 255) / 256);
-  if (grid > 4096) grid = 4096;
-  if (grid < 1) grid = 1;
-  return launch_ex(scatter_kernel, dim3(grid), dim3(256), 0, s, pdl, perm_token, xhat, xperm, rows,
-                   d);
-}
-
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl) {
-  const int grid = p.T;
-  return launch_ex(final_kernel, dim3(grid), dim3(256), 0, s, pdl, p);
+  return launch_ex(final_kernel, dim3(p.T), dim3(256), 0, s, pdl, p);
 }
 
 }  // namespace mv

@@ -251,3 +251,133 @@ def test_host_argument_errors(tiny):
     with pytest.raises(B.MoeVerifyError) as e:
         ctx.layer(5, torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda"))
     assert e.value.code == B.ERR_ARG
+
+
+# ------------------------------------------------ skewed routing and the sweep
+
+@pytest.fixture(scope="module")
+def full_zipf(full):
+    """The full stack with the Zipf(s=1.2) router bias, room for 256 x 4 tokens."""
+    B = _B()
+    w = dict(full[1].w)
+    w["router_bias"] = S.router_bias(S.FULL_ZIPF)
+    ctx = B.MoeVerify(S.FULL_ZIPF, B.weights_to_device(w), max_batch=256, max_k=3)
+    torch.cuda.empty_cache()
+    yield ctx, O.Oracle(S.FULL_ZIPF, w)
+    ctx.close()
+
+
+def test_full_zipf_batch256_k3_sampled(full_zipf):
+    """Skewed routing, 1,024 verify tokens: one expert takes almost every
+    token (its rows are cut into several items).  Routing and residual stream
+    of every token come from the probes; 24 sampled tokens against the oracle."""
+    ctx, orc = full_zipf
+    B = _B()
+    ids = S.uniform_ids(256 * 4, S.SEED_START_IDS, 13, S.FULL.vocab).reshape(256, 4)
+    probe, pt = B.make_probe(S.FULL.n_layers, 1024, S.FULL)
+    tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=probe)
+    torch.cuda.synchronize()
+    assert ctx.sync_status() == B.OK
+    idx = pt["topk_idx"].cpu().numpy()
+    counts = np.bincount(idx[0].reshape(-1), minlength=64)
+    assert counts[0] > 512, counts[:8]           # the skew is there
+    sample = list(range(3, 1024, 43))
+    stats = check_tokens(orc, ids.reshape(-1), tg.cpu().numpy().reshape(-1), idx,
+                         pt["topk_w"].cpu().numpy(), pt["hidden"].cpu().numpy(), sample=sample)
+    print("zipf:", stats, "layer-0 expert counts (top 4):", sorted(counts)[-4:])
+
+
+@pytest.mark.parametrize("Bn", [1, 8, 32, 128])
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_sweep_shapes_sampled(full, Bn, K):
+    """The sweep's shapes (B in {1, 8, 32, 128} x K in {1, 2, 3}): every
+    block and the target of sampled tokens, teacher-forced."""
+    ctx, orc = full
+    B = _B()
+    if Bn > 32:
+        pytest.skip("covered by the 256-sequence context below")
+    T = Bn * (K + 1)
+    ids = S.uniform_ids(T, 61 + Bn, K, S.FULL.vocab).reshape(Bn, K + 1)
+    probe, pt = B.make_probe(S.FULL.n_layers, T, S.FULL)
+    tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=probe)
+    sample = sorted(set(np.linspace(0, T - 1, min(T, 4)).astype(int).tolist()))
+    check_tokens(orc, ids.reshape(-1), tg.cpu().numpy().reshape(-1), pt["topk_idx"].cpu().numpy(),
+                 pt["topk_w"].cpu().numpy(), pt["hidden"].cpu().numpy(), sample=sample)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_sweep_batch128_sampled(full_zipf_free, K):
+    ctx, orc = full_zipf_free
+    B = _B()
+    T = 128 * (K + 1)
+    ids = S.uniform_ids(T, 67, K, S.FULL.vocab).reshape(128, K + 1)
+    probe, pt = B.make_probe(S.FULL.n_layers, T, S.FULL)
+    tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=probe)
+    sample = sorted(set(np.linspace(0, T - 1, 4).astype(int).tolist()))
+    check_tokens(orc, ids.reshape(-1), tg.cpu().numpy().reshape(-1), pt["topk_idx"].cpu().numpy(),
+                 pt["topk_w"].cpu().numpy(), pt["hidden"].cpu().numpy(), sample=sample)
+
+
+@pytest.fixture(scope="module")
+def full_zipf_free(full):
+    """The full stack without bias, room for 128 x 4 tokens."""
+    B = _B()
+    ctx = B.MoeVerify(S.FULL, B.weights_to_device(full[1].w), max_batch=128, max_k=3)
+    torch.cuda.empty_cache()
+    yield ctx, full[1]
+    ctx.close()
+
+
+@pytest.mark.parametrize("Bn,K,p", [(8, 2, 0.576), (32, 3, 0.75), (1, 1, 0.576)])
+def test_decode_loop(full, Bn, K, p):
+    """A few decode iterations through step + accept on the GPU, drafts taken
+    from the oracle's greedy chain with probability p.  Each step's targets are
+    checked teacher-forced against the oracle (every block and the final
+    argmax, exact outside near ties); the commits are exactly the acceptance
+    rule applied to those targets.  Commits that differ from the oracle's own
+    free-running chain (drift across the 12 blocks) are counted, not failed."""
+    ctx, orc = full
+    B = _B()
+    V = S.FULL.vocab
+    src = S.DraftSource(p, V, K, seed=5)
+    last = S.start_ids(Bn, V, first=900).astype(np.int64)
+    memo = {}
+
+    def g(x):
+        if x not in memo:
+            memo[x] = orc.target(int(x))
+        return memo[x]
+
+    import concurrent.futures as fut
+    drift = 0
+    committed_total = 0
+    for step in range(3):
+        with fut.ThreadPoolExecutor(max_workers=threads()) as ex:
+            list(ex.map(g, sorted(set(last.tolist()))))
+        chains = np.zeros((Bn, K + 1), dtype=np.int64)
+        for b in range(Bn):
+            x = int(last[b])
+            for i in range(K + 1):
+                if i > 0 and x not in memo:
+                    memo[x] = orc.target(x)
+                x = g(x)
+                chains[b, i] = x
+        drafts = np.stack([src.drafts(b, step, chains[b, :K]) for b in range(Bn)])
+        T = Bn * (K + 1)
+        probe, pt = B.make_probe(S.FULL.n_layers, T, S.FULL)
+        tg = ctx.step(_i32(last), _i32(drafts), probe=probe)
+        com, alen = ctx.accept(_i32(drafts), tg)
+        tg, com, alen = tg.cpu().numpy(), com.cpu().numpy(), alen.cpu().numpy()
+        ids = np.concatenate([last.reshape(-1, 1), drafts], axis=1).reshape(-1)
+        sample = sorted(set(np.linspace(0, T - 1, min(T, 8)).astype(int).tolist()))
+        check_tokens(orc, ids, tg.reshape(-1), pt["topk_idx"].cpu().numpy(),
+                     pt["topk_w"].cpu().numpy(), pt["hidden"].cpu().numpy(), sample=sample)
+        wc, wl, _ = O.accept(drafts, tg, V)
+        assert np.array_equal(com, wc) and np.array_equal(alen, wl)
+        for b in range(Bn):
+            n = int(alen[b])
+            committed_total += n + 1
+            drift += int(np.sum(com[b, : n + 1] != chains[b, : n + 1]))
+            last[b] = int(com[b, n])
+    print(f"decode B={Bn} K={K} p={p}: {committed_total} committed, "
+          f"{drift} differ from the oracle's free-running chain")
