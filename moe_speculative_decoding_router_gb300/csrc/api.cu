@@ -8,7 +8,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/moe_verify.h"
+#include "moe_verify.h"
 #include "internal.h"
 
 

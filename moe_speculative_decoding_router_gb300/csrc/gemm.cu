@@ -50,13 +50,6 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
-  uint32_t lo = (uint32_t)v, hi = (uint32_t)(v >> 32);
-  lo = __shfl_xor_sync(0xffffffffu, lo, o);
-  hi = __shfl_xor_sync(0xffffffffu, hi, o);
-  return ((unsigned long long)hi << 32) | lo;
-}
-
 // Barriers and flags at the start of the control area.
 struct Ctrl {
   uint64_t* full;
@@ -653,15 +646,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float lv = __uint_as_float(v[j]);
-            unsigned long long key = valid ? argmax_key(lv, vid) : 0ull;
             if (p.logits && valid && c0 + j < it.n)
               p.logits[(size_t)(it.b_row + c0 + j) * p.V + vid] = lv;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const unsigned long long other = shfl_xor_u64(key, o);
-              key = other > key ? other : key;
-            }
-            keys[j] = key;
+            // warp argmax in two 32-bit reductions: the largest orderable
+            // logit, then the largest inverted id among the lanes holding it
+            // (= the lowest vocabulary id)
+            const unsigned long long k = valid ? argmax_key(lv, vid) : 0ull;
+            const uint32_t hi = (uint32_t)(k >> 32);
+            const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+            const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? (uint32_t)k : 0u);
+            keys[j] = ((unsigned long long)mh << 32) | ml;
           }
           ok = mbar_wait(&C.xempty[xb], (xu & 1u) ^ 1u, C.abort_flag, p.status);
           if (!ok) break;

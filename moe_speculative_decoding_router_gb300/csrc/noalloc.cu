@@ -14,7 +14,7 @@
 
 #include <mutex>
 
-#include "../../include/moe_verify.h"
+#include "moe_verify.h"
 #include "internal.h"
 #include "ptx.cuh"
 
