@@ -375,16 +375,8 @@ def run_ours(args, rank, world, local):
         with open(prof) as f:
             traffic = json.load(f).get("bytes_per_launch")
 
-    # max over ranks
-    vals = np.array([ms, e_s, tokens, e_tokens], dtype=np.float64)
     if dist:
-        t = torch.tensor(vals, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx[:2], op=dist.ReduceOp.MAX)
-        sm = t.clone()
-        dist.all_reduce(sm[2:], op=dist.ReduceOp.SUM)
-        ms, e_s = float(mx[0]), float(mx[1])
-        tokens, e_tokens = float(sm[2]), float(sm[3])
+        ms, e_s, tokens, e_tokens = whole_job(ms, e_s, tokens, e_tokens, dev)
     value = tokens / (ms / 1e3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -423,6 +415,18 @@ def run_ours(args, rank, world, local):
     ctx.close()
     if dist:
         dist.destroy_process_group()
+
+
+def whole_job(ms, e_s, tokens, e_tokens, device):
+    """Whole-job figures over the ranks of the default process group: the
+    slowest rank's device and end-to-end times, every rank's committed tokens."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, e_s, tokens, e_tokens], dtype=torch.float64, device=device)
+    mx, sm = t.clone(), t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(mx[1]), float(sm[2]), float(sm[3])
 
 
 # ------------------------------------------------------------ CPU baseline
