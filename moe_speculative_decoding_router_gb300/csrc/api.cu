@@ -40,7 +40,7 @@ struct moe_verify_ctx {
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
           *io_alen = nullptr;
-  CUtensorMap map_gu, map_dn, map_lm, map_x, map_a, map_f;
+  CUtensorMap map_gu, map_dn, map_lm, map_x, map_a;
   std::vector<void*> allocs;
   // profiling
   bool timing = false;
@@ -512,8 +512,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
   int e4 = encode_map(&c->map_x, c->xperm, d, c->rows_max, 16);
   int e5 = encode_map(&c->map_a, c->abuf, c->I_pad, c->rows_max, 16);
-  int e6 = encode_map(&c->map_f, c->xf, d, round_up(c->T_max, 16), 16);
-  if (e1 || e2 || e3 || e4 || e5 || e6) return fail(MOE_VERIFY_ERR_CUDA);
+  if (e1 || e2 || e3 || e4 || e5) return fail(MOE_VERIFY_ERR_CUDA);
 #undef AL
 #undef CKF
   *out = c;
@@ -563,9 +562,14 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   gp.targets = target_ids;
   gp.bad = ctx->bad;
   gp.done = ctx->done_lm;
+  // the normalised rows of one token chunk arrive as a single TMA box (rows
+  // past T_max read as zeros, rows in [T, T_max) are never used)
+  CUtensorMap map_f;
+  if (encode_map(&map_f, ctx->xf, ctx->d, round_up(ctx->T_max, 16), (uint32_t)sh.nch_lm))
+    return MOE_VERIFY_ERR_CUDA;
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_lmhead(ctx->map_lm, ctx->map_f, gp, ctx->num_sms, s, pdl));
+    CK(mv::launch_lmhead(ctx->map_lm, map_f, gp, ctx->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }

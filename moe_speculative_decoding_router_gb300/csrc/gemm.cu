@@ -8,8 +8,10 @@
 // All gate/up items come first, then all down items; item i runs on CTA
 // i mod gridDim.  A down item waits (bounded) until both SwiGLU halves of
 // every gate/up tile of its chunk of rows are written.
-// lmhead_kernel: [128 vocabulary rows] x [all verify tokens], epilogue the
-// running greedy argmax over the vocabulary.
+// lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
+// epilogue the running greedy argmax over the vocabulary.  The chunk's
+// normalised rows arrive as one TMA box per stage (the tensor map's box is
+// the chunk width): many small boxes per stage throttled the TMA unit.
 //
 // The weight rows sit on the MMA's M side (128) and the few tokens of an
 // expert on its N side (16..256), so every weight byte is streamed from HBM
@@ -541,8 +543,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int pi = i, pk = kb;
       LmItem pt = it;
       while (pre < p.stages && pi < n_items) {
-        const int npad = (pt.n + 15) & ~15;
-        mbar_arrive_expect_tx(&C.full[pre], (uint32_t)(kStageA + npad * 128));
+        mbar_arrive_expect_tx(&C.full[pre], (uint32_t)(kStageA + p.nch * 128));
         tma_load_2d(stages + (size_t)pre * stage_bytes, &mapA, &C.full[pre], pk * 64, pt.a_row,
                     pol_w);
         ++pre;
@@ -556,10 +557,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     for (int s = 0; s < pre; ++s) {
-      const int npad = (it.n + 15) & ~15;
-      uint8_t* sb = stages + (size_t)s * stage_bytes + kStageA;
-      for (int j = 0; j < npad; j += 16)
-        tma_load_2d(sb + j * 128, &mapB, &C.full[s], kb * 64, it.b_row + j, pol_x);
+      tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &mapB, &C.full[s], kb * 64,
+                  it.b_row, pol_x);
       if (++kb == p.kblocks) {
         kb = 0;
         i += gridDim.x;
@@ -574,16 +573,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     bool ok = true;
     while (i < n_items) {
-      const int npad = (it.n + 15) & ~15;
       if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
         ok = false;
         break;
       }
       uint8_t* sa = stages + (size_t)stage * stage_bytes;
-      mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + npad * 128));
+      mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + p.nch * 128));
       tma_load_2d(sa, &mapA, &C.full[stage], kb * 64, it.a_row, pol_w);
-      for (int j = 0; j < npad; j += 16)
-        tma_load_2d(sa + kStageA + j * 128, &mapB, &C.full[stage], kb * 64, it.b_row + j, pol_x);
+      tma_load_2d(sa + kStageA, &mapB, &C.full[stage], kb * 64, it.b_row, pol_x);
       ++issued;
       if (++stage == p.stages) {
         stage = 0;

@@ -149,10 +149,12 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
+  const int nch = (T + 15) / 16 * 16;
   CUtensorMap map_lm, map_xf;
-  // rows past V (the last vocabulary tile) and past T are read as zeros
+  // rows past V (the last vocabulary tile) and past T are read as zeros; the
+  // T normalised rows arrive as one box of nch rows
   if (!encode(&map_lm, lm_head, (uint64_t)d, (uint64_t)V, 128) ||
-      !encode(&map_xf, scratch, (uint64_t)d, (uint64_t)kMaxTokens, 16))
+      !encode(&map_xf, scratch, (uint64_t)d, (uint64_t)kMaxTokens, (uint32_t)nch))
     return MOE_VERIFY_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -160,7 +162,6 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
                                          rms_eps, scratch);
   if (cudaGetLastError() != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
 
-  const int nch = (T + 15) / 16 * 16;
   int cols = 32;
   while (cols < 2 * nch) cols <<= 1;
   mv::GemmParams gp = {};
