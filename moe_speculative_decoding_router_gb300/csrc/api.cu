@@ -40,7 +40,7 @@ struct moe_verify_ctx {
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
           *io_alen = nullptr;
-  CUtensorMap map_gu, map_dn, map_lm, map_x, map_a;
+  CUtensorMap map_gu, map_dn, map_lm;
   std::vector<void*> allocs;
   // profiling
   bool timing = false;
@@ -239,10 +239,14 @@ struct StepShape {
   int T, tpb, grid_route, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
   bool wr_smem;
   size_t route_smem;
+  // activation tiles of the expert FFN and the lm_head: one TMA box per stage,
+  // as wide as the item's chunk of rows (rows past the buffers read as zeros;
+  // rows past an item's own are loaded but never used)
+  CUtensorMap map_x, map_a, map_f;
 };
 
-StepShape shape_for(const moe_verify_ctx* c, int T) {
-  StepShape s;
+int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
+  StepShape& s = *out;
   s.T = T;
   // tokens per routing block: 1, 2, 4 or 8, enough blocks to cover the SMs
   const int want = (T + c->num_sms - 1) / c->num_sms;
@@ -262,7 +266,11 @@ StepShape shape_for(const moe_verify_ctx* c, int T) {
   s.tmem_cols = pow2_at_least(need);
   s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E, c->k, c->S);
   s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, c->k, c->S, s.wr_smem);
-  return s;
+  if (encode_map(&s.map_x, c->xperm, c->d, c->rows_max, (uint32_t)s.nch) ||
+      encode_map(&s.map_a, c->abuf, c->I_pad, c->rows_max, (uint32_t)s.nch) ||
+      encode_map(&s.map_f, c->xf, c->d, round_up(c->T_max, 16), (uint32_t)s.nch_lm))
+    return MOE_VERIFY_ERR_CUDA;
+  return MOE_VERIFY_OK;
 }
 
 int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int32_t* context_ids,
@@ -335,7 +343,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   fp.done = c->done_ffn;
   {
     Timed tm(c, 0, s);
-    CK(mv::launch_ffn(c->map_gu, c->map_x, c->map_dn, c->map_a, fp, c->num_sms, s, pdl));
+    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, fp, c->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -510,9 +518,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   int e1 = encode_map(&c->map_gu, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 128);
   int e2 = encode_map(&c->map_dn, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 128);
   int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
-  int e4 = encode_map(&c->map_x, c->xperm, d, c->rows_max, 16);
-  int e5 = encode_map(&c->map_a, c->abuf, c->I_pad, c->rows_max, 16);
-  if (e1 || e2 || e3 || e4 || e5) return fail(MOE_VERIFY_ERR_CUDA);
+  if (e1 || e2 || e3) return fail(MOE_VERIFY_ERR_CUDA);
 #undef AL
 #undef CKF
   *out = c;
@@ -523,7 +529,8 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
                         int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
                         cudaStream_t s) {
   const int T = B * (K + 1);
-  StepShape sh = shape_for(ctx, T);
+  StepShape sh;
+  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
   const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
     int rc = run_layer(ctx, l, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
@@ -562,14 +569,9 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   gp.targets = target_ids;
   gp.bad = ctx->bad;
   gp.done = ctx->done_lm;
-  // the normalised rows of one token chunk arrive as a single TMA box (rows
-  // past T_max read as zeros, rows in [T, T_max) are never used)
-  CUtensorMap map_f;
-  if (encode_map(&map_f, ctx->xf, ctx->d, round_up(ctx->T_max, 16), (uint32_t)sh.nch_lm))
-    return MOE_VERIFY_ERR_CUDA;
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_lmhead(ctx->map_lm, map_f, gp, ctx->num_sms, s, pdl));
+    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, ctx->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -609,7 +611,8 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   if (layer < 0 || layer >= ctx->L || T < 1 || T > ctx->T_max) return MOE_VERIFY_ERR_ARG;
   if (!aligned16(h_in) || !aligned16(h_out)) return MOE_VERIFY_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  StepShape sh = shape_for(ctx, T);
+  StepShape sh;
+  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
   int rc = run_layer(ctx, layer, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
                      true);
   if (rc != MOE_VERIFY_OK) return rc;

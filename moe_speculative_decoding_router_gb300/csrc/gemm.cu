@@ -298,12 +298,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int issued = 0;
       if (hit) {
         // the weight tiles are already in place: add the activation tiles
-        const int npad = (it.n + 15) & ~15;
         for (int s = 0; s < pre; ++s) {
           uint8_t* sb = stages + (size_t)s * stage_bytes + kStageA;
-          mbar_arrive_expect_tx(&C.full[s], (uint32_t)(npad * 128));
-          for (int j = 0; j < npad; j += 16)
-            tma_load_2d(sb + j * 128, &map_x, &C.full[s], s * 64, it.row0 + j, pol_x);
+          mbar_arrive_expect_tx(&C.full[s], (uint32_t)(p.nch * 128));
+          tma_load_2d(sb, &map_x, &C.full[s], s * 64, it.row0, pol_x);
         }
         issued = pre;
         stage = pre;
@@ -319,14 +317,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       while (ok && i < n_items) {
-        const int npad = (it.n + 15) & ~15;
         if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
           ok = false;
           break;
         }
         uint8_t* sa = stages + (size_t)stage * stage_bytes;
         uint8_t* sb = sa + kStageA;
-        mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + npad * 128));
+        mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(kStageA + p.nch * 128));
         tma_load_2d(sa, it.down ? &map_dn : &map_gu, &C.full[stage], kb * 64, it.a_row, pol_w);
         if (it.down && kb == 0) {
           // both SwiGLU halves of every gate/up tile of this chunk are written
@@ -347,9 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         // on a failed wait the activation tiles are still loaded (stale rows),
         // so that the stage's byte count completes and the drain ends
-        for (int j = 0; j < npad; j += 16)
-          tma_load_2d(sb + j * 128, it.down ? &map_a : &map_x, &C.full[stage], kb * 64,
-                      it.row0 + j, pol_x);
+        tma_load_2d(sb, it.down ? &map_a : &map_x, &C.full[stage], kb * 64, it.row0, pol_x);
         ++issued;
         if (++stage == p.stages) {
           stage = 0;
