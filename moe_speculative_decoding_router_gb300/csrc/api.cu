@@ -40,7 +40,7 @@ struct moe_verify_ctx {
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
           *io_alen = nullptr;
-  CUtensorMap map_gu, map_dn, map_lm;
+  CUtensorMap map_gu, map_dn, map_lm, map_wr;
   std::vector<void*> allocs;
   // profiling
   bool timing = false;
@@ -298,6 +298,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   rp.y = c->y;
   rp.gain = c->gain + (size_t)l * c->d;
   rp.Wr = c->router + (size_t)l * c->E * c->d;
+  rp.wr_row = l * c->E;
   rp.bias = c->has_bias ? c->bias + (size_t)l * c->E : nullptr;
   rp.bad = c->bad;
   rp.status = c->status;
@@ -313,7 +314,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   rp.perm_w = c->perm_w;
   {
     Timed tm(c, 3, s);
-    CK(mv::launch_route(rp, sh.grid_route, sh.route_smem, s, pdl));
+    CK(mv::launch_route(c->map_wr, rp, sh.grid_route, sh.route_smem, s, pdl));
   }
   mv::FfnParams fp = {};
   fp.cnt = c->cnt;
@@ -341,6 +342,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   fp.kS = c->kS;
   fp.status = c->status;
   fp.done = c->done_ffn;
+  fp.next_item = reinterpret_cast<int32_t*>(c->done_ffn + 1);
   {
     Timed tm(c, 0, s);
     CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, fp, c->num_sms, s, pdl));
@@ -518,7 +520,9 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   int e1 = encode_map(&c->map_gu, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 128);
   int e2 = encode_map(&c->map_dn, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 128);
   int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
-  if (e1 || e2 || e3) return fail(MOE_VERIFY_ERR_CUDA);
+  // router weights of all layers: boxes of 64 columns x E rows
+  int e4 = encode_map(&c->map_wr, c->router, d, (uint64_t)L * E, (uint32_t)E);
+  if (e1 || e2 || e3 || e4) return fail(MOE_VERIFY_ERR_CUDA);
 #undef AL
 #undef CKF
   *out = c;

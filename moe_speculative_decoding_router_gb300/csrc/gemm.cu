@@ -5,9 +5,12 @@
 //            epilogue a = bf16(silu(g) * u)                  (SwiGLU)
 //   down     [128 rows of one expert's down projection] x [the same rows' a]
 //            epilogue y[token, slot] = p * (a W_d^T)         (weighted combine)
-// All gate/up items come first, then all down items; item i runs on CTA
-// i mod gridDim.  A down item waits (bounded) until both SwiGLU halves of
-// every gate/up tile of its chunk of rows are written.
+// All gate/up items come first, then all down items.  CTA c starts with item
+// c; later items are claimed in order from a global counter (one claim ahead
+// of use), so CTAs that stream faster take more items and all finish within
+// about one item of each other.  A down item waits (bounded) until both
+// SwiGLU halves of every gate/up tile of its chunk of rows are written; the
+// items it waits for were claimed earlier and have no waits of their own.
 // lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
 // epilogue the running greedy argmax over the vocabulary.  The chunk's
 // normalised rows arrive as one TMA box per stage (the tensor map's box is
@@ -33,6 +36,8 @@ constexpr int kGemmThreads = 192;
 constexpr int kStageA = 128 * 128;  // 128 weight rows x 64 bf16
 constexpr int kXbufBytes = 2 * 16 * 64 * 4;
 constexpr int kCtrlBytes = 1024;
+constexpr int kMaxExperts = 264;  // routed (<= 256) + shared (<= 8)
+constexpr int kQueue = 8;         // claimed items in flight inside a CTA
 constexpr int kListBytes = 6144;  // per-expert counts and prefix sums (<= 264 experts)
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -62,6 +67,9 @@ struct Ctrl {
   uint64_t* xfull;
   uint64_t* xempty;
   uint64_t* spec;
+  uint64_t* q_full;   // [kQueue] item queue: producer -> MMA issuer and epilogue
+  uint64_t* q_empty;  // [kQueue]
+  int* q_item;        // [kQueue]
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -76,7 +84,10 @@ __device__ __forceinline__ Ctrl ctrl_at(uint8_t* base, int stages) {
   c.xfull = c.drain + 1;
   c.xempty = c.xfull + 2;
   c.spec = c.xempty + 2;
-  c.tmem_slot = reinterpret_cast<uint32_t*>(c.spec + 1);
+  c.q_full = c.spec + 1;
+  c.q_empty = c.q_full + kQueue;
+  c.q_item = reinterpret_cast<int*>(c.q_empty + kQueue);
+  c.tmem_slot = reinterpret_cast<uint32_t*>(c.q_item + kQueue);
   c.abort_flag = reinterpret_cast<volatile int*>(c.tmem_slot + 1);
   return c;
 }
@@ -95,6 +106,10 @@ __device__ __forceinline__ void init_ctrl(const Ctrl& c, int stages, uint32_t xf
   }
   mbar_init(c.drain, 1);
   mbar_init(c.spec, 1);
+  for (int q = 0; q < kQueue; ++q) {
+    mbar_init(&c.q_full[q], 1);
+    mbar_init(&c.q_empty[q], 5);  // the MMA issuer and the four epilogue warps
+  }
   *c.abort_flag = 0;
   fence_mbar_init();
 }
@@ -117,6 +132,30 @@ __device__ __forceinline__ void producer_drain(const Ctrl& c, int issued, int st
     while (!mbar_try_wait(&c.full[s], par) && globaltimer_ns() - t0 < kWaitLimitNs) {
     }
   }
+}
+
+// Item queue inside a CTA.  The producer pushes each item it starts (-1 when
+// there are no more); the MMA issuer and every epilogue warp pop them in the
+// same order.  n counts the pushes (pops) made so far.
+__device__ __forceinline__ bool queue_push(const Ctrl& c, int n, int item, uint32_t* status) {
+  const int q = n % kQueue;
+  const uint32_t use = (uint32_t)(n / kQueue);
+  if (!mbar_wait(&c.q_empty[q], (use & 1u) ^ 1u, c.abort_flag, status)) return false;
+  c.q_item[q] = item;
+  mbar_arrive(&c.q_full[q]);
+  return true;
+}
+
+// Returns the item, or -1 at the end (also when a wait gave up).  Every lane
+// of the calling warp gets the value; lane 0 releases the slot.
+__device__ __forceinline__ int queue_pop(const Ctrl& c, int n, uint32_t* status, bool warp_wide) {
+  const int q = n % kQueue;
+  const uint32_t use = (uint32_t)(n / kQueue);
+  if (!mbar_wait(&c.q_full[q], use & 1u, c.abort_flag, status)) return -1;
+  const int item = c.q_item[q];
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&c.q_empty[q]);
+  return item;
 }
 
 // Issues the MMAs of one item (kblocks stages) into TMEM columns tmem_d.
@@ -240,12 +279,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // per-expert rows, chunk and item prefix sums: one warp, 32 experts per
     // round, shuffle scans with a running carry
+    // all counts are loaded before the scans (one memory round trip)
+    constexpr int kMaxRounds = (kMaxExperts + 31) / 32;
+    int craw[kMaxRounds];
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+      const int e = r * 32 + lane;
+      craw[r] = (e < E) ? __ldcg(p.cnt + e) : p.T;
+    }
     int cc = 0, cg = 0, cd = 0;
-    for (int e0 = 0; e0 < nE; e0 += 32) {
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+      const int e0 = r * 32;
+      if (e0 >= nE) break;
       const int e = e0 + lane;
       int c = 0, ch = 0;
       if (e < nE) {
-        c = (e < E) ? min(__ldcg(p.cnt + e), p.T) : p.T;
+        c = min(craw[r], p.T);
         ch = (c + p.nch - 1) / p.nch;
         L.cnt[e] = c;
       }
@@ -287,12 +337,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      int i = blockIdx.x, kb = 0;
+      int i = (int)blockIdx.x < n_items ? (int)blockIdx.x : -1, kb = 0;
       FItem it = {};
-      if (i < n_items) it = decode(p, L, nE, n_gu, i);
+      // announce item `item` to the MMA issuer and the epilogue, and claim
+      // the item after it (the claim's result is first used when `item` is
+      // fully issued, so its latency is hidden)
+      int nq = 0, next_raw = 0;
+      auto start_item = [&](int item) -> bool {
+        if (!queue_push(C, nq++, item, p.status)) return false;
+        if (item >= 0) {
+          it = decode(p, L, nE, n_gu, item);
+          next_raw = atomicAdd(p.next_item, 1);
+        }
+        return true;
+      };
+      auto next_item = [&]() -> int {
+        const int c = next_raw + (int)gridDim.x;
+        return c < n_items ? c : -1;
+      };
       bool ok = true;
       if (pre > 0) ok = mbar_wait(C.spec, 0, C.abort_flag, p.status);  // speculative tiles landed
-      const bool hit = ok && pre > 0 && i < n_items && !it.down && it.a_row == guess_row;
+      ok = ok && start_item(i);
+      const bool hit = ok && pre > 0 && i >= 0 && !it.down && it.a_row == guess_row;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -308,15 +374,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         kb = pre;
         if (kb == it.kblocks) {
           kb = 0;
-          i += gridDim.x;
-          if (i < n_items) it = decode(p, L, nE, n_gu, i);
+          i = next_item();
+          ok = start_item(i);
         }
         if (stage == p.stages) {
           stage = 0;
           phase = 1;
         }
       }
-      while (ok && i < n_items) {
+      while (ok && i >= 0) {
         if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
           ok = false;
           break;
@@ -352,8 +418,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (++kb == it.kblocks) {
           kb = 0;
-          i += gridDim.x;
-          if (i < n_items) it = decode(p, L, nE, n_gu, i);
+          i = next_item();
+          if (!start_item(i)) ok = false;
         }
       }
       if (!ok) producer_drain(C, issued, p.stages);
@@ -361,9 +427,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, local = 0;
+      int stage = 0;
       uint32_t phase = 0;
-      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+      for (int local = 0;; ++local) {
+        const int i = queue_pop(C, local, p.status, false);
+        if (i < 0) break;
         const FItem it = decode(p, L, nE, n_gu, i);
         const int npad = (it.n + 15) & ~15;
         const int buf = local & 1;
@@ -382,9 +450,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------ epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    int local = 0;
     uint32_t chunk_seq = 0;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+    for (int local = 0;; ++local) {
+      const int i = queue_pop(C, local, p.status, true);
+      if (i < 0) break;
       const FItem it = decode(p, L, nE, n_gu, i);
       const int npad = (it.n + 15) & ~15;
       const int buf = local & 1;
@@ -477,7 +546,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (is_last) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) p.cnt_clear[e] = 0;
     for (int c = threadIdx.x; c < s_totals[2]; c += blockDim.x) p.dep[c] = 0;
-    if (threadIdx.x == 0) *p.done = 0u;
+    if (threadIdx.x == 0) {
+      *p.next_item = 0;
+      *p.done = 0u;
+    }
   }
 }
 

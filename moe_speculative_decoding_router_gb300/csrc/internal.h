@@ -31,6 +31,7 @@ struct RouteParams {
   const float* y;              // [T, k+S, d] expert outputs of the previous block
   const float* gain;           // [d]
   const __nv_bfloat16* Wr;     // [E, d]
+  int wr_row;                  // first row of this layer's router in the router tensor map
   const float* bias;           // [E] or nullptr
   int32_t* bad;                // [T]
   uint32_t* status;
@@ -64,7 +65,8 @@ struct FfnParams {
   float* y;                    // [T, kS, d]
   int d, kS;
   uint32_t* status;
-  unsigned int* done;
+  unsigned int* done;          // CTAs finished (the last one clears the counters)
+  int* next_item;              // items claimed past the first gridDim (zero on entry)
 };
 
 struct FinalParams {
@@ -111,7 +113,8 @@ size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem);
 bool route_wr_fits(int tpb, int d, int E, int k, int S);
 
 // Launchers (enqueue only).  `pdl` requests programmatic dependent launch.
-cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int grid, size_t smem,
+                         cudaStream_t s, bool pdl);
 cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_dn, const CUtensorMap& map_a, const FfnParams& p,
                        int grid, cudaStream_t s, bool pdl);

@@ -55,36 +55,56 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
   return make_float4(a.x, a.y, c.x, c.y);
 }
 
-// Residual stream entering the block for chunk c (4 floats) of token t.
-template <int SRC>
-__device__ __forceinline__ float4 residual_chunk(const RouteParams& p, int t, int c,
-                                                 const __nv_bfloat16* erow) {
-  const int d = p.d, nc = d / 4;
-  if (SRC == kSrcEmbed) return bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(erow) + c));
-  if (SRC == kSrcBf16)
-    return bf16x4_to_f4(__ldg(reinterpret_cast<const uint2*>(p.h_in + (size_t)t * d) + c));
-  const int kS = p.k + p.S;
-  float4 v = reinterpret_cast<const float4*>(p.h + (size_t)t * d)[c];
-  const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * kS * d) + c;
-  // routed slots in selection order, then shared experts, summed first
-  float4 acc = yr[0];
-#pragma unroll 8
-  for (int s = 1; s < kS; ++s) {
-    const float4 u = yr[(size_t)s * nc];
-    acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
+// Bulk copy of `bytes` (16-byte aligned, multiple of 16) into shared memory,
+// completing on `bar`, in pieces of at most 16 KB.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, size_t bytes, uint64_t* bar) {
+  for (size_t off = 0; off < bytes; off += 16384) {
+    const uint32_t n = (uint32_t)min((size_t)16384, bytes - off);
+    bulk_load(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off, n, bar);
   }
-  v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
-  return v;
 }
 
-// Stage 1 for the block's tokens t0 .. t0+ntok-1, all threads: build h (and
-// write it back), RMSNorm; the normalised row goes to xs [TPB, d] (widened
-// bf16 values, for the router) and xb [TPB, d] (bf16, for the expert rows).
+// acc[j] = y[0][c_j] + y[1][c_j] + ... + y[kS-1][c_j] (fp32, slot order) for
+// NC float4 chunks of one token's expert outputs y [kS, nc].  Slots go in
+// fixed groups of 8 whose loads are all issued before the first add, so a
+// token costs one memory round trip per 8 slots.
+template <int NC>
+__device__ __forceinline__ void sum_slots(const float4* __restrict__ yr, int nc, int kS,
+                                          const int (&c)[NC], float4 (&acc)[NC]) {
+  for (int s0 = 0; s0 < kS; s0 += 8) {
+    float4 u[8][NC];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        u[q][j] = (s0 + q < kS) ? __ldcg(yr + (size_t)(s0 + q) * nc + c[j])
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        if (s0 + q == 0) {
+          acc[j] = u[q][j];
+        } else if (s0 + q < kS) {
+          acc[j].x += u[q][j].x; acc[j].y += u[q][j].y;
+          acc[j].z += u[q][j].z; acc[j].w += u[q][j].w;
+        }
+      }
+  }
+}
+
+// Stage 1 for the block's tokens t0 .. t0+ntok-1, all threads: build the
+// residual stream h entering the block (and write it back), RMSNorm, and the
+// normalised bf16 row xb [TPB, d] (row pitch xpitch elements).  For the combine source xs [TPB, d] already
+// holds the tokens' h rows and gs [d] the gain (bulk copies issued before the
+// wait); the expert outputs of the previous block are summed in slot order
+// (routed slots in selection order, then the shared experts) and added to h.
 template <int SRC, int TPB>
-__device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs,
-                           __nv_bfloat16* xb, float* red) {
+__device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, const float* gs,
+                           __nv_bfloat16* xb, int xpitch, float* red) {
+  constexpr int kPass = 2;  // float4 chunks per thread whose loads are issued together
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int d = p.d, nc = d / 4;
+  const int d = p.d, nc = d / 4, kS = p.k + p.S;
   float ss[TPB];
 #pragma unroll
   for (int i = 0; i < TPB; ++i) ss[i] = 0.f;
@@ -92,23 +112,51 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs,
   for (int tt = 0; tt < TPB; ++tt) {
     if (tt >= ntok) break;
     const int t = t0 + tt;
-    const __nv_bfloat16* erow = nullptr;
-    if (SRC == kSrcEmbed) {
-      const int b = t / (p.K + 1), i = t % (p.K + 1);
-      const int id = (i == 0) ? p.context_ids[b] : p.draft_ids[(size_t)b * p.K + (i - 1)];
-      const bool ok = (id >= 0 && id < p.V);
-      if (tid == 0) {
-        p.bad[t] = ok ? 0 : 1;
-        if (!ok) atomicOr(p.status, kErrIdRange);
+    float4* hx = reinterpret_cast<float4*>(xs + tt * d);
+    float4* hg = reinterpret_cast<float4*>(p.h + (size_t)t * d);
+    float4* hp = p.probe_hidden ? reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d) : nullptr;
+    if (SRC == kSrcCombine) {
+      const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * kS * d);
+      for (int c0 = tid; c0 < nc; c0 += kPass * kRouteThreads) {
+        float4 acc[kPass];
+        int cj[kPass];
+#pragma unroll
+        for (int j = 0; j < kPass; ++j) cj[j] = min(c0 + j * kRouteThreads, nc - 1);
+        sum_slots<kPass>(yr, nc, kS, cj, acc);
+#pragma unroll
+        for (int j = 0; j < kPass; ++j) {
+          const int c = c0 + j * kRouteThreads;
+          if (c < nc) {
+            float4 v = hx[c];
+            v.x += acc[j].x; v.y += acc[j].y; v.z += acc[j].z; v.w += acc[j].w;
+            hx[c] = v;
+            hg[c] = v;
+            if (hp) hp[c] = v;
+            ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+          }
+        }
       }
-      erow = p.embed + (size_t)(ok ? id : 0) * d;
-    }
-    for (int c = tid; c < nc; c += kRouteThreads) {
-      const float4 v = residual_chunk<SRC>(p, t, c, erow);
-      reinterpret_cast<float4*>(p.h + (size_t)t * d)[c] = v;
-      if (p.probe_hidden) reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d)[c] = v;
-      reinterpret_cast<float4*>(xs + tt * d)[c] = v;
-      ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    } else {
+      const uint2* src;
+      if (SRC == kSrcEmbed) {
+        const int b = t / (p.K + 1), i = t % (p.K + 1);
+        const int id = (i == 0) ? p.context_ids[b] : p.draft_ids[(size_t)b * p.K + (i - 1)];
+        const bool ok = (id >= 0 && id < p.V);
+        if (tid == 0) {
+          p.bad[t] = ok ? 0 : 1;
+          if (!ok) atomicOr(p.status, kErrIdRange);
+        }
+        src = reinterpret_cast<const uint2*>(p.embed + (size_t)(ok ? id : 0) * d);
+      } else {
+        src = reinterpret_cast<const uint2*>(p.h_in + (size_t)t * d);
+      }
+      for (int c = tid; c < nc; c += kRouteThreads) {
+        const float4 v = bf16x4_to_f4(__ldg(src + c));
+        hx[c] = v;
+        hg[c] = v;
+        if (hp) hp[c] = v;
+        ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
     }
   }
 #pragma unroll
@@ -126,113 +174,149 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs,
     for (int w = 0; w < kRouteWarps; ++w) tot += red[w * 8 + tt];
     const float r = rsqrtf(tot / (float)d + p.eps);
     for (int c = tid; c < nc; c += kRouteThreads) {
-      float4 v = reinterpret_cast<const float4*>(xs + tt * d)[c];
-      const float4 g = __ldg(reinterpret_cast<const float4*>(p.gain) + c);
-      __nv_bfloat16 q0 = __float2bfloat16_rn(v.x * r * g.x);
-      __nv_bfloat16 q1 = __float2bfloat16_rn(v.y * r * g.y);
-      __nv_bfloat16 q2 = __float2bfloat16_rn(v.z * r * g.z);
-      __nv_bfloat16 q3 = __float2bfloat16_rn(v.w * r * g.w);
-      __nv_bfloat162 lo = __halves2bfloat162(q0, q1), hi = __halves2bfloat162(q2, q3);
+      const float4 v = reinterpret_cast<const float4*>(xs + tt * d)[c];
+      const float4 g = reinterpret_cast<const float4*>(gs)[c];
+      __nv_bfloat162 lo = __halves2bfloat162(__float2bfloat16_rn(v.x * r * g.x),
+                                             __float2bfloat16_rn(v.y * r * g.y));
+      __nv_bfloat162 hi = __halves2bfloat162(__float2bfloat16_rn(v.z * r * g.z),
+                                             __float2bfloat16_rn(v.w * r * g.w));
       uint2 packed;
       packed.x = *reinterpret_cast<uint32_t*>(&lo);
       packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(xb + tt * d)[c] = packed;
-      v = make_float4(__bfloat162float(q0), __bfloat162float(q1), __bfloat162float(q2),
-                      __bfloat162float(q3));
-      reinterpret_cast<float4*>(xs + tt * d)[c] = v;
+      reinterpret_cast<uint2*>(xb + tt * xpitch)[c] = packed;
     }
   }
 }
 
-template <int SRC, int TPB>
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
-  extern __shared__ __align__(128) float rsm[];
+// Router-logit partition over the warps: 16-expert tiles x K splits.
+__host__ __device__ inline int route_ksplit(int E) {
+  const int n_mt = (E + 15) / 16;
+  return n_mt >= 8 ? 1 : 8 / n_mt;
+}
+
+// Shared-memory bytes of the staged router weights: d/64 panels of E rows x
+// 128 bytes (64 bf16), 128-byte swizzled, each panel 1024-byte aligned.
+__host__ __device__ inline size_t route_wr_panel(int E) { return (size_t)((E + 7) / 8) * 1024; }
+
+// WR: the router weights are staged in shared memory by TMA (else read
+// through L1).
+template <int SRC, int TPB, bool WR>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const __grid_constant__ CUtensorMap map_wr, RouteParams p) {
+  extern __shared__ __align__(1024) uint8_t rsm_raw[];
+  uint8_t* rsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) &
+                                            ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = p.d, E = p.E, k = p.k, S = p.S;
   const int t0 = blockIdx.x * TPB;
   const int ntok = min(TPB, p.T - t0);
-  // shared memory: [router weights E x d bf16, when staged] [xs TPB x d fp32]
-  // [xb TPB x d bf16] [zs TPB x E] [red 64] [rows TPB x (k+S) ints]
-  const size_t wr_bytes = p.wr_smem ? (size_t)E * d * 2 : 0;
-  __nv_bfloat16* wr_s = reinterpret_cast<__nv_bfloat16*>(rsm);
-  float* xs = reinterpret_cast<float*>(reinterpret_cast<char*>(rsm) + wr_bytes);
+  const int n_mt = (E + 15) / 16, ksplit = route_ksplit(E);
+  // normalised bf16 rows are padded by 16 bytes so that the B-fragment loads
+  // of the 8 token rows fall in distinct shared-memory banks
+  const int pitch = d + 8;
+  // shared memory: [router weights, when staged] [gain d fp32] [xs TPB x d fp32]
+  // [xb TPB x pitch bf16] [partial logits ksplit x 16n_mt x 8] [zs TPB x E]
+  // [red 64] [rows TPB x (k+S)]
+  const size_t panel = route_wr_panel(E);
+  const size_t wr_bytes = WR ? (size_t)(d / 64) * panel : 0;
+  uint8_t* wr_s = rsm;
+  float* gs = reinterpret_cast<float*>(rsm + wr_bytes);
+  float* xs = gs + d;
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + TPB * d);
-  float* zs = reinterpret_cast<float*>(xb + TPB * d);
+  float* part = reinterpret_cast<float*>(xb + TPB * pitch);
+  float* zs = part + ksplit * n_mt * 16 * 8;
   float* red = zs + TPB * E;
   int* rows = reinterpret_cast<int*>(red + 64);
-  __shared__ __align__(8) uint64_t wr_bar;
+  __shared__ __align__(8) uint64_t hx_bar, wr_bar;
   __shared__ int abort_flag;
 
-  // The router weights do not depend on earlier kernels: start their copy
-  // into shared memory before waiting for the previous kernel.
-  if (p.wr_smem && tid == 0) {
+  // Before waiting for the previous kernel: the gain and the router weights
+  // (static), and for the combine source the tokens' h rows, which the
+  // routing kernel two launches back wrote (a kernel lets its dependents start
+  // only after its own wait, so that kernel is complete here).
+  if (tid == 0) {
     abort_flag = 0;
+    mbar_init(&hx_bar, 1);
     mbar_init(&wr_bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&wr_bar, (uint32_t)wr_bytes);
-    const char* src = reinterpret_cast<const char*>(p.Wr);
-    char* dst = reinterpret_cast<char*>(wr_s);
-    for (size_t off = 0; off < wr_bytes; off += 16384) {
-      const uint32_t n = (uint32_t)min((size_t)16384, wr_bytes - off);
-      bulk_load(dst + off, src + off, n, &wr_bar);
+    const size_t h_bytes = (SRC == kSrcCombine) ? (size_t)ntok * d * 4 : 0;
+    mbar_arrive_expect_tx(&hx_bar, (uint32_t)((size_t)d * 4 + h_bytes));
+    bulk_copy(gs, p.gain, (size_t)d * 4, &hx_bar);
+    if (h_bytes) bulk_copy(xs, p.h + (size_t)t0 * d, h_bytes, &hx_bar);
+    if (WR) {
+      const uint64_t pol = policy_evict_last();
+      mbar_arrive_expect_tx(&wr_bar, (uint32_t)((size_t)E * d * 2));
+      for (int pn = 0; pn < d / 64; ++pn)
+        tma_load_2d(wr_s + (size_t)pn * panel, &map_wr, &wr_bar, pn * 64, p.wr_row, pol);
     }
   }
+  for (int i = tid; i < TPB * (k + S); i += kRouteThreads) rows[i] = -1;
+  __syncthreads();
   // Wait for the previous kernel, then let dependents start: a kernel two
   // launches later may then read what the kernel before this one wrote.
   pdl_wait();
   pdl_launch_dependents();
-  block_norm<SRC, TPB>(p, t0, ntok, xs, xb, red);
+  bool ok = mbar_wait(&hx_bar, 0, &abort_flag, p.status);
+  if (ok) block_norm<SRC, TPB>(p, t0, ntok, xs, gs, xb, pitch, red);
   __syncthreads();
-  bool wr_ok = true;
-  if (p.wr_smem) wr_ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
-  for (int i = tid; i < TPB * (k + S); i += kRouteThreads) rows[i] = -1;
+  if (WR && ok) ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
 
-  // router logits: warp w computes experts 8w .. 8w+7 (then + 64, ...) for
-  // every token of the block, eight independent accumulation chains per lane
-  const __nv_bfloat16* wsrc = p.wr_smem ? wr_s : p.Wr;
-  for (int e0 = warp * 8; e0 < E && wr_ok; e0 += kRouteWarps * 8) {
-    float acc[8][TPB];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int tt = 0; tt < TPB; ++tt) acc[j][tt] = 0.f;
-    for (int c = lane; c < d / 8; c += 32) {
-      float4 xa[TPB], xv[TPB];
-#pragma unroll
-      for (int tt = 0; tt < TPB; ++tt) {
-        const float4* x4 = reinterpret_cast<const float4*>(xs + tt * d + c * 8);
-        xa[tt] = x4[0];
-        xv[tt] = x4[1];
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = min(e0 + j, E - 1);
-        const uint4* wrow = reinterpret_cast<const uint4*>(wsrc + (size_t)e * d);
-        float w8[8];
-        unpack8(p.wr_smem ? wrow[c] : __ldg(wrow + c), w8);
-#pragma unroll
-        for (int tt = 0; tt < TPB; ++tt) {
-          float a = acc[j][tt];
-          a = fmaf(w8[0], xa[tt].x, a);
-          a = fmaf(w8[1], xa[tt].y, a);
-          a = fmaf(w8[2], xa[tt].z, a);
-          a = fmaf(w8[3], xa[tt].w, a);
-          a = fmaf(w8[4], xv[tt].x, a);
-          a = fmaf(w8[5], xv[tt].y, a);
-          a = fmaf(w8[6], xv[tt].z, a);
-          a = fmaf(w8[7], xv[tt].w, a);
-          acc[j][tt] = a;
+  // Router logits on the tensor cores: z^T = W_r xhat^T as 16x8x16 tiles,
+  // rows = experts, columns = the block's tokens (columns >= ntok are not
+  // used), fp32 accumulation.  Warp unit u covers expert tile u % n_mt and
+  // the u / n_mt-th of the K range, alternating two accumulators; the
+  // partial sums are added in K-split order.
+  if (ok) {
+    const int ksteps = d / 16;
+    const int kper = (ksteps + ksplit - 1) / ksplit;
+    const int g = lane >> 2, t4 = lane & 3;
+    const __nv_bfloat16* xrow = xb + (size_t)min(g, TPB - 1) * pitch + 2 * t4;
+    for (int u = warp; u < n_mt * ksplit; u += kRouteWarps) {
+      const int m0 = (u % n_mt) * 16, ks = u / n_mt;
+      const int kb = ks * kper, ke = min(ksteps, kb + kper);
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // this lane's ldmatrix row (WR: row r, 16-byte chunk c of a panel sits
+      // at r * 128 + ((c ^ (r % 8)) * 16)) or fragment rows (direct loads)
+      const int mi = lane >> 3;
+      const int ar = min(m0 + (lane & 7) + (mi & 1) * 8, E - 1);
+      const uint8_t* arow = wr_s + (size_t)ar * 128;
+      const __nv_bfloat16* r0 = p.Wr + (size_t)min(m0 + g, E - 1) * d + 2 * t4;
+      const __nv_bfloat16* r1 = p.Wr + (size_t)min(m0 + g + 8, E - 1) * d + 2 * t4;
+      auto step = [&](int kk, float(&dacc)[4]) {
+        uint32_t a[4];
+        if (WR) {
+          const int c = ((kk & 3) << 1) | (mi >> 1);
+          ldmatrix_x4(a, arow + (size_t)(kk >> 2) * panel + ((c ^ (ar & 7)) << 4));
+        } else {
+          a[0] = __ldg(reinterpret_cast<const uint32_t*>(r0 + kk * 16));
+          a[1] = __ldg(reinterpret_cast<const uint32_t*>(r1 + kk * 16));
+          a[2] = __ldg(reinterpret_cast<const uint32_t*>(r0 + kk * 16 + 8));
+          a[3] = __ldg(reinterpret_cast<const uint32_t*>(r1 + kk * 16 + 8));
         }
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xrow + kk * 16);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xrow + kk * 16 + 8);
+        mma_16816_bf16(dacc, a, b0, b1);
+      };
+      int kk = kb;
+      for (; kk + 1 < ke; kk += 2) {
+        step(kk, acc[0]);
+        step(kk + 1, acc[1]);
       }
+      if (kk < ke) step(kk, acc[0]);
+      float* pt = part + ((size_t)ks * n_mt * 16 + m0) * 8;
+      pt[g * 8 + 2 * t4] = acc[0][0] + acc[1][0];
+      pt[g * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1];
+      pt[(g + 8) * 8 + 2 * t4] = acc[0][2] + acc[1][2];
+      pt[(g + 8) * 8 + 2 * t4 + 1] = acc[0][3] + acc[1][3];
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = e0 + j;
-#pragma unroll
-      for (int tt = 0; tt < TPB; ++tt) {
-        const float z = warp_sum(acc[j][tt]);
-        if (lane == 0 && e < E) zs[tt * E + e] = z + (p.bias ? __ldg(p.bias + e) : 0.f);
-      }
+  }
+  __syncthreads();
+  if (ok) {
+    for (int i = tid; i < ntok * E; i += kRouteThreads) {
+      const int tt = i / E, e = i - tt * E;
+      float z = part[e * 8 + tt];
+      for (int ks = 1; ks < ksplit; ++ks) z += part[((size_t)ks * n_mt * 16 + e) * 8 + tt];
+      zs[tt * E + e] = z + (p.bias ? __ldg(p.bias + e) : 0.f);
     }
   }
   __syncthreads();
@@ -241,7 +325,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   // experts ordered before it by (z desc, index asc); the experts of rank < k
   // are the selection, in rank order.  Each selected expert's row is claimed
   // with its counter; shared experts take the token's own row.
-  if (warp < ntok && wr_ok) {
+  if (warp < ntok && ok) {
     const int tt = warp, t = t0 + tt;
     const float* z = zs + tt * E;
     float m = -FLT_MAX;
@@ -253,6 +337,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     for (int e = lane; e < E; e += 32) {
       const float ze = z[e];
       int rank = 0;
+#pragma unroll 8
       for (int f = 0; f < E; ++f) {
         const float zf = z[f];
         rank += (zf > ze || (zf == ze && f < e)) ? 1 : 0;
@@ -284,7 +369,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   __syncthreads();
 
   // copy each token's normalised row into its k + S expert rows
-  if (wr_ok) {
+  if (ok) {
     const int cpr = d / 8;  // 16-byte chunks per row
     const int nslots = ntok * (k + S);
     for (int i = tid; i < nslots * cpr; i += kRouteThreads) {
@@ -293,7 +378,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
       const int row = rows[q];
       if (row >= 0)
         reinterpret_cast<uint4*>(p.xperm + (size_t)row * d)[c] =
-            reinterpret_cast<const uint4*>(xb + tt * d)[c];
+            reinterpret_cast<const uint4*>(xb + tt * pitch)[c];
     }
   }
 }
@@ -315,13 +400,10 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
   float ss = 0.f;
   for (int c = tid; c < nc; c += 256) {
     float4 v = reinterpret_cast<const float4*>(hrow)[c];
-    float4 acc = yr[c];
-#pragma unroll 8
-    for (int s = 1; s < p.kS; ++s) {
-      const float4 u = yr[(size_t)s * nc + c];
-      acc.x += u.x; acc.y += u.y; acc.z += u.z; acc.w += u.w;
-    }
-    v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
+    float4 acc[1];
+    const int cj[1] = {c};
+    sum_slots<1>(yr, nc, p.kS, cj, acc);
+    v.x += acc[0].x; v.y += acc[0].y; v.z += acc[0].z; v.w += acc[0].w;
     reinterpret_cast<float4*>(hrow)[c] = v;
     if (p.probe_hidden) reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d)[c] = v;
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
@@ -371,40 +453,46 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStrea
 }
 
 template <int SRC, int TPB>
-cudaError_t launch_route_t(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
-  auto k = route_kernel<SRC, TPB>;
+cudaError_t launch_route_t(const CUtensorMap& map_wr, const RouteParams& p, int grid, size_t smem,
+                           cudaStream_t s, bool pdl) {
+  auto k = p.wr_smem ? route_kernel<SRC, TPB, true> : route_kernel<SRC, TPB, false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, p);
+  return launch_ex(k, dim3(grid), dim3(kRouteThreads), smem, s, pdl, map_wr, p);
 }
 
 template <int SRC>
-cudaError_t launch_route_src(const RouteParams& p, int grid, size_t smem, cudaStream_t s,
-                             bool pdl) {
+cudaError_t launch_route_src(const CUtensorMap& map_wr, const RouteParams& p, int grid,
+                             size_t smem, cudaStream_t s, bool pdl) {
   switch (p.tpb) {
-    case 1: return launch_route_t<SRC, 1>(p, grid, smem, s, pdl);
-    case 2: return launch_route_t<SRC, 2>(p, grid, smem, s, pdl);
-    case 4: return launch_route_t<SRC, 4>(p, grid, smem, s, pdl);
-    default: return launch_route_t<SRC, 8>(p, grid, smem, s, pdl);
+    case 1: return launch_route_t<SRC, 1>(map_wr, p, grid, smem, s, pdl);
+    case 2: return launch_route_t<SRC, 2>(map_wr, p, grid, smem, s, pdl);
+    case 4: return launch_route_t<SRC, 4>(map_wr, p, grid, smem, s, pdl);
+    default: return launch_route_t<SRC, 8>(map_wr, p, grid, smem, s, pdl);
   }
 }
 
 }  // namespace
 
 size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem) {
-  return (wr_smem ? (size_t)E * d * 2 : 0) + (size_t)tpb * d * (4 + 2) +
-         ((size_t)tpb * E + 64) * sizeof(float) + (size_t)tpb * (k + S) * sizeof(int);
+  const size_t pitch = (size_t)d + 8;
+  const size_t part = (size_t)route_ksplit(E) * ((E + 15) / 16) * 16 * 8;
+  return 1024 /* alignment slack */ + (wr_smem ? (size_t)(d / 64) * route_wr_panel(E) : 0) +
+         (size_t)d * 4 + (size_t)tpb * d * 4 +
+         (size_t)tpb * pitch * 2 + (part + (size_t)tpb * E + 64) * sizeof(float) +
+         (size_t)tpb * (k + S) * sizeof(int);
 }
 
 bool route_wr_fits(int tpb, int d, int E, int k, int S) {
   return route_smem_bytes(tpb, d, E, k, S, true) <= 220 * 1024;
 }
 
-cudaError_t launch_route(const RouteParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
+cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int grid, size_t smem,
+                         cudaStream_t s, bool pdl) {
   switch (p.src) {
-    case kSrcEmbed: return launch_route_src<kSrcEmbed>(p, grid, smem, s, pdl);
-    case kSrcBf16: return launch_route_src<kSrcBf16>(p, grid, smem, s, pdl);
-    default: return launch_route_src<kSrcCombine>(p, grid, smem, s, pdl);
+    case kSrcEmbed: return launch_route_src<kSrcEmbed>(map_wr, p, grid, smem, s, pdl);
+    case kSrcBf16: return launch_route_src<kSrcBf16>(map_wr, p, grid, smem, s, pdl);
+    default: return launch_route_src<kSrcCombine>(map_wr, p, grid, smem, s, pdl);
   }
 }
 
