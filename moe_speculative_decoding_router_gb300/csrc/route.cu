@@ -65,7 +65,8 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, size_t byt
 }
 
 // acc[j] = y[0][c_j] + y[1][c_j] + ... + y[kS-1][c_j] (fp32, slot order) for
-// NC float4 chunks of one token's expert outputs y [kS, nc].  Slots go in
+// NC float4 chunks of one token's expert outputs y [kS, nc] (chunks c_j >= nc
+// are skipped).  Slots go in
 // fixed groups of 8 whose loads are all issued before the first add, so a
 // token costs one memory round trip per 8 slots.
 template <int NC>
@@ -77,8 +78,8 @@ __device__ __forceinline__ void sum_slots(const float4* __restrict__ yr, int nc,
     for (int q = 0; q < 8; ++q)
 #pragma unroll
       for (int j = 0; j < NC; ++j)
-        u[q][j] = (s0 + q < kS) ? __ldcg(yr + (size_t)(s0 + q) * nc + c[j])
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        u[q][j] = (s0 + q < kS && c[j] < nc) ? __ldcg(yr + (size_t)(s0 + q) * nc + c[j])
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q)
 #pragma unroll
@@ -121,7 +122,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
         float4 acc[kPass];
         int cj[kPass];
 #pragma unroll
-        for (int j = 0; j < kPass; ++j) cj[j] = min(c0 + j * kRouteThreads, nc - 1);
+        for (int j = 0; j < kPass; ++j) cj[j] = c0 + j * kRouteThreads;
         sum_slots<kPass>(yr, nc, kS, cj, acc);
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
@@ -197,6 +198,70 @@ __host__ __device__ inline int route_ksplit(int E) {
 // Shared-memory bytes of the staged router weights: d/64 panels of E rows x
 // 128 bytes (64 bf16), 128-byte swizzled, each panel 1024-byte aligned.
 __host__ __device__ inline size_t route_wr_panel(int E) { return (size_t)((E + 7) / 8) * 1024; }
+
+// Softmax over the E router logits z of token t and its top-k selection, one
+// warp; lane l holds experts l, l + 32, ... (PER of them, E <= 32 * PER).
+// Writes the token's k + S expert rows into rows[] and the row metadata.
+template <int PER>
+__device__ __forceinline__ void select_experts(const RouteParams& p, const float* z, int t,
+                                               int* rows) {
+  const int lane = threadIdx.x & 31, E = p.E, k = p.k, S = p.S;
+  float ze[PER];
+  int rank[PER];
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    ze[j] = e < E ? z[e] : -FLT_MAX;
+    m = fmaxf(m, ze[j]);
+    rank[j] = 0;
+  }
+  m = warp_max(m);
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (lane + 32 * j < E) sum += __expf(ze[j] - m);
+  sum = warp_sum(sum);
+#pragma unroll 4
+  for (int f = 0; f < E; ++f) {
+    const float zf = z[f];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane + 32 * j;
+      rank[j] += (zf > ze[j] || (zf == ze[j] && f < e)) ? 1 : 0;
+    }
+  }
+  int slot[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    slot[j] = (lane + 32 * j < E && rank[j] < k) ? atomicAdd(p.cnt + lane + 32 * j, 1) : 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E && rank[j] < k) {
+      const float w = __expf(ze[j] - m) / sum;
+      int sl = slot[j];
+      if (sl >= p.T) {  // only reachable if the counters were not cleared
+        atomicOr(p.status, kErrInternal);
+        sl = p.T - 1;
+      }
+      const int row = e * p.T + sl;
+      rows[rank[j]] = row;
+      p.perm_token[row] = t;
+      p.perm_slot[row] = rank[j];
+      p.perm_w[row] = w;
+      if (p.probe_idx) p.probe_idx[(size_t)t * k + rank[j]] = e;
+      if (p.probe_w) p.probe_w[(size_t)t * k + rank[j]] = w;
+    }
+  }
+  for (int s = lane; s < S; s += 32) {
+    const int row = (E + s) * p.T + t;
+    rows[k + s] = row;
+    p.perm_token[row] = t;
+    p.perm_slot[row] = k + s;
+    p.perm_w[row] = 1.0f;
+  }
+}
 
 // WR: the router weights are staged in shared memory by TMA (else read
 // through L1).
@@ -282,8 +347,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       const uint8_t* arow = wr_s + (size_t)ar * 128;
       const __nv_bfloat16* r0 = p.Wr + (size_t)min(m0 + g, E - 1) * d + 2 * t4;
       const __nv_bfloat16* r1 = p.Wr + (size_t)min(m0 + g + 8, E - 1) * d + 2 * t4;
-      auto step = [&](int kk, float(&dacc)[4]) {
-        uint32_t a[4];
+      // fragments of step kk (A: experts x 16 K, B: 16 K x tokens)
+      auto load = [&](int kk, uint32_t(&a)[4], uint32_t(&b)[2]) {
         if (WR) {
           const int c = ((kk & 3) << 1) | (mi >> 1);
           ldmatrix_x4(a, arow + (size_t)(kk >> 2) * panel + ((c ^ (ar & 7)) << 4));
@@ -293,16 +358,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
           a[2] = __ldg(reinterpret_cast<const uint32_t*>(r0 + kk * 16 + 8));
           a[3] = __ldg(reinterpret_cast<const uint32_t*>(r1 + kk * 16 + 8));
         }
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xrow + kk * 16);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xrow + kk * 16 + 8);
-        mma_16816_bf16(dacc, a, b0, b1);
+        b[0] = *reinterpret_cast<const uint32_t*>(xrow + kk * 16);
+        b[1] = *reinterpret_cast<const uint32_t*>(xrow + kk * 16 + 8);
       };
-      int kk = kb;
-      for (; kk + 1 < ke; kk += 2) {
-        step(kk, acc[0]);
-        step(kk + 1, acc[1]);
+      // software pipeline: the fragments of the next step load while the
+      // current step's MMA issues (the asm statements keep program order)
+      uint32_t fa[2][4], fb[2][2];
+      if (kb < ke) load(kb, fa[0], fb[0]);
+      for (int kk = kb; kk < ke; kk += 2) {
+        if (kk + 1 < ke) load(kk + 1, fa[1], fb[1]);
+        mma_16816_bf16(acc[0], fa[0], fb[0][0], fb[0][1]);
+        if (kk + 2 < ke) load(kk + 2, fa[0], fb[0]);
+        if (kk + 1 < ke) mma_16816_bf16(acc[1], fa[1], fb[1][0], fb[1][1]);
       }
-      if (kk < ke) step(kk, acc[0]);
       float* pt = part + ((size_t)ks * n_mt * 16 + m0) * 8;
       pt[g * 8 + 2 * t4] = acc[0][0] + acc[1][0];
       pt[g * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1];
@@ -324,47 +392,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // softmax and top-k, one warp per token.  Rank of expert e = number of
   // experts ordered before it by (z desc, index asc); the experts of rank < k
   // are the selection, in rank order.  Each selected expert's row is claimed
-  // with its counter; shared experts take the token's own row.
+  // with its counter (all claims of a lane issued together); shared experts
+  // take the token's own row.
   if (warp < ntok && ok) {
-    const int tt = warp, t = t0 + tt;
-    const float* z = zs + tt * E;
-    float m = -FLT_MAX;
-    for (int e = lane; e < E; e += 32) m = fmaxf(m, z[e]);
-    m = warp_max(m);
-    float sum = 0.f;
-    for (int e = lane; e < E; e += 32) sum += __expf(z[e] - m);
-    sum = warp_sum(sum);
-    for (int e = lane; e < E; e += 32) {
-      const float ze = z[e];
-      int rank = 0;
-#pragma unroll 8
-      for (int f = 0; f < E; ++f) {
-        const float zf = z[f];
-        rank += (zf > ze || (zf == ze && f < e)) ? 1 : 0;
-      }
-      if (rank < k) {
-        const float w = __expf(ze - m) / sum;
-        int slot = atomicAdd(p.cnt + e, 1);
-        if (slot >= p.T) {  // only reachable if the counters were not cleared
-          atomicOr(p.status, kErrInternal);
-          slot = p.T - 1;
-        }
-        const int row = e * p.T + slot;
-        rows[tt * (k + S) + rank] = row;
-        p.perm_token[row] = t;
-        p.perm_slot[row] = rank;
-        p.perm_w[row] = w;
-        if (p.probe_idx) p.probe_idx[(size_t)t * k + rank] = e;
-        if (p.probe_w) p.probe_w[(size_t)t * k + rank] = w;
-      }
-    }
-    for (int s = lane; s < S; s += 32) {
-      const int row = (E + s) * p.T + t;
-      rows[tt * (k + S) + k + s] = row;
-      p.perm_token[row] = t;
-      p.perm_slot[row] = k + s;
-      p.perm_w[row] = 1.0f;
-    }
+    if (E <= 64)
+      select_experts<2>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
+    else
+      select_experts<8>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
   }
   __syncthreads();
 
