@@ -134,7 +134,7 @@ Sizes sizes(const moe_verify_config* c, const Derived& r) {
   s.xf = (uint64_t)round_up(r.T_max, 16) * d * 2;
   s.bad = (uint64_t)r.T_max * 4;
   s.perm = (uint64_t)r.rows_max * 4;
-  s.cnt = (uint64_t)c->n_experts * 4;
+  s.cnt = (uint64_t)c->n_experts * 4 * 2;  // two parities
   s.dep = (uint64_t)r.chunks_cap * 4;
   s.keys = (uint64_t)r.T_max * 8;
   s.io = (uint64_t)r.T_max * 4;
@@ -273,9 +273,14 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
   return MOE_VERIFY_OK;
 }
 
-int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int32_t* context_ids,
-              const int32_t* draft_ids, int B, int K, const void* h_in,
-              const moe_verify_probe* probe, int probe_layer, cudaStream_t s, bool pdl) {
+// Expert counters alternate between two buffers by position in the launch
+// sequence (parity): routing kernel n claims rows on buffer n % 2 and clears
+// buffer (n + 1) % 2, whose users are complete by then; the final kernel
+// clears the buffer of the last layer.
+int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh,
+              const int32_t* context_ids, const int32_t* draft_ids, int B, int K,
+              const void* h_in, const moe_verify_probe* probe, int probe_layer, cudaStream_t s,
+              bool pdl) {
   const int T = sh.T;
   mv::RouteParams rp = {};
   rp.T = T;
@@ -307,7 +312,11 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
     if (probe->topk_w) rp.probe_w = probe->topk_w + (size_t)probe_layer * T * c->k;
     if (probe->hidden) rp.probe_hidden = probe->hidden + (size_t)probe_layer * T * c->d;
   }
-  rp.cnt = c->cnt;
+  rp.cnt = c->cnt + (size_t)parity * c->E;
+  rp.cnt_other = c->cnt + (size_t)(1 - parity) * c->E;
+  rp.dep_clear = c->dep;
+  rp.n_dep_clear = c->chunks_cap;
+  rp.next_item_clear = reinterpret_cast<int32_t*>(c->done_ffn + 1);
   rp.xperm = c->xperm;
   rp.perm_token = c->perm_token;
   rp.perm_slot = c->perm_slot;
@@ -317,8 +326,7 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
     CK(mv::launch_route(c->map_wr, rp, sh.grid_route, sh.route_smem, s, pdl));
   }
   mv::FfnParams fp = {};
-  fp.cnt = c->cnt;
-  fp.cnt_clear = c->cnt;
+  fp.cnt = c->cnt + (size_t)parity * c->E;
   fp.dep = c->dep;
   fp.E = c->E;
   fp.S = c->S;
@@ -341,7 +349,6 @@ int run_layer(moe_verify_ctx* c, int l, int src, const StepShape& sh, const int3
   fp.d = c->d;
   fp.kS = c->kS;
   fp.status = c->status;
-  fp.done = c->done_ffn;
   fp.next_item = reinterpret_cast<int32_t*>(c->done_ffn + 1);
   {
     Timed tm(c, 0, s);
@@ -537,7 +544,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
   const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
-    int rc = run_layer(ctx, l, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
+    int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
                        draft_ids, B, K, nullptr, probe, l, s, pdl);
     if (rc != MOE_VERIFY_OK) return rc;
   }
@@ -553,6 +560,8 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   fp.out = ctx->xf;
   fp.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
   fp.keys = ctx->keys;
+  fp.cnt_clear = ctx->cnt + (size_t)((ctx->L - 1) & 1) * ctx->E;
+  fp.n_cnt_clear = ctx->E;
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, pdl));
@@ -617,7 +626,7 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   StepShape sh;
   if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
-  int rc = run_layer(ctx, layer, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
+  int rc = run_layer(ctx, layer, 0, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
                      true);
   if (rc != MOE_VERIFY_OK) return rc;
   mv::FinalParams fp = {};
@@ -632,6 +641,8 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   fp.out = static_cast<__nv_bfloat16*>(h_out);
   fp.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)T * ctx->d : nullptr;
   fp.keys = ctx->keys;
+  fp.cnt_clear = ctx->cnt;
+  fp.n_cnt_clear = ctx->E;
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, true));

@@ -239,7 +239,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int* list_base = reinterpret_cast<int*>(ctrl_base + kCtrlBytes);
   float* xbuf = reinterpret_cast<float*>(ctrl_base + kCtrlBytes + kListBytes);
   __shared__ int s_totals[3];  // gate/up items, down items, chunks
-  __shared__ int is_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, nE = p.E + p.S;
@@ -538,19 +537,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
-  // the last CTA clears the counters for the next layer
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (is_last) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) p.cnt_clear[e] = 0;
-    for (int c = threadIdx.x; c < s_totals[2]; c += blockDim.x) p.dep[c] = 0;
-    if (threadIdx.x == 0) {
-      *p.next_item = 0;
-      *p.done = 0u;
-    }
-  }
+  // the counters this launch used are cleared by the next routing kernel
 }
 
 // ------------------------------------------------------------- lm_head

@@ -40,6 +40,13 @@ struct RouteParams {
   float* probe_hidden;         // [T, d] or nullptr
   // expert-major rows: expert e owns rows [e*T, e*T + cnt[e])
   int32_t* cnt;                // [E] rows claimed per routed expert (zero on entry)
+  // cleared after the wait (the kernels that used them are complete): the
+  // other parity's expert counters and the previous expert-FFN launch's
+  // dependency counters and item counter
+  int32_t* cnt_other;          // [E]
+  int32_t* dep_clear;          // [n_dep_clear]
+  int n_dep_clear;
+  int32_t* next_item_clear;
   __nv_bfloat16* xperm;        // [(E+S)*T, d] normalised inputs
   int32_t* perm_token;         // [(E+S)*T] token of each row
   int32_t* perm_slot;          // [(E+S)*T] its slot: routed rank, or k + s
@@ -50,8 +57,7 @@ struct RouteParams {
 // every (expert, 128-row tile, chunk of <= nch rows), then the down items.
 struct FfnParams {
   const int32_t* cnt;          // [E] routed rows per expert (shared experts: T)
-  int32_t* cnt_clear;          // the same counters, cleared by the last CTA
-  int32_t* dep;                // [chunks] finished gate/up halves per chunk
+  int32_t* dep;                // [chunks] finished gate/up halves per chunk (zero on entry)
   int E, S, T, nch;
   int mt_gu, mt_dn;            // 128-row tiles per expert
   int kb_gu, kb_dn;            // 64-wide K blocks: d/64 and I_pad/64
@@ -65,7 +71,6 @@ struct FfnParams {
   float* y;                    // [T, kS, d]
   int d, kS;
   uint32_t* status;
-  unsigned int* done;          // CTAs finished (the last one clears the counters)
   int* next_item;              // items claimed past the first gridDim (zero on entry)
 };
 
@@ -79,6 +84,8 @@ struct FinalParams {
   __nv_bfloat16* out;          // mode 0: xf [T, d]; mode 1: h_out [T, d]
   float* probe_hidden;         // [T, d] or nullptr
   unsigned long long* keys;    // [T] argmax keys, cleared in mode 0
+  int32_t* cnt_clear;          // [n_cnt_clear] expert counters of the last layer, cleared
+  int n_cnt_clear;
 };
 
 // The lm_head GEMM with its argmax epilogue.

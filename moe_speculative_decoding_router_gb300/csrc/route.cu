@@ -201,7 +201,8 @@ __host__ __device__ inline size_t route_wr_panel(int E) { return (size_t)((E + 7
 
 // Softmax over the E router logits z of token t and its top-k selection, one
 // warp; lane l holds experts l, l + 32, ... (PER of them, E <= 32 * PER).
-// Writes the token's k + S expert rows into rows[] and the row metadata.
+// Writes the token's k routed expert rows into rows[] and the row metadata
+// of all k + S.
 template <int PER>
 __device__ __forceinline__ void select_experts(const RouteParams& p, const float* z, int t,
                                                int* rows) {
@@ -254,9 +255,9 @@ __device__ __forceinline__ void select_experts(const RouteParams& p, const float
       if (p.probe_w) p.probe_w[(size_t)t * k + rank[j]] = w;
     }
   }
+  // shared experts: their rows were copied right after the RMSNorm
   for (int s = lane; s < S; s += 32) {
     const int row = (E + s) * p.T + t;
-    rows[k + s] = row;
     p.perm_token[row] = t;
     p.perm_slot[row] = k + s;
     p.perm_w[row] = 1.0f;
@@ -321,9 +322,28 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // launches later may then read what the kernel before this one wrote.
   pdl_wait();
   pdl_launch_dependents();
+  if (blockIdx.x == 0) {
+    // counters of kernels that are complete now (the expert FFN before this
+    // kernel, the routing kernel before that); the expert FFN after this
+    // kernel reads them only after its own wait
+    for (int i = tid; i < p.n_dep_clear; i += kRouteThreads) p.dep_clear[i] = 0;
+    for (int e = tid; e < E; e += kRouteThreads) p.cnt_other[e] = 0;
+    if (tid == 0) *p.next_item_clear = 0;
+  }
   bool ok = mbar_wait(&hx_bar, 0, &abort_flag, p.status);
   if (ok) block_norm<SRC, TPB>(p, t0, ntok, xs, gs, xb, pitch, red);
   __syncthreads();
+  const int cpr = d / 8;  // 16-byte chunks per row
+  if (ok) {
+    // shared experts hold token t in row (E+s)*T + t: copy those rows now,
+    // while the router runs
+    for (int i = tid; i < ntok * S * cpr; i += kRouteThreads) {
+      const int q = i / cpr, c = i - q * cpr;
+      const int tt = q / S, sx = q - tt * S;
+      reinterpret_cast<uint4*>(p.xperm + ((size_t)(E + sx) * p.T + t0 + tt) * d)[c] =
+          reinterpret_cast<const uint4*>(xb + tt * pitch)[c];
+    }
+  }
   if (WR && ok) ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
 
   // Router logits on the tensor cores: z^T = W_r xhat^T as 16x8x16 tiles,
@@ -402,9 +422,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncthreads();
 
-  // copy each token's normalised row into its k + S expert rows
+  // copy each token's normalised row into its k routed expert rows
   if (ok) {
-    const int cpr = d / 8;  // 16-byte chunks per row
     const int nslots = ntok * (k + S);
     for (int i = tid; i < nslots * cpr; i += kRouteThreads) {
       const int q = i / cpr, c = i - q * cpr;
@@ -425,6 +444,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
   pdl_wait();
   pdl_launch_dependents();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < p.n_cnt_clear; e += 256) p.cnt_clear[e] = 0;
   __shared__ float red[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;
