@@ -66,7 +66,8 @@ struct Ctrl {
   uint64_t* drain;
   uint64_t* xfull;
   uint64_t* xempty;
-  uint64_t* spec;
+  uint64_t* spec;      // speculative weight tiles of the first item
+  uint64_t* spec_b;    // speculative activation tiles of the first item
   uint64_t* q_full;   // [kQueue] item queue: producer -> MMA issuer and epilogue
   uint64_t* q_empty;  // [kQueue]
   int* q_item;        // [kQueue]
@@ -84,7 +85,8 @@ __device__ __forceinline__ Ctrl ctrl_at(uint8_t* base, int stages) {
   c.xfull = c.drain + 1;
   c.xempty = c.xfull + 2;
   c.spec = c.xempty + 2;
-  c.q_full = c.spec + 1;
+  c.spec_b = c.spec + 1;
+  c.q_full = c.spec_b + 1;
   c.q_empty = c.q_full + kQueue;
   c.q_item = reinterpret_cast<int*>(c.q_empty + kQueue);
   c.tmem_slot = reinterpret_cast<uint32_t*>(c.q_item + kQueue);
@@ -106,6 +108,7 @@ __device__ __forceinline__ void init_ctrl(const Ctrl& c, int stages, uint32_t xf
   }
   mbar_init(c.drain, 1);
   mbar_init(c.spec, 1);
+  mbar_init(c.spec_b, 1);
   for (int q = 0; q < kQueue; ++q) {
     mbar_init(&c.q_full[q], 1);
     mbar_init(&c.q_empty[q], 5);  // the MMA issuer and the four epilogue warps
@@ -275,6 +278,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // and rows are read; dependents may start once this grid is past its wait.
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0 && pre > 0) {
+    // the speculated first item's activation rows (chunk 0 of expert
+    // blockIdx / mt_gu) load while the item lists are built
+    const uint64_t pol_x = policy_evict_last();
+    const int row0 = (int)(blockIdx.x / p.mt_gu) * p.T;
+    mbar_arrive_expect_tx(C.spec_b, (uint32_t)(pre * p.nch * 128));
+    for (int s = 0; s < pre; ++s)
+      tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &map_x, C.spec_b, s * 64, row0, pol_x);
+  }
   if (warp == 0) {
     // per-expert rows, chunk and item prefix sums: one warp, 32 experts per
     // round, shuffle scans with a running carry
@@ -355,19 +367,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         return c < n_items ? c : -1;
       };
       bool ok = true;
-      if (pre > 0) ok = mbar_wait(C.spec, 0, C.abort_flag, p.status);  // speculative tiles landed
+      // the speculative tiles have landed (kept on a hit, overwritten otherwise)
+      if (pre > 0) ok = mbar_wait(C.spec, 0, C.abort_flag, p.status) &&
+                        mbar_wait(C.spec_b, 0, C.abort_flag, p.status);
       ok = ok && start_item(i);
-      const bool hit = ok && pre > 0 && i >= 0 && !it.down && it.a_row == guess_row;
+      const bool hit = ok && pre > 0 && i >= 0 && !it.down && it.a_row == guess_row &&
+                       it.row0 == (int)(blockIdx.x / p.mt_gu) * p.T;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       if (hit) {
-        // the weight tiles are already in place: add the activation tiles
-        for (int s = 0; s < pre; ++s) {
-          uint8_t* sb = stages + (size_t)s * stage_bytes + kStageA;
-          mbar_arrive_expect_tx(&C.full[s], (uint32_t)(p.nch * 128));
-          tma_load_2d(sb, &map_x, &C.full[s], s * 64, it.row0, pol_x);
-        }
+        // weight and activation tiles are in place: release the stages
+        for (int s = 0; s < pre; ++s) mbar_arrive(&C.full[s]);
         issued = pre;
         stage = pre;
         kb = pre;

@@ -24,7 +24,7 @@ namespace mv {
 
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -192,7 +192,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
 // Router-logit partition over the warps: 16-expert tiles x K splits.
 __host__ __device__ inline int route_ksplit(int E) {
   const int n_mt = (E + 15) / 16;
-  return n_mt >= 8 ? 1 : 8 / n_mt;
+  return n_mt >= kRouteWarps ? 1 : kRouteWarps / n_mt;
 }
 
 // Shared-memory bytes of the staged router weights: d/64 panels of E rows x
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   float* part = reinterpret_cast<float*>(xb + TPB * pitch);
   float* zs = part + ksplit * n_mt * 16 * 8;
   float* red = zs + TPB * E;
-  int* rows = reinterpret_cast<int*>(red + 64);
+  int* rows = reinterpret_cast<int*>(red + kRouteWarps * 8);
   __shared__ __align__(8) uint64_t hx_bar, wr_bar;
   __shared__ int abort_flag;
 
@@ -534,7 +534,7 @@ size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem) {
   const size_t part = (size_t)route_ksplit(E) * ((E + 15) / 16) * 16 * 8;
   return 1024 /* alignment slack */ + (wr_smem ? (size_t)(d / 64) * route_wr_panel(E) : 0) +
          (size_t)d * 4 + (size_t)tpb * d * 4 +
-         (size_t)tpb * pitch * 2 + (part + (size_t)tpb * E + 64) * sizeof(float) +
+         (size_t)tpb * pitch * 2 + (part + (size_t)tpb * E + kRouteWarps * 8) * sizeof(float) +
          (size_t)tpb * (k + S) * sizeof(int);
 }
 

@@ -97,6 +97,45 @@ def test_tiny_logits_probe(tiny):
         assert rel_err(lg[t], r["logits"]) <= REL
 
 
+@pytest.fixture(scope="module")
+def tiny3():
+    """The tiny stack with an odd layer count (expert counters alternate
+    between two buffers by layer parity)."""
+    import dataclasses
+    B = _B()
+    cfg = dataclasses.replace(S.TINY, n_layers=3)
+    w = S.make_weights(cfg)
+    ctx = B.MoeVerify(cfg, B.weights_to_device(w), max_batch=64, max_k=3)
+    yield ctx, O.Oracle(cfg, w), cfg
+    ctx.close()
+
+
+def test_tiny_odd_layers_steps_and_layer_calls_interleaved(tiny3):
+    """Steps and single-block calls in any order leave every counter clean:
+    each call matches the oracle on its own."""
+    ctx, orc, cfg = tiny3
+    B = _B()
+    for rnd in range(3):
+        for Bn, K in [(32, 3), (5, 1), (64, 3)]:
+            ids = S.uniform_ids(Bn * (K + 1), 900 + 7 * rnd + Bn, K, cfg.vocab).reshape(Bn, K + 1)
+            tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]))
+            check_tokens(orc, ids.reshape(-1), tg.cpu().numpy().reshape(-1))
+        T = 9 + rnd
+        hin = S.hidden_input(T, cfg.hidden, seed=S.SEED_HIDDEN + 50 + rnd)
+        hin_t = torch.from_numpy(hin.view(np.int16)).cuda().view(torch.bfloat16)
+        probe, pt = B.make_probe(1, T, cfg)
+        hout = ctx.layer(rnd % cfg.n_layers, hin_t, probe=probe)
+        got = hout.view(torch.int16).cpu().numpy().view(np.uint16)
+        gsel = pt["topk_idx"].cpu().numpy()[0]
+        for t in range(T):
+            _, _, sel, _, gap = orc.layer_bf16(rnd % cfg.n_layers, hin[t])
+            if set(sel.tolist()) != set(gsel[t].tolist()):
+                assert gap < TIE, (rnd, t, gap)
+            _, f64, _, _, _ = orc.layer_bf16(rnd % cfg.n_layers, hin[t], force_sel=gsel[t])
+            assert rel_err(S.bf16_bits_to_f32(got[t]), f64) <= REL, (rnd, t)
+    assert ctx.sync_status() == B.OK
+
+
 # ---------------------------------------------------------- single MoE block
 
 @pytest.mark.parametrize("T", [4, 1, 37, 128, 300, 1024, 4096])
