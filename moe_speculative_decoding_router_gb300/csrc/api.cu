@@ -277,10 +277,12 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
 // sequence (parity): routing kernel n claims rows on buffer n % 2 and clears
 // buffer (n + 1) % 2, whose users are complete by then; the final kernel
 // clears the buffer of the last layer.
+// next_head: the lm_head follows this layer (its first items are prefetched
+// into L2 at the end of the expert FFN, as the next layer's are otherwise).
 int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh,
               const int32_t* context_ids, const int32_t* draft_ids, int B, int K,
               const void* h_in, const moe_verify_probe* probe, int probe_layer, cudaStream_t s,
-              bool pdl) {
+              bool pdl, bool next_head) {
   const int T = sh.T;
   mv::RouteParams rp = {};
   rp.T = T;
@@ -350,9 +352,24 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   fp.kS = c->kS;
   fp.status = c->status;
   fp.next_item = reinterpret_cast<int32_t*>(c->done_ffn + 1);
+  // the guessed first items are right when every routed expert holds one
+  // chunk: expect at least 6 rows per expert
+  fp.spec = ((int64_t)T * c->k >= 6LL * c->E) ? 1 : 0;
+  const CUtensorMap* map_pf = &c->map_gu;
+  fp.pf_kb = c->d / 64;
+  if (next_head) {
+    map_pf = &c->map_lm;
+    fp.pf_base = 0;
+    fp.pf_div = sh.n_chunks_lm;
+    fp.pf_limit = (c->V_pad / 128) * sh.n_chunks_lm;
+  } else if (fp.spec && l + 1 < c->L && src != mv::kSrcBf16) {
+    fp.pf_base = (l + 1) * c->nE * c->mt_gu * 128;
+    fp.pf_div = 1;
+    fp.pf_limit = c->nE * c->mt_gu;
+  }
   {
     Timed tm(c, 0, s);
-    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, fp, c->num_sms, s, pdl));
+    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, fp, c->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -545,7 +562,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
     int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
-                       draft_ids, B, K, nullptr, probe, l, s, pdl);
+                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1);
     if (rc != MOE_VERIFY_OK) return rc;
   }
   mv::FinalParams fp = {};
@@ -627,7 +644,7 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   StepShape sh;
   if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
   int rc = run_layer(ctx, layer, 0, mv::kSrcBf16, sh, nullptr, nullptr, T, 0, h_in, probe, 0, s,
-                     true);
+                     true, false);
   if (rc != MOE_VERIFY_OK) return rc;
   mv::FinalParams fp = {};
   fp.T = T;

@@ -232,7 +232,7 @@ __device__ __forceinline__ FItem decode(const FfnParams& p, const Lists& L, int 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
                const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
-               const FfnParams p) {
+               const __grid_constant__ CUtensorMap map_pf, const FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stage_bytes = kStageA + p.nch * 128;
@@ -253,9 +253,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // Speculation: when every expert holds one chunk, the first item of CTA c
   // is gate/up tile c of this layer.  Its weight tiles do not depend on the
-  // routing, so they start streaming before waiting for it.
+  // routing, so they start streaming before waiting for it.  The host turns
+  // this on only when every routed expert expects several rows (else most
+  // guesses would miss and their loads would only take bandwidth).
   const int guess_row = p.a_base_gu + blockIdx.x * 128;
-  const bool guess_valid = (int)blockIdx.x < nE * p.mt_gu;
+  const bool guess_valid = p.spec && (int)blockIdx.x < nE * p.mt_gu;
   const int pre = guess_valid ? min(p.stages, p.kb_gu) : 0;
   if (threadIdx.x == 0) {
     init_ctrl(C, p.stages, 2, 2);
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&map_x);
     tma_prefetch_desc(&map_dn);
     tma_prefetch_desc(&map_a);
+    if (p.pf_limit > 0) tma_prefetch_desc(&map_pf);
     if (pre > 0) {
       const uint64_t pol_w = policy_evict_first();
       mbar_arrive_expect_tx(C.spec, (uint32_t)(pre * kStageA));
@@ -431,6 +434,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           i = next_item();
           if (!start_item(i)) ok = false;
         }
+      }
+      if (ok && (int)blockIdx.x < p.pf_limit) {
+        // every load of this CTA is issued: pull the next kernel's first
+        // weight item for this CTA index into L2 while HBM has room (the
+        // last items of other CTAs and the routing in between)
+        const int row = p.pf_base + (int)(blockIdx.x / p.pf_div) * 128;
+        for (int k = 0; k < p.pf_kb; ++k) tma_prefetch_l2_2d(&map_pf, k * 64, row);
       }
       if (!ok) producer_drain(C, issued, p.stages);
     }
@@ -803,10 +813,11 @@ int gemm_max_stages(int nch) {
 }
 
 cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
-                       const CUtensorMap& map_dn, const CUtensorMap& map_a, const FfnParams& p,
-                       int grid, cudaStream_t s, bool pdl) {
+                       const CUtensorMap& map_dn, const CUtensorMap& map_a,
+                       const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
+                       bool pdl) {
   return launch_gemm_ex(ffn_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu, map_x,
-                        map_dn, map_a, p);
+                        map_dn, map_a, map_pf, p);
 }
 
 cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,

@@ -72,6 +72,11 @@ struct FfnParams {
   int d, kS;
   uint32_t* status;
   int* next_item;              // items claimed past the first gridDim (zero on entry)
+  // L2 prefetch of the next kernel's first weight item of this CTA index c,
+  // issued once this CTA has no items left: rows pf_base + (c / pf_div) * 128
+  // of the prefetch tensor map, pf_kb 64-column boxes, for c < pf_limit
+  int pf_base, pf_div, pf_limit, pf_kb;
+  int spec;                    // 1: load the guessed first item's tiles before the wait
 };
 
 struct FinalParams {
@@ -123,8 +128,9 @@ bool route_wr_fits(int tpb, int d, int E, int k, int S);
 cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int grid, size_t smem,
                          cudaStream_t s, bool pdl);
 cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
-                       const CUtensorMap& map_dn, const CUtensorMap& map_a, const FfnParams& p,
-                       int grid, cudaStream_t s, bool pdl);
+                       const CUtensorMap& map_dn, const CUtensorMap& map_a,
+                       const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
+                       bool pdl);
 cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
                           int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
