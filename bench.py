@@ -73,41 +73,36 @@ class Trajectory:
         self.steps = np.zeros(B, dtype=np.int64)
 
     def drafts(self):
-        d = np.empty((self.B, self.K), dtype=np.int32)
-        for b in range(self.B):
-            truth, x = [], int(self.last[b])
-            for _ in range(self.K):
-                x = int(self.g[x])
-                truth.append(x)
-            d[b] = self.src.drafts(int(self.page_id[b]), int(self.steps[b]), truth)
+        truth = np.empty((self.B, self.K), dtype=np.int64)
+        x = self.last.copy()
+        for i in range(self.K):
+            x = self.g[x]
+            truth[:, i] = x
+        d = self.src.drafts_batch(self.page_id, self.steps, truth)
         return self.last.astype(np.int32).copy(), d
 
     def advance(self, committed: np.ndarray, alen: np.ndarray) -> int:
         """Apply one step's outcome; returns the committed tokens it counts."""
-        counted = 0
-        for b in range(self.B):
-            n = int(alen[b])
-            take = min(n + 1, self.page - int(self.done[b]))
-            counted += take
-            self.done[b] += take
-            self.steps[b] += 1
-            self.last[b] = int(committed[b, n])
-            if self.done[b] >= self.page:
-                self.page_id[b] = self.rank * 1_000_000 + self.next_page
-                self.next_page += 1
-                self.last[b] = int(S.start_ids(1, self.V, first=int(self.page_id[b]))[0])
-                self.done[b] = 0
-                self.steps[b] = 0
-        return counted
+        n = np.asarray(alen, dtype=np.int64)
+        take = np.minimum(n + 1, self.page - self.done)
+        self.done += take
+        self.steps += 1
+        self.last = np.asarray(committed, dtype=np.int64)[np.arange(self.B), n]
+        for b in np.nonzero(self.done >= self.page)[0]:
+            self.page_id[b] = self.rank * 1_000_000 + self.next_page
+            self.next_page += 1
+            self.last[b] = int(S.start_ids(1, self.V, first=int(self.page_id[b]))[0])
+            self.done[b] = 0
+            self.steps[b] = 0
+        return int(take.sum())
 
     def expected(self, ctx_ids: np.ndarray, drafts: np.ndarray):
         toks = np.concatenate([ctx_ids.reshape(-1, 1), drafts], axis=1).astype(np.int64)
         y = self.g[toks].astype(np.int32)
         match = drafts == y[:, :-1]
         n = np.where(match.all(axis=1), self.K, np.argmin(match, axis=1))
-        committed = np.full_like(y, -1)
-        for b in range(self.B):
-            committed[b, : n[b] + 1] = y[b, : n[b] + 1]
+        keep = np.arange(self.K + 1)[None, :] <= n[:, None]
+        committed = np.where(keep, y, -1).astype(np.int32)
         return committed, n.astype(np.int32)
 
 

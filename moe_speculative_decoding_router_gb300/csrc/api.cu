@@ -42,6 +42,13 @@ struct moe_verify_ctx {
           *io_alen = nullptr;
   CUtensorMap map_gu, map_dn, map_lm, map_wr;
   std::vector<void*> allocs;
+  // host-buffer decode: one captured graph (step + accept) per (B, K)
+  struct DecodeGraph {
+    int B, K;
+    cudaGraphExec_t exec;
+  };
+  std::vector<DecodeGraph> decode_graphs;
+  cudaStream_t capture_stream = nullptr;
   // profiling
   bool timing = false;
   std::vector<TimingPair> pending;
@@ -667,6 +674,50 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   return MOE_VERIFY_OK;
 }
 
+namespace {
+
+// The device part of a host-buffer decode call: step + accept on the
+// context's own io buffers.
+int enqueue_decode(moe_verify_ctx* ctx, int B, int K, cudaStream_t s) {
+  int rc = enqueue_step(ctx, ctx->io_ctx, ctx->io_drafts, B, K, ctx->io_targets, nullptr, s);
+  if (rc != MOE_VERIFY_OK) return rc;
+  return moe_verify_accept(ctx, ctx->io_drafts, ctx->io_targets, B, K, ctx->io_committed,
+                           ctx->io_alen, s);
+}
+
+// The captured graph of enqueue_decode for (B, K), built on first use
+// (captured on a library-owned stream, launched on the caller's).  Returns
+// nullptr when it cannot be built (the caller then enqueues directly).
+cudaGraphExec_t decode_graph(moe_verify_ctx* ctx, int B, int K) {
+  constexpr size_t kMaxGraphs = 16;
+  for (const auto& g : ctx->decode_graphs)
+    if (g.B == B && g.K == K) return g.exec;
+  if (ctx->decode_graphs.size() >= kMaxGraphs) return nullptr;
+  if (!ctx->capture_stream &&
+      cudaStreamCreateWithFlags(&ctx->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    ctx->capture_stream = nullptr;
+    return nullptr;
+  }
+  cudaStream_t cs = ctx->capture_stream;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return nullptr;
+  const int rc = enqueue_decode(ctx, B, K, cs);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (rc == MOE_VERIFY_OK && ec == cudaSuccess && graph &&
+      cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    exec = nullptr;
+  if (graph) cudaGraphDestroy(graph);
+  if (!exec) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  ctx->decode_graphs.push_back({B, K, exec});
+  return exec;
+}
+
+}  // namespace
+
 int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
                            const int32_t* host_draft_ids, int32_t B, int32_t K,
                            int32_t* host_committed, int32_t* host_accept_len, void* cuda_stream) {
@@ -678,11 +729,13 @@ int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
   if (K > 0)
     CK(cudaMemcpyAsync(ctx->io_drafts, host_draft_ids, (size_t)B * K * 4, cudaMemcpyHostToDevice,
                        s));
-  int rc = enqueue_step(ctx, ctx->io_ctx, ctx->io_drafts, B, K, ctx->io_targets, nullptr, s);
-  if (rc != MOE_VERIFY_OK) return rc;
-  rc = moe_verify_accept(ctx, ctx->io_drafts, ctx->io_targets, B, K, ctx->io_committed,
-                         ctx->io_alen, s);
-  if (rc != MOE_VERIFY_OK) return rc;
+  cudaGraphExec_t exec = ctx->timing ? nullptr : decode_graph(ctx, B, K);
+  if (exec) {
+    CK(cudaGraphLaunch(exec, s));
+  } else {
+    int rc = enqueue_decode(ctx, B, K, s);
+    if (rc != MOE_VERIFY_OK) return rc;
+  }
   CK(cudaMemcpyAsync(host_committed, ctx->io_committed, (size_t)B * (K + 1) * 4,
                      cudaMemcpyDeviceToHost, s));
   CK(cudaMemcpyAsync(host_accept_len, ctx->io_alen, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
@@ -706,6 +759,9 @@ int moe_verify_sync_status(moe_verify_ctx* ctx) {
 void moe_verify_destroy(moe_verify_ctx* ctx) {
   if (!ctx) return;
   cudaDeviceSynchronize();
+  for (auto& g : ctx->decode_graphs) cudaGraphExecDestroy(g.exec);
+  ctx->decode_graphs.clear();
+  if (ctx->capture_stream) cudaStreamDestroy(ctx->capture_stream);
   free_all(ctx);
   delete ctx;
 }

@@ -86,6 +86,10 @@ def lib():
         L.synth_ids.argtypes = [ctypes.c_void_p, i64, u64, u64, u64, i64, i32]
         L.synth_uniform.restype = None
         L.synth_uniform.argtypes = [ctypes.c_void_p, i64, u64, u64, u64, i32]
+        L.synth_uniform_at.restype = None
+        L.synth_uniform_at.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, u64, u64]
+        L.synth_ids_at.restype = None
+        L.synth_ids_at.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, u64, u64, i64]
         _lib = L
     return _lib
 
@@ -218,6 +222,21 @@ class DraftSource:
 
     def _index(self, seq: int, step: int, i: int) -> int:
         return ((seq * 1_000_003 + step) * 16 + i)
+
+    def drafts_batch(self, seqs, steps, truth) -> np.ndarray:
+        """drafts() for many sequences at once: seqs [B], steps [B],
+        truth [B, K] -> [B, K] int32 (the same draws, counter-indexed)."""
+        seqs = np.asarray(seqs, dtype=np.uint64).reshape(-1, 1)
+        steps = np.asarray(steps, dtype=np.uint64).reshape(-1, 1)
+        truth = np.asarray(truth).reshape(len(seqs), self.K)
+        j = np.ascontiguousarray((seqs * np.uint64(1_000_003) + steps) * np.uint64(16) +
+                                 np.arange(self.K, dtype=np.uint64).reshape(1, -1))
+        u = np.empty(j.shape, dtype=np.float64)
+        ids = np.empty(j.shape, dtype=np.int32)
+        L = lib()
+        L.synth_uniform_at(u.ctypes.data, j.ctypes.data, j.size, self.seed, TID_DRAFT_COIN)
+        L.synth_ids_at(ids.ctypes.data, j.ctypes.data, j.size, self.seed, TID_DRAFT_ID, self.V)
+        return np.where(u < self.p, truth, ids).astype(np.int32)
 
     def drafts(self, seq: int, step: int, truth) -> np.ndarray:
         """truth[i] = the greedy token the i-th draft should predict."""

@@ -156,3 +156,17 @@ SYNTH_API void synth_uniform(double* out, int64_t n, uint64_t seed, uint64_t tid
   job_t b = {2, out, 0, 0, stream_key(seed, tid), first, 0.0, 0};
   run_parallel(b, n, nthreads);
 }
+
+/* out[i] = uniform [0,1) from draw(seed, tid, idx[i]) (arbitrary indices). */
+SYNTH_API void synth_uniform_at(double* out, const uint64_t* idx, int64_t n, uint64_t seed,
+                                uint64_t tid) {
+  const uint64_t key = stream_key(seed, tid);
+  for (int64_t i = 0; i < n; ++i) out[i] = (double)(draw_at(key, idx[i]) >> 11) * kInv53;
+}
+
+/* out[i] = draw(seed, tid, idx[i]) % modulus (arbitrary indices). */
+SYNTH_API void synth_ids_at(int32_t* out, const uint64_t* idx, int64_t n, uint64_t seed,
+                            uint64_t tid, int64_t modulus) {
+  const uint64_t key = stream_key(seed, tid);
+  for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)(draw_at(key, idx[i]) % (uint64_t)modulus);
+}

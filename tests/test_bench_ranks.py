@@ -74,6 +74,36 @@ def test_trajectory_counts_and_pages():
     assert tr.next_page == B + 2 * B
 
 
+def test_draft_batch_equals_per_sequence():
+    """The batched draft draws are the per-sequence draws (same counters)."""
+    src = S.DraftSource(0.6, V, K)
+    rng = np.random.default_rng(5)
+    seqs = rng.integers(0, 3_000_000, 50)
+    steps = rng.integers(0, 500, 50)
+    truth = rng.integers(0, V, (50, K))
+    a = src.drafts_batch(seqs, steps, truth)
+    b = np.stack([src.drafts(int(seqs[i]), int(steps[i]), truth[i]) for i in range(50)])
+    assert np.array_equal(a, b)
+    assert 0 < np.mean(a == truth) < 1
+
+
+def test_expected_commits_follow_the_prefix_rule():
+    g = _table()
+    tr = bench.Trajectory(g, 0, B=B, K=K, p=0.5, page_tokens=PAGE)
+    for _ in range(6):
+        ctx_ids, drafts = tr.drafts()
+        com, n = tr.expected(ctx_ids, drafts)
+        y = g[np.concatenate([ctx_ids[:, None], drafts], axis=1)]
+        for b in range(B):
+            m = 0
+            while m < K and drafts[b, m] == y[b, m]:
+                m += 1
+            assert n[b] == m
+            assert list(com[b, : m + 1]) == list(y[b, : m + 1])
+            assert all(com[b, m + 1:] == -1)
+        tr.advance(com, n)
+
+
 def test_two_rank_replicas(tmp_path):
     world = 2
     mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,

@@ -210,16 +210,22 @@ def test_full_batch_invariance(full):
 
 
 def test_full_decode_host_matches_device(full):
+    """The host-buffer entry point (a graph per (B, K) after its first call)
+    returns what step + accept return, over repeated and alternating shapes."""
     ctx, _ = full
-    ids = S.uniform_ids(32 * 4, 91, 1, S.FULL.vocab).reshape(32, 4)
-    ctxi, dr = _i32(ids[:, 0]), _i32(ids[:, 1:])
-    tg = ctx.step(ctxi, dr)
-    com, alen = ctx.accept(dr, tg)
-    hc = np.zeros((32, 4), np.int32)
-    ha = np.zeros(32, np.int32)
-    ctx.decode_host(np.ascontiguousarray(ids[:, 0]), np.ascontiguousarray(ids[:, 1:]), hc, ha)
-    assert np.array_equal(hc, com.cpu().numpy())
-    assert np.array_equal(ha, alen.cpu().numpy())
+    for rep in range(3):
+        for Bn, K in [(32, 3), (5, 1), (32, 3), (1, 0), (17, 2)]:
+            ids = S.uniform_ids(Bn * (K + 1), 91 + rep, 1 + Bn + K, S.FULL.vocab).reshape(Bn, K + 1)
+            ctxi = _i32(ids[:, 0])
+            dr = _i32(ids[:, 1:]) if K else None
+            tg = ctx.step(ctxi, dr)
+            com, alen = ctx.accept(dr, tg)
+            hc = np.zeros((Bn, K + 1), np.int32)
+            ha = np.zeros(Bn, np.int32)
+            ctx.decode_host(np.ascontiguousarray(ids[:, 0]),
+                            np.ascontiguousarray(ids[:, 1:]) if K else None, hc, ha)
+            assert np.array_equal(hc, com.cpu().numpy()), (rep, Bn, K)
+            assert np.array_equal(ha, alen.cpu().numpy()), (rep, Bn, K)
 
 
 def test_full_graph_capture(full):
