@@ -163,8 +163,13 @@ MOE_VERIFY_API int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const vo
  * context_ids [B] and draft_ids [B, K] from host memory (pinned memory makes
  * the copies asynchronous), runs moe_verify_step and moe_verify_accept on
  * cuda_stream, copies committed [B, K+1] and accept_len [B] back to host
- * memory, and waits for the stream.  target_ids (device, [B, K+1]) may be
- * NULL; the context's own buffer is used then.  Not capturable. */
+ * memory, and waits for the stream (the targets stay in a context-owned
+ * device buffer).  1 <= B <= max_batch, 0 <= K <= max_k.  Not capturable.
+ * The first call for a given (B, K) captures the device part (step + accept
+ * on the context's own buffers) into a CUDA graph on a library-owned stream;
+ * later calls with that shape launch the graph on cuda_stream (up to 16
+ * shapes are kept; others, and calls while per-launch timing is on, enqueue
+ * the kernels directly).  Calls on one context must not run concurrently. */
 MOE_VERIFY_API int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
                            const int32_t* host_draft_ids, int32_t B, int32_t K,
                            int32_t* host_committed, int32_t* host_accept_len,
