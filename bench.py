@@ -197,10 +197,14 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
 
     cfg = S.FULL if not args.layers else __import__("dataclasses").replace(S.FULL, n_layers=args.layers)
+    # the workload's batch shape; profiling runs may time another one
+    Bq = args.batch if (args.profile and args.batch) else B_SEQ
+    Kq = args.drafts if (args.profile and args.drafts is not None) else K_DRAFT
     t_setup = time.perf_counter()
     w_host = S.make_weights(cfg)
     w_dev = BND.weights_to_device(w_host, device=dev)
-    ctx = BND.MoeVerify(cfg, w_dev, max_batch=1024, max_k=K_DRAFT)
+    ctx = BND.MoeVerify(cfg, w_dev, max_batch=Bq if args.profile else 1024,
+                        max_k=Kq if args.profile else K_DRAFT)
     del w_dev
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
@@ -211,25 +215,25 @@ def run_ours(args, rank, world, local):
     g = np.empty(V, dtype=np.int32)
     if args.profile:
         g[:] = S.uniform_ids(V, 99, 0, V)
-    chunk = 1024 * (K_DRAFT + 1)
+    chunk = 1024 * (Kq + 1)
     all_ids = torch.arange(V, dtype=torch.int32, device=dev)
     for s0 in (range(0, V, chunk) if not args.profile else ()):
         n = min(chunk, V - s0)
-        Bn = (n + K_DRAFT) // (K_DRAFT + 1)
-        ids = torch.zeros(Bn * (K_DRAFT + 1), dtype=torch.int32, device=dev)
+        Bn = (n + Kq) // (Kq + 1)
+        ids = torch.zeros(Bn * (Kq + 1), dtype=torch.int32, device=dev)
         ids[:n] = all_ids[s0:s0 + n]
-        ids = ids.view(Bn, K_DRAFT + 1)
+        ids = ids.view(Bn, Kq + 1)
         tg = ctx.step(ids[:, 0].contiguous(), ids[:, 1:].contiguous())
         g[s0:s0 + n] = tg.view(-1)[:n].cpu().numpy()
     assert ctx.sync_status() == BND.OK
 
     # the decode trajectory, planned on the host
     total = args.warmup + args.steps
-    traj = Trajectory(g, rank)
-    plan_ctx = np.empty((total, B_SEQ), np.int32)
-    plan_dr = np.empty((total, B_SEQ, K_DRAFT), np.int32)
-    plan_com = np.empty((total, B_SEQ, K_DRAFT + 1), np.int32)
-    plan_alen = np.empty((total, B_SEQ), np.int32)
+    traj = Trajectory(g, rank, B=Bq, K=Kq)
+    plan_ctx = np.empty((total, Bq), np.int32)
+    plan_dr = np.empty((total, Bq, Kq), np.int32)
+    plan_com = np.empty((total, Bq, Kq + 1), np.int32)
+    plan_alen = np.empty((total, Bq), np.int32)
     counted = np.zeros(total, np.int64)
     for i in range(total):
         c, d = traj.drafts()
@@ -240,16 +244,16 @@ def run_ours(args, rank, world, local):
 
     d_ctx = torch.from_numpy(plan_ctx).to(dev)
     d_dr = torch.from_numpy(plan_dr).to(dev)
-    d_tg = torch.empty((total, B_SEQ, K_DRAFT + 1), dtype=torch.int32, device=dev)
+    d_tg = torch.empty((total, Bq, Kq + 1), dtype=torch.int32, device=dev)
     d_com = torch.empty_like(d_tg)
-    d_alen = torch.empty((total, B_SEQ), dtype=torch.int32, device=dev)
+    d_alen = torch.empty((total, Bq), dtype=torch.int32, device=dev)
 
     # one CUDA graph per step: step + accept on fixed buffers, inputs copied in
-    in_ctx = torch.empty((B_SEQ,), dtype=torch.int32, device=dev)
-    in_dr = torch.empty((B_SEQ, K_DRAFT), dtype=torch.int32, device=dev)
-    out_tg = torch.empty((B_SEQ, K_DRAFT + 1), dtype=torch.int32, device=dev)
+    in_ctx = torch.empty((Bq,), dtype=torch.int32, device=dev)
+    in_dr = torch.empty((Bq, Kq), dtype=torch.int32, device=dev)
+    out_tg = torch.empty((Bq, Kq + 1), dtype=torch.int32, device=dev)
     out_com = torch.empty_like(out_tg)
-    out_alen = torch.empty((B_SEQ,), dtype=torch.int32, device=dev)
+    out_alen = torch.empty((Bq,), dtype=torch.int32, device=dev)
     in_ctx.copy_(d_ctx[0])
     in_dr.copy_(d_dr[0])
     cs = torch.cuda.Stream(device=dev)
@@ -305,8 +309,9 @@ def run_ours(args, rank, world, local):
 
     if args.profile:
         if rank == 0:
-            print(json.dumps({"profile": True, "layers": cfg.n_layers, "steps": args.steps,
-                              "ms_per_step": round(ms / args.steps, 4), "clocks": clk}), flush=True)
+            print(json.dumps({"profile": True, "layers": cfg.n_layers, "batch": Bq, "drafts": Kq,
+                              "steps": args.steps, "ms_per_step": round(ms / args.steps, 4),
+                              "clocks": clk}), flush=True)
         ctx.close()
         return
 
@@ -319,11 +324,11 @@ def run_ours(args, rank, world, local):
     tokens = float(counted[args.warmup:].sum())
 
     # end to end: the same steps through the host-buffer entry point
-    h_ctx = torch.empty((B_SEQ,), dtype=torch.int32, pin_memory=True).numpy()
-    h_dr = torch.empty((B_SEQ, K_DRAFT), dtype=torch.int32, pin_memory=True).numpy()
-    h_com = torch.empty((B_SEQ, K_DRAFT + 1), dtype=torch.int32, pin_memory=True).numpy()
-    h_alen = torch.empty((B_SEQ,), dtype=torch.int32, pin_memory=True).numpy()
-    etraj = Trajectory(g, rank)
+    h_ctx = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
+    h_dr = torch.empty((Bq, Kq), dtype=torch.int32, pin_memory=True).numpy()
+    h_com = torch.empty((Bq, Kq + 1), dtype=torch.int32, pin_memory=True).numpy()
+    h_alen = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
+    etraj = Trajectory(g, rank, B=Bq, K=Kq)
     pre = [etraj.drafts()]
     for i in range(args.warmup):
         c, d = pre[-1]
@@ -351,7 +356,7 @@ def run_ours(args, rank, world, local):
     ctx.set_timing(True)
     ctx.get_timing(reset=True)
     alg_bytes = 0.0
-    probe, pt = BND.make_probe(cfg.n_layers, B_SEQ * (K_DRAFT + 1), cfg, topk=True, hidden=False,
+    probe, pt = BND.make_probe(cfg.n_layers, Bq * (Kq + 1), cfg, topk=True, hidden=False,
                                device=dev)
     for i in range(args.warmup, total):
         ctx.step(d_ctx[i], d_dr[i], target_ids=d_tg[i], probe=probe)
@@ -380,14 +385,14 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform start ids, drafts right w.p. 0.75)",
         "config": {"workload": WORKLOAD, "layers": cfg.n_layers, "hidden": cfg.hidden,
                    "experts": f"{cfg.n_experts}x{cfg.expert_inter} top-{cfg.top_k} + "
-                              f"{cfg.n_shared} shared", "vocab": cfg.vocab, "batch": B_SEQ,
-                   "drafts": K_DRAFT, "p_match": P_MATCH, "page_tokens": PAGE_TOKENS,
+                              f"{cfg.n_shared} shared", "vocab": cfg.vocab, "batch": Bq,
+                   "drafts": Kq, "p_match": P_MATCH, "page_tokens": PAGE_TOKENS,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (5.8 GB of weights per step)",
                    "cuda_graph": graph is not None},
         "e2e": {"value": round(e_tokens / e_s, 1), "unit": UNIT,
-                "h2d_bytes_per_step": B_SEQ * 4 + B_SEQ * K_DRAFT * 4,
-                "d2h_bytes_per_step": B_SEQ * (K_DRAFT + 1) * 4 + B_SEQ * 4},
+                "h2d_bytes_per_step": Bq * 4 + Bq * Kq * 4,
+                "d2h_bytes_per_step": Bq * (Kq + 1) * 4 + Bq * 4},
         "gpu_launches": int(args.steps * (2 * cfg.n_layers + 3)),
         "roofline": {"kernel": "expert FFN (gate/up + SwiGLU + down + combine)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
@@ -515,11 +520,19 @@ def main():
                     help="timing loop only (random greedy table; no e2e, roofline or CPU legs)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: a shorter stack (same per-layer shapes)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling only: sequences per step (default 32)")
+    ap.add_argument("--drafts", type=int, default=None,
+                    help="profiling only: drafts per sequence, 0..15 (default 3)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.layers and not args.profile:
-        ap.error("--layers is for profiling runs only (--profile)")
+    if (args.layers or args.batch or args.drafts is not None) and not args.profile:
+        ap.error("--layers, --batch and --drafts are for profiling runs only (--profile)")
+    if args.drafts is not None and not 0 <= args.drafts <= 15:
+        ap.error("--drafts must be in 0..15")
+    if (args.batch or B_SEQ) * ((K_DRAFT if args.drafts is None else args.drafts) + 1) > 4096:
+        ap.error("--batch x (--drafts + 1) must be at most 4096 verify tokens")
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)

@@ -360,8 +360,13 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   fp.status = c->status;
   fp.next_item = reinterpret_cast<int32_t*>(c->done_ffn + 1);
   // the guessed first items are right when every routed expert holds one
-  // chunk: expect at least 6 rows per expert
-  fp.spec = ((int64_t)T * c->k >= 6LL * c->E) ? 1 : 0;
+  // chunk.  Loading them early costs little when a guess misses (the loads
+  // overlap the routing), so it is on from one expected row per expert; the
+  // L2 pull of the next layer's guesses competes with this layer's streaming
+  // and is on only from six
+  const int64_t rows_x_E = (int64_t)T * c->k;
+  fp.spec = (rows_x_E >= c->E) ? 1 : 0;
+  const bool pull_next = rows_x_E >= 6LL * c->E;
   const CUtensorMap* map_pf = &c->map_gu;
   fp.pf_kb = c->d / 64;
   if (next_head) {
@@ -369,7 +374,7 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.pf_base = 0;
     fp.pf_div = sh.n_chunks_lm;
     fp.pf_limit = (c->V_pad / 128) * sh.n_chunks_lm;
-  } else if (fp.spec && l + 1 < c->L && src != mv::kSrcBf16) {
+  } else if (pull_next && l + 1 < c->L && src != mv::kSrcBf16) {
     fp.pf_base = (l + 1) * c->nE * c->mt_gu * 128;
     fp.pf_div = 1;
     fp.pf_limit = c->nE * c->mt_gu;
