@@ -11,6 +11,8 @@
 // about one item of each other.  A down item waits (bounded) until both
 // SwiGLU halves of every gate/up tile of its chunk of rows are written; the
 // items it waits for were claimed earlier and have no waits of their own.
+// Once a CTA has issued its last load it pulls into L2 the weight item its
+// index starts with in the next kernel (next layer, or the lm_head).
 // lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
 // epilogue the running greedy argmax over the vocabulary.  The chunk's
 // normalised rows arrive as one TMA box per stage (the tensor map's box is

@@ -15,6 +15,11 @@
 // independent of its row (each row is a separate column of the expert's GEMM,
 // reduced in a fixed order), so the outputs do not.  Shared expert s holds
 // token t in row (E+s)*T + t.
+//
+// One block per token (up to eight at large T).  Static data and the
+// residual rows are staged before the block waits for the previous kernel;
+// the router logits run on the tensor cores (mma.sync m16n8k16, the block's
+// tokens as the N columns).
 #include <float.h>
 
 #include "internal.h"
@@ -37,16 +42,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 v = __bfloat1622float2(b[i]);
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
 }
 
 __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
