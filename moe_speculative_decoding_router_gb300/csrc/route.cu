@@ -344,47 +344,59 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // Router logits on the tensor cores: z^T = W_r xhat^T as 16x8x16 tiles,
   // rows = experts, columns = the block's tokens (columns >= ntok are not
   // used), fp32 accumulation.  Warp unit u covers expert tile u % n_mt and
-  // the u / n_mt-th of the K range, alternating two accumulators; the
-  // partial sums are added in K-split order.
+  // the u / n_mt-th share of the 64-column panels; a panel is four MMA steps
+  // on two alternating accumulators, and the next panel's fragments load
+  // while the current panel's MMAs issue.  The partial sums are added in
+  // K-split order.
   if (ok) {
-    const int ksteps = d / 16;
-    const int kper = (ksteps + ksplit - 1) / ksplit;
+    const int npan = d / 64;
+    const int pper = (npan + ksplit - 1) / ksplit;
     const int g = lane >> 2, t4 = lane & 3;
     const __nv_bfloat16* xrow = xb + (size_t)min(g, TPB - 1) * pitch + 2 * t4;
     for (int u = warp; u < n_mt * ksplit; u += kRouteWarps) {
       const int m0 = (u % n_mt) * 16, ks = u / n_mt;
-      const int kb = ks * kper, ke = min(ksteps, kb + kper);
+      const int pb = ks * pper, pe = min(npan, pb + pper);
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      // this lane's ldmatrix row (WR: row r, 16-byte chunk c of a panel sits
-      // at r * 128 + ((c ^ (r % 8)) * 16)) or fragment rows (direct loads)
+      // WR: this lane's ldmatrix row ar and the byte offsets of its four
+      // 16-byte chunks in a panel (chunk c of row r sits at r * 128 +
+      // ((c ^ (r % 8)) * 16)); otherwise the rows of its direct loads
       const int mi = lane >> 3;
       const int ar = min(m0 + (lane & 7) + (mi & 1) * 8, E - 1);
-      const uint8_t* arow = wr_s + (size_t)ar * 128;
+      uint32_t off[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        off[j] = (uint32_t)ar * 128u + ((uint32_t)(((j << 1) | (mi >> 1)) ^ (ar & 7)) << 4);
       const __nv_bfloat16* r0 = p.Wr + (size_t)min(m0 + g, E - 1) * d + 2 * t4;
       const __nv_bfloat16* r1 = p.Wr + (size_t)min(m0 + g + 8, E - 1) * d + 2 * t4;
-      // fragments of step kk (A: experts x 16 K, B: 16 K x tokens)
-      auto load = [&](int kk, uint32_t(&a)[4], uint32_t(&b)[2]) {
-        if (WR) {
-          const int c = ((kk & 3) << 1) | (mi >> 1);
-          ldmatrix_x4(a, arow + (size_t)(kk >> 2) * panel + ((c ^ (ar & 7)) << 4));
-        } else {
-          a[0] = __ldg(reinterpret_cast<const uint32_t*>(r0 + kk * 16));
-          a[1] = __ldg(reinterpret_cast<const uint32_t*>(r1 + kk * 16));
-          a[2] = __ldg(reinterpret_cast<const uint32_t*>(r0 + kk * 16 + 8));
-          a[3] = __ldg(reinterpret_cast<const uint32_t*>(r1 + kk * 16 + 8));
+      auto load_panel = [&](int pn, uint32_t(&a)[4][4], uint32_t(&b)[4][2]) {
+        const uint8_t* pbase = wr_s + (size_t)pn * panel;
+        const __nv_bfloat16* xp = xrow + pn * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (WR) {
+            ldmatrix_x4(a[j], pbase + off[j]);
+          } else {
+            const int k0 = pn * 64 + j * 16;
+            a[j][0] = __ldg(reinterpret_cast<const uint32_t*>(r0 + k0));
+            a[j][1] = __ldg(reinterpret_cast<const uint32_t*>(r1 + k0));
+            a[j][2] = __ldg(reinterpret_cast<const uint32_t*>(r0 + k0 + 8));
+            a[j][3] = __ldg(reinterpret_cast<const uint32_t*>(r1 + k0 + 8));
+          }
+          b[j][0] = *reinterpret_cast<const uint32_t*>(xp + j * 16);
+          b[j][1] = *reinterpret_cast<const uint32_t*>(xp + j * 16 + 8);
         }
-        b[0] = *reinterpret_cast<const uint32_t*>(xrow + kk * 16);
-        b[1] = *reinterpret_cast<const uint32_t*>(xrow + kk * 16 + 8);
       };
-      // software pipeline: the fragments of the next step load while the
-      // current step's MMA issues (the asm statements keep program order)
-      uint32_t fa[2][4], fb[2][2];
-      if (kb < ke) load(kb, fa[0], fb[0]);
-      for (int kk = kb; kk < ke; kk += 2) {
-        if (kk + 1 < ke) load(kk + 1, fa[1], fb[1]);
-        mma_16816_bf16(acc[0], fa[0], fb[0][0], fb[0][1]);
-        if (kk + 2 < ke) load(kk + 2, fa[0], fb[0]);
-        if (kk + 1 < ke) mma_16816_bf16(acc[1], fa[1], fb[1][0], fb[1][1]);
+      auto mma_panel = [&](const uint32_t(&a)[4][4], const uint32_t(&b)[4][2]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_16816_bf16(acc[j & 1], a[j], b[j][0], b[j][1]);
+      };
+      uint32_t fa[2][4][4], fb[2][4][2];
+      if (pb < pe) load_panel(pb, fa[0], fb[0]);
+      for (int pn = pb; pn < pe; pn += 2) {
+        if (pn + 1 < pe) load_panel(pn + 1, fa[1], fb[1]);
+        mma_panel(fa[0], fb[0]);
+        if (pn + 2 < pe) load_panel(pn + 2, fa[0], fb[0]);
+        if (pn + 1 < pe) mma_panel(fa[1], fb[1]);
       }
       float* pt = part + ((size_t)ks * n_mt * 16 + m0) * 8;
       pt[g * 8 + 2 * t4] = acc[0][0] + acc[1][0];
