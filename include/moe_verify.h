@@ -175,6 +175,19 @@ MOE_VERIFY_API int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* ho
                            int32_t* host_committed, int32_t* host_accept_len,
                            void* cuda_stream);
 
+/* Diagnostic (no counterpart in the method): checks the bounded waits that
+ * every step kernel uses, without a context.  One thread waits on an
+ * mbarrier phase that nothing completes, then on a device flag that nothing
+ * sets, each for limit_ns nanoseconds (1e3 <= limit_ns <= 1e9), using the same
+ * bounded-wait code as the kernels; nothing faults or traps, the kernel
+ * returns when both waits have given up.  On return, elapsed_ns (host, may be
+ * NULL) holds the device time of the two waits.  Returns MOE_VERIFY_OK when
+ * both waits gave up and raised the timeout bit, MOE_VERIFY_ERR_TIMEOUT
+ * never, MOE_VERIFY_ERR_CUDA when a wait did not report (or on a CUDA error),
+ * MOE_VERIFY_ERR_ARG for a limit out of range.  Synchronises cuda_stream. */
+MOE_VERIFY_API int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns,
+                                                 void* cuda_stream);
+
 /* Waits for the device, then returns and clears the sticky device error:
  * MOE_VERIFY_OK, MOE_VERIFY_ERR_ID_RANGE, MOE_VERIFY_ERR_TIMEOUT or
  * MOE_VERIFY_ERR_CUDA. */

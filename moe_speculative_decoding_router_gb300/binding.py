@@ -29,7 +29,8 @@ ERR_UNSUPPORTED = -6
 EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_verify_layer",
             "moe_verify_decode_host", "moe_verify_sync_status", "moe_verify_destroy",
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
-            "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc")
+            "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc",
+            "moe_verify_check_bounded_wait")
 
 
 class Config(ctypes.Structure):
@@ -93,6 +94,8 @@ def load(build_if_missing: bool = True):
     L.moe_verify_set_timing.argtypes = [_P, _i32]
     L.moe_verify_get_timing.restype = _i32
     L.moe_verify_get_timing.argtypes = [_P, _P, _P, _i32]
+    L.moe_verify_check_bounded_wait.restype = _i32
+    L.moe_verify_check_bounded_wait.argtypes = [ctypes.c_int64, _P, _P]
     L.moe_verify_greedy_head_noalloc.restype = _i32
     L.moe_verify_greedy_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P,
                                                  _P]
@@ -290,6 +293,17 @@ def greedy_head_noalloc(h, final_norm, lm_head, rms_eps: float, target_ids=None,
     return target_ids
 
 
+def check_bounded_wait(limit_ns: int, stream=None):
+    """moe_verify_check_bounded_wait: returns (status, elapsed ns of the two
+    waits that nothing completes)."""
+    el = ctypes.c_int64(0)
+    # an out-of-range limit is refused on the host, before any stream is needed
+    ok_limit = 1000 <= int(limit_ns) <= 1_000_000_000
+    rc = load().moe_verify_check_bounded_wait(int(limit_ns), ctypes.byref(el),
+                                              _stream_handle(stream) if ok_limit else None)
+    return int(rc), int(el.value)
+
+
 def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logits: bool = False,
                device="cuda"):
     """Allocate probe buffers; returns (Probe struct, dict of tensors)."""
@@ -308,4 +322,4 @@ def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logi
 
 
 __all__ = ["load", "MoeVerify", "MoeVerifyError", "Probe", "make_probe", "check_config",
-           "device_bytes", "strerror", "weights_to_device", "EXPORTED"]
+           "device_bytes", "strerror", "weights_to_device", "check_bounded_wait", "EXPORTED"]

@@ -748,6 +748,18 @@ int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
   return MOE_VERIFY_OK;
 }
 
+int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns, void* cuda_stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return MOE_VERIFY_ERR_ARG;
+  unsigned long long out[3] = {0, 0, 0};
+  uint32_t st = 0;
+  if (mv::run_bounded_wait_check((uint64_t)limit_ns, static_cast<cudaStream_t>(cuda_stream), out,
+                                 &st) != cudaSuccess)
+    return MOE_VERIFY_ERR_CUDA;
+  if (elapsed_ns) *elapsed_ns = (int64_t)out[0];
+  return (out[1] == 1 && out[2] == 1 && (st & mv::kErrTimeout)) ? MOE_VERIFY_OK
+                                                                : MOE_VERIFY_ERR_CUDA;
+}
+
 int moe_verify_sync_status(moe_verify_ctx* ctx) {
   if (!ctx) return MOE_VERIFY_ERR_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_VERIFY_ERR_CUDA;

@@ -136,6 +136,10 @@ cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, cons
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
 
+// Self-check of the bounded waits (see moe_verify_check_bounded_wait).
+cudaError_t run_bounded_wait_check(uint64_t limit_ns, cudaStream_t s, unsigned long long* host_out,
+                                   uint32_t* host_status);
+
 // Weight repacking (init only).
 cudaError_t launch_repack_gateup(__nv_bfloat16* dst, const __nv_bfloat16* gate,
                                  const __nv_bfloat16* up, const __nv_bfloat16* s_gate,

@@ -108,7 +108,65 @@ int grid_for(int64_t total) {
   return (int)g;
 }
 
+// Self-check of the bounded waits: one thread waits on an mbarrier phase
+// that nothing completes, then spins (acquire loads, as the expert FFN's
+// dependency wait does) on a flag that nothing sets, each with limit_ns.
+// out[0] = elapsed ns, out[1] = 1 if the mbarrier wait gave up and raised the
+// timeout bit, out[2] = 1 if the flag wait gave up.
+__global__ void bounded_wait_check_kernel(const int32_t* flag, uint32_t* status, uint64_t limit_ns,
+                                          unsigned long long* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  const uint64_t t0 = globaltimer_ns();
+  const bool got = mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+  out[1] = (!got && abort_flag && (*status & kErrTimeout)) ? 1ull : 0ull;
+  abort_flag = 0;
+  const uint64_t t1 = globaltimer_ns();
+  bool gave_up = false;
+  uint32_t n = 0;
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v > 0) break;
+    if ((++n & 63u) == 0 && globaltimer_ns() - t1 > limit_ns) {
+      atomicOr(status, kErrTimeout);
+      gave_up = true;
+      break;
+    }
+  }
+  out[2] = gave_up ? 1ull : 0ull;
+  out[0] = globaltimer_ns() - t0;
+}
+
+__device__ int32_t g_never_set;               // stays 0
+__device__ uint32_t g_check_status;
+__device__ unsigned long long g_check_out[3];
+
 }  // namespace
+
+cudaError_t run_bounded_wait_check(uint64_t limit_ns, cudaStream_t s, unsigned long long* host_out,
+                                   uint32_t* host_status) {
+  int32_t* flag = nullptr;
+  uint32_t* st = nullptr;
+  unsigned long long* out = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&flag), g_never_set);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st), g_check_status);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&out), g_check_out);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(out, 0, sizeof(unsigned long long) * 3, s);
+  if (e != cudaSuccess) return e;
+  bounded_wait_check_kernel<<<1, 32, 0, s>>>(flag, st, limit_ns, out);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaMemcpyAsync(host_out, out, sizeof(unsigned long long) * 3, cudaMemcpyDeviceToHost,
+                           s)) != cudaSuccess)
+    return e;
+  if ((e = cudaMemcpyAsync(host_status, st, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s) {
   const int grid = (p.B + 127) / 128;

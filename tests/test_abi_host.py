@@ -79,3 +79,9 @@ def test_null_arguments_fail_on_the_host():
     assert lib.moe_verify_init(None, None, None, ctypes.byref(h)) == B.ERR_ARG
     assert h.value is None
     lib.moe_verify_destroy(None)
+
+
+def test_bounded_wait_check_rejects_limits_on_the_host():
+    """Out-of-range limits are refused before any device work."""
+    assert B.check_bounded_wait(10)[0] == B.ERR_ARG
+    assert B.check_bounded_wait(2_000_000_000)[0] == B.ERR_ARG

@@ -284,6 +284,22 @@ def test_step_flags_out_of_range_ids(tiny):
     assert alen.cpu().numpy()[1] == -1 and alen.cpu().numpy()[2] == -1
 
 
+def test_bounded_waits_give_up_and_report(tiny):
+    """A wait on an mbarrier phase nothing completes and a spin on a flag
+    nothing sets both give up after their limit and raise the timeout bit;
+    the context keeps working afterwards."""
+    ctx, orc = tiny
+    B = _B()
+    limit = 2_000_000  # 2 ms each
+    rc, elapsed = B.check_bounded_wait(limit)
+    assert rc == B.OK, B.strerror(rc)
+    assert 2 * limit <= elapsed < 2 * limit + 50_000_000, elapsed
+    ids = S.uniform_ids(8, 77, 3, 512).reshape(2, 4)
+    tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]))
+    check_tokens(orc, ids.reshape(-1), tg.cpu().numpy().reshape(-1))
+    assert ctx.sync_status() == B.OK
+
+
 def test_host_argument_errors(tiny):
     ctx, _ = tiny
     B = _B()
