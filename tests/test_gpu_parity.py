@@ -290,6 +290,7 @@ def test_bounded_waits_give_up_and_report(tiny):
     the context keeps working afterwards."""
     ctx, orc = tiny
     B = _B()
+    ctx.sync_status()  # clear what earlier tests on this context left
     limit = 2_000_000  # 2 ms each
     rc, elapsed = B.check_bounded_wait(limit)
     assert rc == B.OK, B.strerror(rc)
