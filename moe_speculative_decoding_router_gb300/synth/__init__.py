@@ -36,6 +36,7 @@ SEED_WEIGHTS = 0
 SEED_START_IDS = 1
 SEED_DRAFTS = 2
 SEED_HIDDEN = 3
+SEED_DRAFT_HEAD = 4
 
 # Stream ids inside a seed.  Weights: embed, then per layer eight tensors,
 # then the final norm and the lm_head.
@@ -156,6 +157,24 @@ LAYER = ModelConfig(1, 1280, 64, 6, 2, 896, 896, 512, name="layer")
 FULL = ModelConfig(12, 1280, 64, 6, 2, 896, 896, 129280, name="full")
 # The full stack with Zipf(s=1.2)-skewed routing.
 FULL_ZIPF = dataclasses.replace(FULL, zipf_s=1.2, name="full_zipf")
+
+
+# FastMTP draft heads: one dense block (a single SwiGLU expert of weight 1 on
+# every token, no routing choice) applied recursively, sharing the verifier's
+# embedding, final norm and lm_head.  The pages give no width: 4 x hidden.
+DRAFT_TINY = ModelConfig(1, 64, 1, 1, 0, 256, 256, 512, sigma=0.05, name="draft_tiny")
+DRAFT = ModelConfig(1, 1280, 1, 1, 0, 5120, 5120, 129280, name="draft")
+
+
+def make_draft_weights(cfg: ModelConfig, target: Dict[str, np.ndarray],
+                       seed: int = SEED_DRAFT_HEAD,
+                       nthreads: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """The draft block's own weights (seeded stream SEED_DRAFT_HEAD) plus the
+    verifier's embedding, final norm and lm_head (the same arrays)."""
+    w = make_weights(cfg, seed=seed, with_embed=False, with_lm_head=False, nthreads=nthreads)
+    for k in ("embed", "final_norm", "lm_head"):
+        w[k] = target[k]
+    return w
 
 
 def router_bias(cfg: ModelConfig) -> Optional[np.ndarray]:

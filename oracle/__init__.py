@@ -81,6 +81,8 @@ def lib():
         L.oracle_head.argtypes = [_P, _P, _P, _P, _P]
         L.oracle_layer_bf16.restype = None
         L.oracle_layer_bf16.argtypes = [_P, _P, _i32, _P, _P, _P, _P, _P, _P, _P]
+        L.oracle_draft.restype = _i32
+        L.oracle_draft.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
         _lib = L
     return _lib
 
@@ -239,6 +241,22 @@ class Oracle:
         gap = np.empty(1)
         y = lib().oracle_head(self._cp, self._wp, _ptr(hh), _ptr(lg), _ptr(gap))
         return int(y), float(gap[0]), lg
+
+    def draft(self, h_prev: np.ndarray, t_prev: int, K: int):
+        """The FastMTP draft head with this instance as the draft block (one
+        layer, one expert): K recursive steps from residual h_prev [d] and
+        token t_prev.  Returns (drafts [K], hidden after each step [K, d],
+        top-2 logit gaps [K])."""
+        d = self.cfg.hidden
+        hp = np.ascontiguousarray(h_prev, dtype=np.float64)
+        drafts = np.empty(K, np.int32)
+        hid = np.empty((K, d))
+        gaps = np.empty(K)
+        rc = lib().oracle_draft(self._cp, self._wp, _ptr(hp), int(t_prev), int(K), _ptr(drafts),
+                                _ptr(hid), _ptr(gaps))
+        if rc != 0:
+            raise ValueError("draft token id outside [0, V)")
+        return drafts, hid, gaps
 
     def layer_bf16(self, l: int, h_in: np.ndarray, force_sel: Optional[np.ndarray] = None):
         """The bf16-in/bf16-out block on one token.  Returns

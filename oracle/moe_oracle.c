@@ -343,3 +343,40 @@ ORACLE_API void oracle_layer_bf16(const oracle_config* c, const oracle_weights* 
   if (h_out_f64) memcpy(h_out_f64, h, sizeof(double) * (size_t)d);
   free(h);
 }
+
+/* FastMTP draft head ("Jina AI Releases jina-ocr-v1, a 3.4B MoE Document
+ * Parser With Built-In Speculative Decoding", FastMTP paragraph: one dense
+ * draft block applied recursively for K steps with the same parameters;
+ * "Jina-OCR-v1: Efficient Document Parsing with Speculative Decoding and
+ * Dense Verifiable Rewards", Abstract: a single draft block shared across the
+ * K prediction steps).  The pages leave the block's inputs open; reading
+ * taken: step i adds the embedding of the previous token to the running
+ * hidden state, applies the block (config c with one expert of weight 1, no
+ * attention), and takes the verifier's greedy head:
+ *   h = h_prev;  t = t_prev;
+ *   for i < K:  h += E[t];  h = block(h);  t = argmax(lm_head . bf16(RMSNorm_f(h)));  drafts[i] = t.
+ * hidden_out [K*d] (h after each step) and gaps [K] (top-2 logit gaps) may be
+ * NULL.  Returns 0, or -1 if an id falls outside [0, V). */
+ORACLE_API int32_t oracle_draft(const oracle_config* c, const oracle_weights* w,
+                                const double* h_prev, int32_t t_prev, int32_t K, int32_t* drafts,
+                                double* hidden_out, double* gaps) {
+  const int d = c->hidden;
+  double* h = (double*)malloc(sizeof(double) * (size_t)d);
+  memcpy(h, h_prev, sizeof(double) * (size_t)d);
+  int32_t t = t_prev;
+  int32_t rc = 0;
+  for (int i = 0; i < K; ++i) {
+    if (t < 0 || t >= c->vocab) {
+      rc = -1;
+      break;
+    }
+    const uint16_t* erow = w->embed + (size_t)t * d;
+    for (int m = 0; m < d; ++m) h[m] += oracle_bf16_value(erow[m]);
+    oracle_layer(c, w, 0, h, NULL, NULL, NULL, NULL, NULL);
+    t = oracle_head(c, w, h, NULL, gaps ? gaps + i : NULL);
+    drafts[i] = t;
+    if (hidden_out) memcpy(hidden_out + (size_t)i * d, h, sizeof(double) * (size_t)d);
+  }
+  free(h);
+  return rc;
+}

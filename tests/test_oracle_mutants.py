@@ -49,6 +49,14 @@ MUTANTS = {
     "accept keeps later matches": ("while (n < K && d[n] == y[n]) ++n;",
                                    "for (int i = 0; i < K; ++i) n += (d[i] == y[i]);"),
     "bf16 ties away from zero": ("double r = nearbyint(q);", "double r = round(q);"),
+    "draft skips the embedding": ("for (int m = 0; m < d; ++m) h[m] += oracle_bf16_value(erow[m]);",
+                                  "(void)erow;"),
+    "draft restarts from h_prev": ("    drafts[i] = t;\n",
+                                   "    drafts[i] = t;\n    if (!hidden_out) memcpy(h, h_prev, sizeof(double) * (size_t)d);\n"
+                                   "    else { memcpy(hidden_out + (size_t)i * d, h, sizeof(double) * (size_t)d);"
+                                   " memcpy(h, h_prev, sizeof(double) * (size_t)d); continue; }\n"),
+    "draft block applied once": ("    oracle_layer(c, w, 0, h, NULL, NULL, NULL, NULL, NULL);",
+                                 "    if (i == 0) oracle_layer(c, w, 0, h, NULL, NULL, NULL, NULL, NULL);"),
 }
 
 

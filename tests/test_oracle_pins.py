@@ -510,3 +510,63 @@ def test_commit_rate_closed_form_and_printed_value(tiny_g):
         var = sum((2 * i + 1) * q ** i for i in range(K + 1)) - mean ** 2
         sigma = math.sqrt(var / len(totals))
         assert abs(np.mean(totals) - mean) < 3.5 * sigma, (K, p, np.mean(totals), mean)
+
+
+# ------------------------------------------------------------ draft head
+
+def _successor_draft_head(V=16, d=64):
+    """A draft head whose greedy drafts are t+1, t+2, ... (mod V): identity
+    block (zero down projection), embedding E[t] = 8 e_{t+1} - 8 e_t and a
+    one-hot lm_head (logit v = coordinate v of the normalised state)."""
+    import dataclasses
+    cfg = dataclasses.replace(S.DRAFT_TINY, hidden=d, vocab=V)
+    w = S.make_weights(cfg, seed=S.SEED_DRAFT_HEAD, with_embed=False, with_lm_head=False)
+    w["w_down"] = np.zeros_like(w["w_down"])
+    eight, minus_eight, one = _bf(8.0), _bf(-8.0), _bf(1.0)
+    emb = np.zeros((V, d), np.uint16)
+    for t in range(V):
+        emb[t, (t + 1) % V] = eight
+        emb[t, t] = minus_eight
+    lm = np.zeros((V, d), np.uint16)
+    for v in range(V):
+        lm[v, v] = one
+    w["embed"], w["lm_head"] = emb, lm
+    w["final_norm"] = np.full((d,), one, np.uint16)
+    return cfg, w
+
+
+def test_draft_head_successor_construction():
+    """From h = 0 and token t the recursion adds E[t], keeps the running
+    state and takes the greedy head at every step: drafts t+1, t+2, t+3 and
+    hidden 8 e_{t+i} - 8 e_t after step i."""
+    cfg, w = _successor_draft_head()
+    o = O.Oracle(cfg, w)
+    V, d = cfg.vocab, cfg.hidden
+    for t in range(V):
+        drafts, hid, gaps = o.draft(np.zeros(d), t, 3)
+        assert list(drafts) == [(t + i) % V for i in (1, 2, 3)], (t, drafts)
+        for i in range(3):
+            want = np.zeros(d)
+            want[(t + i + 1) % V] = 8.0
+            want[t] = -8.0
+            assert np.array_equal(hid[i], want), (t, i)
+        assert np.all(gaps > 0)
+
+
+def test_draft_head_composes_block_and_head_per_step():
+    """Each step is h += E[t], then the (separately pinned) block and head,
+    with the state carried to the next step."""
+    tw = S.make_weights(S.TINY)
+    dw = S.make_draft_weights(S.DRAFT_TINY, tw)
+    o = O.Oracle(S.DRAFT_TINY, dw)
+    emb = S.bf16_bits_to_f32(tw["embed"]).astype(np.float64)
+    for t0 in (0, 5, 511):
+        h0 = S.bf16_bits_to_f32(S.normal_bf16((64,), 21 + t0, 0, 0.5)).astype(np.float64)
+        drafts, hid, _ = o.draft(h0, t0, 3)
+        h, t = h0.copy(), t0
+        for i in range(3):
+            h, *_ = o.layer(0, h + emb[t])
+            t, _, _ = o.head(h)
+            assert drafts[i] == t and np.array_equal(hid[i], h), (t0, i)
+    with pytest.raises(ValueError):
+        o.draft(np.zeros(64), 512, 1)
