@@ -175,6 +175,39 @@ MOE_VERIFY_API int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* ho
                            int32_t* host_committed, int32_t* host_accept_len,
                            void* cuda_stream);
 
+/* FastMTP draft head ("Jina AI Releases jina-ocr-v1, a 3.4B MoE Document
+ * Parser With Built-In Speculative Decoding", FastMTP paragraph: one dense
+ * draft block applied recursively for K steps with constant parameters;
+ * "Jina-OCR-v1: ...", Abstract: one draft block shared across the K steps).
+ * The pages leave the block's inputs open; reading taken here: from the
+ * verifier's final residual h_prev of a sequence's last accepted position and
+ * the token t_prev committed there, each step does
+ *   h += E[t];  h = block(h);  t = argmax(lm_head . bf16(RMSNorm_f(h)));
+ * and emits t.  `ctx` is a context initialised with n_layers = 1 whose
+ * layer is the draft block (a dense block is one expert with top_k = 1 and
+ * no shared experts: its softmax weight is exactly 1) and whose embed,
+ * final_norm and lm_head are the verifier's.
+ *   h_prev [B, d] fp32 (16-byte aligned), t_prev [B] int32 (device; ids
+ *   outside [0, V) set the sticky MOE_VERIFY_ERR_ID_RANGE flag and give -1
+ *   drafts), drafts [B, K] int32 written, hidden_out [K, B, d] fp32 (h after
+ *   each step) or NULL.  1 <= B <= max_batch * (max_k + 1), 1 <= K <= 15.
+ * Asynchronous on cuda_stream; capturable. */
+MOE_VERIFY_API int moe_verify_draft(moe_verify_ctx* ctx, const float* h_prev, const int32_t* t_prev,
+                                    int32_t B, int32_t K, int32_t* drafts, float* hidden_out,
+                                    void* cuda_stream);
+
+/* The draft head's inputs after moe_verify_step + moe_verify_accept on the
+ * verifier's context: for each sequence b, with n = max(accept_len[b], 0),
+ *   h_out[b] = the final residual (fp32, before the final RMSNorm) of verify
+ *              token b*(K+1) + n of the last step;
+ *   t_out[b] = committed[b*(K+1) + n]  (the last committed token).
+ * committed [B, K+1], accept_len [B] as written by moe_verify_accept (device);
+ * h_out [B, d] fp32 (16-byte aligned), t_out [B] int32 written.  B and K are
+ * those of the last step.  Asynchronous on cuda_stream; capturable. */
+MOE_VERIFY_API int moe_verify_draft_inputs(moe_verify_ctx* ctx, const int32_t* committed,
+                                           const int32_t* accept_len, int32_t B, int32_t K,
+                                           float* h_out, int32_t* t_out, void* cuda_stream);
+
 /* Diagnostic (no counterpart in the method): checks the bounded waits that
  * every step kernel uses, without a context.  One thread waits on an
  * mbarrier phase that nothing completes, then on a device flag that nothing

@@ -30,7 +30,7 @@ EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_veri
             "moe_verify_decode_host", "moe_verify_sync_status", "moe_verify_destroy",
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
             "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc",
-            "moe_verify_check_bounded_wait")
+            "moe_verify_check_bounded_wait", "moe_verify_draft", "moe_verify_draft_inputs")
 
 
 class Config(ctypes.Structure):
@@ -94,6 +94,10 @@ def load(build_if_missing: bool = True):
     L.moe_verify_set_timing.argtypes = [_P, _i32]
     L.moe_verify_get_timing.restype = _i32
     L.moe_verify_get_timing.argtypes = [_P, _P, _P, _i32]
+    L.moe_verify_draft.restype = _i32
+    L.moe_verify_draft.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
+    L.moe_verify_draft_inputs.restype = _i32
+    L.moe_verify_draft_inputs.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
     L.moe_verify_check_bounded_wait.restype = _i32
     L.moe_verify_check_bounded_wait.argtypes = [ctypes.c_int64, _P, _P]
     L.moe_verify_greedy_head_noalloc.restype = _i32
@@ -234,6 +238,37 @@ class MoeVerify:
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_layer")
         return h_out
+
+    def draft_inputs(self, committed, accept_len, h_out=None, t_out=None, stream=None):
+        """moe_verify_draft_inputs: (h [B, d] fp32, t [B] int32) of each
+        sequence's last accepted position after step + accept."""
+        import torch
+        B, K1 = committed.shape
+        if h_out is None:
+            h_out = torch.empty((B, self.cfg.hidden), dtype=torch.float32, device=committed.device)
+        if t_out is None:
+            t_out = torch.empty((B,), dtype=torch.int32, device=committed.device)
+        rc = self.lib.moe_verify_draft_inputs(self.handle, _ptr(_dev_i32(committed)),
+                                              _ptr(_dev_i32(accept_len)), B, K1 - 1, _ptr(h_out),
+                                              _ptr(t_out), _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_draft_inputs")
+        return h_out, t_out
+
+    def draft(self, h_prev, t_prev, K: int, drafts=None, hidden: bool = False, stream=None):
+        """moe_verify_draft on this (one-layer draft-block) context: drafts
+        [B, K] int32, and the state after each step [K, B, d] when hidden."""
+        import torch
+        B = t_prev.shape[0]
+        if drafts is None:
+            drafts = torch.empty((B, K), dtype=torch.int32, device=t_prev.device)
+        hid = (torch.empty((K, B, self.cfg.hidden), dtype=torch.float32, device=t_prev.device)
+               if hidden else None)
+        rc = self.lib.moe_verify_draft(self.handle, _ptr(h_prev), _ptr(_dev_i32(t_prev)), B, int(K),
+                                       _ptr(drafts), _ptr(hid), _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_draft")
+        return (drafts, hid) if hidden else drafts
 
     def decode_host(self, context_ids: np.ndarray, draft_ids: Optional[np.ndarray],
                     committed: np.ndarray, accept_len: np.ndarray, stream=None):

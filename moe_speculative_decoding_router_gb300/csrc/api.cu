@@ -565,18 +565,12 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   return MOE_VERIFY_OK;
 }
 
-static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
-                        int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
-                        cudaStream_t s) {
-  const int T = B * (K + 1);
-  StepShape sh;
-  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
-  const bool pdl = true;
-  for (int l = 0; l < ctx->L; ++l) {
-    int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
-                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1);
-    if (rc != MOE_VERIFY_OK) return rc;
-  }
+// Final RMSNorm (after the residual update of the last block) and the
+// greedy lm_head for T rows; clears the expert counters of the last block
+// (parity `last_parity`).  probe_hidden [T, d] and logits [T, V] may be NULL.
+static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int last_parity,
+                        int32_t* target_ids, float* probe_hidden, float* logits, cudaStream_t s,
+                        bool pdl) {
   mv::FinalParams fp = {};
   fp.T = T;
   fp.d = ctx->d;
@@ -587,9 +581,9 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   fp.y = ctx->y;
   fp.gain = ctx->final_gain;
   fp.out = ctx->xf;
-  fp.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
+  fp.probe_hidden = probe_hidden;
   fp.keys = ctx->keys;
-  fp.cnt_clear = ctx->cnt + (size_t)((ctx->L - 1) & 1) * ctx->E;
+  fp.cnt_clear = ctx->cnt + (size_t)last_parity * ctx->E;
   fp.n_cnt_clear = ctx->E;
   {
     Timed tm(ctx, 3, s);
@@ -607,7 +601,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   gp.n_chunks = sh.n_chunks_lm;
   gp.nch_lm = sh.nch_lm;
   gp.keys = ctx->keys;
-  gp.logits = probe ? probe->logits : nullptr;
+  gp.logits = logits;
   gp.targets = target_ids;
   gp.bad = ctx->bad;
   gp.done = ctx->done_lm;
@@ -616,6 +610,23 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
     CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, ctx->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
+}
+
+static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
+                        int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
+                        cudaStream_t s) {
+  const int T = B * (K + 1);
+  StepShape sh;
+  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
+  const bool pdl = true;
+  for (int l = 0; l < ctx->L; ++l) {
+    int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
+                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1);
+    if (rc != MOE_VERIFY_OK) return rc;
+  }
+  float* ph = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
+  return enqueue_head(ctx, T, sh, (ctx->L - 1) & 1, target_ids, ph, probe ? probe->logits : nullptr,
+                      s, pdl);
 }
 
 int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
@@ -745,6 +756,46 @@ int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
                      cudaMemcpyDeviceToHost, s));
   CK(cudaMemcpyAsync(host_accept_len, ctx->io_alen, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_draft_inputs(moe_verify_ctx* ctx, const int32_t* committed,
+                            const int32_t* accept_len, int32_t B, int32_t K, float* h_out,
+                            int32_t* t_out, void* cuda_stream) {
+  if (!ctx || !committed || !accept_len || !h_out || !t_out) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || K < 0 || (int64_t)B * (K + 1) > ctx->T_max) return MOE_VERIFY_ERR_ARG;
+  if (!aligned16(h_out)) return MOE_VERIFY_ERR_ARG;
+  CK(mv::launch_draft_inputs(ctx->h, committed, accept_len, B, K, ctx->d, h_out, t_out,
+                             static_cast<cudaStream_t>(cuda_stream)));
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_draft(moe_verify_ctx* ctx, const float* h_prev, const int32_t* t_prev, int32_t B,
+                     int32_t K, int32_t* drafts, float* hidden_out, void* cuda_stream) {
+  if (!ctx || !h_prev || !t_prev || !drafts) return MOE_VERIFY_ERR_ARG;
+  if (ctx->L != 1) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || B > ctx->T_max || K < 1 || K > 15) return MOE_VERIFY_ERR_ARG;
+  if (!aligned16(h_prev) || (hidden_out && !aligned16(hidden_out))) return MOE_VERIFY_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const int T = B;
+  StepShape sh;
+  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
+  const size_t hb = (size_t)T * ctx->d * sizeof(float);
+  CK(cudaMemcpyAsync(ctx->h, h_prev, hb, cudaMemcpyDeviceToDevice, s));
+  const int32_t* ids = t_prev;
+  for (int i = 0; i < K; ++i) {
+    // h += E[t];  the block;  t = greedy head of h
+    int rc = run_layer(ctx, 0, 0, mv::kSrcEmbedAdd, sh, ids, nullptr, B, 0, nullptr, nullptr, 0, s,
+                       true, true);
+    if (rc != MOE_VERIFY_OK) return rc;
+    rc = enqueue_head(ctx, T, sh, 0, ctx->io_targets, nullptr, nullptr, s, true);
+    if (rc != MOE_VERIFY_OK) return rc;
+    CK(mv::launch_scatter_column(ctx->io_targets, B, drafts, K, i, s));
+    if (hidden_out)
+      CK(cudaMemcpyAsync(hidden_out + (size_t)i * T * ctx->d, ctx->h, hb, cudaMemcpyDeviceToDevice,
+                         s));
+    ids = ctx->io_targets;
+  }
   return MOE_VERIFY_OK;
 }
 

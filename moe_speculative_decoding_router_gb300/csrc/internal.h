@@ -14,7 +14,9 @@ constexpr uint32_t kErrTimeout = 2u;
 constexpr uint32_t kErrInternal = 4u;
 
 // Sources of the residual stream entering a routing kernel.
-enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2 };
+// kSrcEmbedAdd: the running state h (written by the previous launch) plus
+// the embedding of each sequence's token (the draft head's step input).
+enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2, kSrcEmbedAdd = 3 };
 
 struct RouteParams {
   int T, B, K;          // verify tokens, sequences, drafts per sequence
@@ -135,6 +137,14 @@ cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, cons
                           int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
+
+// Draft head plumbing: h_out[b] = h[b*(K+1) + n_b], t_out[b] =
+// committed[b*(K+1) + n_b] with n_b = max(accept_len[b], 0).
+cudaError_t launch_draft_inputs(const float* h, const int32_t* committed, const int32_t* accept_len,
+                                int B, int K, int d, float* h_out, int32_t* t_out, cudaStream_t s);
+// dst[b * stride + col] = src[b], b < B.
+cudaError_t launch_scatter_column(const int32_t* src, int B, int32_t* dst, int stride, int col,
+                                  cudaStream_t s);
 
 // Self-check of the bounded waits (see moe_verify_check_bounded_wait).
 cudaError_t run_bounded_wait_check(uint64_t limit_ns, cudaStream_t s, unsigned long long* host_out,

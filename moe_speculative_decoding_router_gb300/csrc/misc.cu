@@ -142,6 +142,27 @@ __global__ void bounded_wait_check_kernel(const int32_t* flag, uint32_t* status,
   out[0] = globaltimer_ns() - t0;
 }
 
+// The draft head's inputs from a verify step: per sequence b, the final
+// residual of its accepted verify position n_b and the token committed
+// there (the last committed token).  One block per sequence.
+__global__ void draft_inputs_kernel(const float* __restrict__ h, const int32_t* __restrict__ committed,
+                                    const int32_t* __restrict__ accept_len, int K, int d,
+                                    float* __restrict__ h_out, int32_t* __restrict__ t_out) {
+  const int b = blockIdx.x;
+  const int n = max(accept_len[b], 0);
+  const size_t row = (size_t)b * (K + 1) + n;
+  const float4* src = reinterpret_cast<const float4*>(h + row * d);
+  float4* dst = reinterpret_cast<float4*>(h_out + (size_t)b * d);
+  for (int c = threadIdx.x; c < d / 4; c += blockDim.x) dst[c] = src[c];
+  if (threadIdx.x == 0) t_out[b] = committed[row];
+}
+
+__global__ void scatter_column_kernel(const int32_t* __restrict__ src, int B, int32_t* dst, int stride,
+                                      int col) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) dst[(size_t)b * stride + col] = src[b];
+}
+
 __device__ int32_t g_never_set;               // stays 0
 __device__ uint32_t g_check_status;
 __device__ unsigned long long g_check_out[3];
@@ -166,6 +187,18 @@ cudaError_t run_bounded_wait_check(uint64_t limit_ns, cudaStream_t s, unsigned l
     return e;
   if ((e = cudaMemcpyAsync(host_status, st, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return e;
   return cudaStreamSynchronize(s);
+}
+
+cudaError_t launch_draft_inputs(const float* h, const int32_t* committed, const int32_t* accept_len,
+                                int B, int K, int d, float* h_out, int32_t* t_out, cudaStream_t s) {
+  draft_inputs_kernel<<<B, 128, 0, s>>>(h, committed, accept_len, K, d, h_out, t_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_column(const int32_t* src, int B, int32_t* dst, int stride, int col,
+                                  cudaStream_t s) {
+  scatter_column_kernel<<<(B + 127) / 128, 128, 0, s>>>(src, B, dst, stride, col);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s) {

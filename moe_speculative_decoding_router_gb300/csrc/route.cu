@@ -134,7 +134,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
       }
     } else {
       const uint2* src;
-      if (SRC == kSrcEmbed) {
+      if (SRC == kSrcEmbed || SRC == kSrcEmbedAdd) {
         const int b = t / (p.K + 1), i = t % (p.K + 1);
         const int id = (i == 0) ? p.context_ids[b] : p.draft_ids[(size_t)b * p.K + (i - 1)];
         const bool ok = (id >= 0 && id < p.V);
@@ -147,7 +147,12 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
         src = reinterpret_cast<const uint2*>(p.h_in + (size_t)t * d);
       }
       for (int c = tid; c < nc; c += kRouteThreads) {
-        const float4 v = bf16x4_to_f4(__ldg(src + c));
+        float4 v = bf16x4_to_f4(__ldg(src + c));
+        if (SRC == kSrcEmbedAdd) {
+          // the running state, written by the previous launch: read after the wait
+          const float4 hv = __ldcg(hg + c);
+          v = make_float4(hv.x + v.x, hv.y + v.y, hv.z + v.z, hv.w + v.w);
+        }
         hx[c] = v;
         hg[c] = v;
         if (hp) hp[c] = v;
@@ -554,6 +559,7 @@ cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int gr
   switch (p.src) {
     case kSrcEmbed: return launch_route_src<kSrcEmbed>(map_wr, p, grid, smem, s, pdl);
     case kSrcBf16: return launch_route_src<kSrcBf16>(map_wr, p, grid, smem, s, pdl);
+    case kSrcEmbedAdd: return launch_route_src<kSrcEmbedAdd>(map_wr, p, grid, smem, s, pdl);
     default: return launch_route_src<kSrcCombine>(map_wr, p, grid, smem, s, pdl);
   }
 }

@@ -443,3 +443,177 @@ def test_decode_loop(full, Bn, K, p):
             last[b] = int(com[b, n])
     print(f"decode B={Bn} K={K} p={p}: {committed_total} committed, "
           f"{drift} differ from the oracle's free-running chain")
+
+
+# ------------------------------------------------------------- draft head
+
+@pytest.fixture(scope="module")
+def tiny_draft():
+    B = _B()
+    tw = S.make_weights(S.TINY)
+    dw = S.make_draft_weights(S.DRAFT_TINY, tw)
+    dctx = B.MoeVerify(S.DRAFT_TINY, B.weights_to_device(dw), max_batch=128, max_k=0)
+    yield dctx, O.Oracle(S.DRAFT_TINY, dw)
+    dctx.close()
+
+
+def _check_drafts(dorc, h, t, drafts, hidden, K):
+    """Each sequence's draft chain against the oracle's from the same inputs:
+    equal until a step whose top-2 logit gap is below the tie band (then the
+    rest of that chain is not compared); states within REL before it."""
+    ties = 0
+    for b in range(h.shape[0]):
+        od, oh, og = dorc.draft(h[b].astype(np.float64), int(t[b]), K)
+        for i in range(K):
+            if drafts[b, i] != od[i]:
+                assert og[i] < TIE, (b, i, int(drafts[b, i]), int(od[i]), og[i])
+                ties += 1
+                break
+            assert rel_err(hidden[i, b], oh[i]) <= REL, (b, i)
+    return ties
+
+
+def test_draft_head_tiny_matches_oracle(tiny, tiny_draft):
+    ctx, _ = tiny
+    dctx, dorc = tiny_draft
+    B = _B()
+    L = S.TINY.n_layers
+    ids = S.uniform_ids(128 * 4, 301, 3, 512).reshape(128, 4)
+    probe, pt = B.make_probe(L, 512, S.TINY)
+    dr = _i32(ids[:, 1:])
+    tg = ctx.step(_i32(ids[:, 0]), dr, probe=probe)
+    com, alen = ctx.accept(dr, tg)
+    h, t = ctx.draft_inputs(com, alen)
+    # the inputs: final residual and committed token of each accepted position
+    n = np.maximum(alen.cpu().numpy(), 0)
+    rows = np.arange(128) * 4 + n
+    hfin = pt["hidden"].cpu().numpy()[L]
+    assert np.array_equal(h.cpu().numpy(), hfin[rows])
+    assert np.array_equal(t.cpu().numpy(), com.cpu().numpy()[np.arange(128), n])
+    drafts, hidden = dctx.draft(h, t, 3, hidden=True)
+    torch.cuda.synchronize()
+    assert dctx.sync_status() == B.OK
+    ties = _check_drafts(dorc, h.cpu().numpy(), t.cpu().numpy(), drafts.cpu().numpy(),
+                         hidden.cpu().numpy(), 3)
+    print(f"draft tiny: 128 chains x 3 steps, {ties} logit near ties")
+
+
+def test_decode_loop_with_draft_head_is_lossless(tiny, tiny_draft):
+    """Verify, accept and draft on the device, drafts fed back: whatever the
+    draft head proposes, the committed stream is plain greedy decoding."""
+    ctx, _ = tiny
+    dctx, _ = tiny_draft
+    g = np.loadtxt(os.path.join(GOLDEN, "tiny_g_table.txt"), dtype=np.int64)
+    Bn, K = 16, 3
+    start = S.uniform_ids(Bn, 402, 0, 512).astype(np.int64)
+    streams = [[] for _ in range(Bn)]
+    # a first verify step without drafts, then K drafts per step
+    tg = ctx.step(_i32(start), None)
+    com, alen = ctx.accept(None, tg)
+    accepted = 0
+    for it in range(12):
+        comh, nh = com.cpu().numpy(), alen.cpu().numpy()
+        for b in range(Bn):
+            streams[b] += [int(x) for x in comh[b, : nh[b] + 1]]
+        accepted += int(nh.sum()) if it else 0
+        h, t = ctx.draft_inputs(com, alen)
+        dr = dctx.draft(h, t, K)
+        tg = ctx.step(t, dr)
+        com, alen = ctx.accept(dr, tg)
+    assert ctx.sync_status() == _B().OK and dctx.sync_status() == _B().OK
+    for b in range(Bn):
+        x, want = int(start[b]), []
+        for _ in range(len(streams[b])):
+            x = int(g[x])
+            want.append(x)
+        assert streams[b] == want, b
+    print(f"decode loop: {sum(map(len, streams))} tokens committed, {accepted} drafts accepted")
+
+
+@pytest.fixture(scope="module")
+def full_draft():
+    B = _B()
+    tw = S.make_weights(S.FULL)
+    dw = S.make_draft_weights(S.DRAFT, tw)
+    dctx = B.MoeVerify(S.DRAFT, B.weights_to_device(dw), max_batch=32, max_k=0)
+    torch.cuda.empty_cache()
+    yield dctx, O.Oracle(S.DRAFT, dw)
+    dctx.close()
+
+
+def test_draft_head_full_sampled(full, full_draft):
+    """The 1280-wide draft block (one 5120-wide SwiGLU) with the 129,280-token
+    head, B = 32 after a K = 3 verify step: 8 sampled chains vs the oracle."""
+    ctx, _ = full
+    dctx, dorc = full_draft
+    ids = S.uniform_ids(32 * 4, 511, 3, S.FULL.vocab).reshape(32, 4)
+    dr = _i32(ids[:, 1:])
+    tg = ctx.step(_i32(ids[:, 0]), dr)
+    com, alen = ctx.accept(dr, tg)
+    h, t = ctx.draft_inputs(com, alen)
+    drafts, hidden = dctx.draft(h, t, 3, hidden=True)
+    torch.cuda.synchronize()
+    assert dctx.sync_status() == _B().OK
+    pick = np.linspace(0, 31, 8).astype(int)
+    hh, tt = h.cpu().numpy()[pick], t.cpu().numpy()[pick]
+    dd, hd = drafts.cpu().numpy()[pick], hidden.cpu().numpy()[:, pick]
+    import concurrent.futures as fut
+
+    def one(j):
+        return _check_drafts(dorc, hh[j:j + 1], tt[j:j + 1], dd[j:j + 1], hd[:, j:j + 1], 3)
+
+    with fut.ThreadPoolExecutor(max_workers=threads()) as ex:
+        ties = sum(ex.map(one, range(len(pick))))
+    print(f"draft full: 8 chains x 3 steps, {ties} logit near ties")
+
+
+def test_decode_iteration_in_one_graph(full, full_draft):
+    """Verify step, accept, draft inputs and the K-step draft captured as one
+    CUDA graph: replays match the same calls made eagerly."""
+    ctx, _ = full
+    dctx, _ = full_draft
+    Bn, K = 32, 3
+    ids = S.uniform_ids(Bn * 4, 612, 3, S.FULL.vocab).reshape(Bn, 4)
+    c0, d0 = _i32(ids[:, 0]), _i32(ids[:, 1:])
+    # eager reference for three iterations
+    ref = []
+    c, d = c0.clone(), d0.clone()
+    for _ in range(3):
+        tg = ctx.step(c, d)
+        com, alen = ctx.accept(d, tg)
+        h, t = ctx.draft_inputs(com, alen)
+        d = dctx.draft(h, t, K)
+        c = t
+        ref.append((com.clone(), d.clone()))
+    # the same iteration as one graph on fixed buffers
+    in_c, in_d = c0.clone(), d0.clone()
+    tg = torch.empty((Bn, K + 1), dtype=torch.int32, device="cuda")
+    com = torch.empty_like(tg)
+    alen = torch.empty((Bn,), dtype=torch.int32, device="cuda")
+    h = torch.empty((Bn, S.FULL.hidden), dtype=torch.float32, device="cuda")
+    t = torch.empty((Bn,), dtype=torch.int32, device="cuda")
+    out_d = torch.empty((Bn, K), dtype=torch.int32, device="cuda")
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+
+    def iteration():
+        ctx.step(in_c, in_d, target_ids=tg, stream=st)
+        ctx.accept(in_d, tg, committed=com, accept_len=alen, stream=st)
+        ctx.draft_inputs(com, alen, h_out=h, t_out=t, stream=st)
+        dctx.draft(h, t, K, drafts=out_d, stream=st)
+
+    with torch.cuda.stream(st):
+        iteration()
+    st.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        iteration()
+    in_c.copy_(c0)
+    in_d.copy_(d0)
+    for r in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(com, ref[r][0]), r
+        assert torch.equal(out_d, ref[r][1]), r
+        in_c.copy_(t)
+        in_d.copy_(out_d)
