@@ -307,6 +307,14 @@ def run_ours(args, rank, world, local):
     ms = ev0.elapsed_time(ev1)
     clk = clocks.summary(w0, w1)
 
+    if args.profile and args.draft_head:
+        line = run_decode_iteration(args, ctx, cfg, w_host, dev, Bq, Kq, stream)
+        line["clocks"] = clk
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        ctx.close()
+        return
+
     if args.profile:
         if rank == 0:
             print(json.dumps({"profile": True, "layers": cfg.n_layers, "batch": Bq, "drafts": Kq,
@@ -429,6 +437,76 @@ def whole_job(ms, e_s, tokens, e_tokens, device):
     return float(mx[0]), float(mx[1]), float(sm[2]), float(sm[3])
 
 
+def run_decode_iteration(args, ctx, cfg, w_host, dev, Bq, Kq, stream):
+    """Timing of one whole decode iteration on the device (profiling only):
+    verify step + accept + draft inputs + the FastMTP draft head (K steps),
+    captured as one CUDA graph whose outputs feed its inputs, so replays run
+    the decode loop autonomously.  The draft head has random weights, so its
+    drafts are rarely accepted; the line reports time, not speed-up."""
+    import torch
+    from moe_speculative_decoding_router_gb300 import binding as BND
+    dw = S.make_draft_weights(S.DRAFT, w_host)
+    dctx = BND.MoeVerify(S.DRAFT, BND.weights_to_device(dw, device=dev), max_batch=Bq, max_k=0)
+    start = torch.from_numpy(S.start_ids(Bq, cfg.vocab).astype(np.int32)).to(dev)
+    in_c = start.clone()
+    in_d = torch.zeros((Bq, Kq), dtype=torch.int32, device=dev)
+    tg = torch.empty((Bq, Kq + 1), dtype=torch.int32, device=dev)
+    com, alen = torch.empty_like(tg), torch.empty((Bq,), dtype=torch.int32, device=dev)
+    h = torch.empty((Bq, cfg.hidden), dtype=torch.float32, device=dev)
+    t = torch.empty((Bq,), dtype=torch.int32, device=dev)
+    out_d = torch.empty((Bq, Kq), dtype=torch.int32, device=dev)
+    committed = torch.zeros((), dtype=torch.int64, device=dev)
+    cs = torch.cuda.Stream(device=dev)
+    cs.wait_stream(stream)
+
+    def iteration(draft=True):
+        ctx.step(in_c, in_d, target_ids=tg, stream=cs)
+        ctx.accept(in_d, tg, committed=com, accept_len=alen, stream=cs)
+        ctx.draft_inputs(com, alen, h_out=h, t_out=t, stream=cs)
+        if draft:
+            dctx.draft(h, t, Kq, drafts=out_d, stream=cs)
+        committed.add_((alen + 1).sum())
+        in_c.copy_(t)
+        in_d.copy_(out_d)
+
+    graphs = {}
+    for key in (True, False):
+        with torch.cuda.stream(cs):
+            iteration(key)
+        cs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            iteration(key)
+        graphs[key] = g
+    times = {}
+    for key in (True, False):
+        # replays and events on the same stream (a replay runs on the
+        # current stream)
+        with torch.cuda.stream(cs):
+            in_c.copy_(start)
+            in_d.zero_()
+            for _ in range(args.warmup):
+                graphs[key].replay()
+            cs.synchronize()
+            committed.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cs)
+            for _ in range(args.steps):
+                graphs[key].replay()
+            e1.record(cs)
+        torch.cuda.synchronize()
+        times[key] = (e0.elapsed_time(e1) / args.steps, float(committed.item()) / args.steps)
+    status = (ctx.sync_status(), dctx.sync_status())
+    dctx.close()
+    ms_it, com_it = times[True]
+    ms_verify = times[False][0]
+    return {"profile": True, "decode_iteration": True, "batch": Bq, "drafts": Kq,
+            "steps": args.steps, "ms_per_iteration": round(ms_it, 4),
+            "ms_verify_accept": round(ms_verify, 4), "ms_draft_head": round(ms_it - ms_verify, 4),
+            "committed_per_iteration": round(com_it, 2),
+            "note": "random draft weights: drafts are rarely accepted", "status": list(status)}
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def _cores():
@@ -524,11 +602,15 @@ def main():
                     help="profiling only: sequences per step (default 32)")
     ap.add_argument("--drafts", type=int, default=None,
                     help="profiling only: drafts per sequence, 0..15 (default 3)")
+    ap.add_argument("--draft-head", action="store_true",
+                    help="profiling only: time whole decode iterations with the FastMTP draft head")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if (args.layers or args.batch or args.drafts is not None) and not args.profile:
-        ap.error("--layers, --batch and --drafts are for profiling runs only (--profile)")
+    if (args.layers or args.batch or args.drafts is not None or args.draft_head) and not args.profile:
+        ap.error("--layers, --batch, --drafts and --draft-head are for profiling runs only (--profile)")
+    if args.draft_head and (args.layers or (args.drafts is not None and args.drafts < 1)):
+        ap.error("--draft-head needs the full stack and at least one draft")
     if args.drafts is not None and not 0 <= args.drafts <= 15:
         ap.error("--drafts must be in 0..15")
     if (args.batch or B_SEQ) * ((K_DRAFT if args.drafts is None else args.drafts) + 1) > 4096:
