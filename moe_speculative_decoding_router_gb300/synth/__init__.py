@@ -159,19 +159,26 @@ FULL = ModelConfig(12, 1280, 64, 6, 2, 896, 896, 129280, name="full")
 FULL_ZIPF = dataclasses.replace(FULL, zipf_s=1.2, name="full_zipf")
 
 
-# FastMTP draft heads: one dense block (a single SwiGLU expert of weight 1 on
-# every token, no routing choice) applied recursively, sharing the verifier's
-# embedding, final norm and lm_head.  The pages give no width: 4 x hidden.
-DRAFT_TINY = ModelConfig(1, 64, 1, 1, 0, 256, 256, 512, sigma=0.05, name="draft_tiny")
-DRAFT = ModelConfig(1, 1280, 1, 1, 0, 5120, 5120, 129280, name="draft")
+# FastMTP draft heads: one dense block applied recursively, sharing the
+# verifier's embedding, final norm and lm_head.  The pages give no width:
+# 4 x hidden.  A SwiGLU FFN is a sum over its intermediate units, so the dense
+# block of width 4d is held as 8 always-on (shared, weight 1) experts of width
+# d/2 -- its units in 8 groups -- which gives the GPU eight times as many
+# down-projection items; the stack's one routed expert has zero weights.
+DRAFT_TINY = ModelConfig(1, 64, 1, 1, 8, 32, 32, 512, sigma=0.05, name="draft_tiny")
+DRAFT = ModelConfig(1, 1280, 1, 1, 8, 64, 640, 129280, name="draft")
 
 
 def make_draft_weights(cfg: ModelConfig, target: Dict[str, np.ndarray],
                        seed: int = SEED_DRAFT_HEAD,
                        nthreads: Optional[int] = None) -> Dict[str, np.ndarray]:
-    """The draft block's own weights (seeded stream SEED_DRAFT_HEAD) plus the
-    verifier's embedding, final norm and lm_head (the same arrays)."""
+    """The draft block's own weights (seeded stream SEED_DRAFT_HEAD; the
+    routed expert zeroed, so the block is the dense FFN of the shared
+    experts) plus the verifier's embedding, final norm and lm_head (the same
+    arrays)."""
     w = make_weights(cfg, seed=seed, with_embed=False, with_lm_head=False, nthreads=nthreads)
+    for k in ("w_gate", "w_up", "w_down"):
+        w[k] = np.zeros_like(w[k])
     for k in ("embed", "final_norm", "lm_head"):
         w[k] = target[k]
     return w

@@ -522,6 +522,7 @@ def _successor_draft_head(V=16, d=64):
     cfg = dataclasses.replace(S.DRAFT_TINY, hidden=d, vocab=V)
     w = S.make_weights(cfg, seed=S.SEED_DRAFT_HEAD, with_embed=False, with_lm_head=False)
     w["w_down"] = np.zeros_like(w["w_down"])
+    w["s_down"] = np.zeros_like(w["s_down"])
     eight, minus_eight, one = _bf(8.0), _bf(-8.0), _bf(1.0)
     emb = np.zeros((V, d), np.uint16)
     for t in range(V):
@@ -570,3 +571,29 @@ def test_draft_head_composes_block_and_head_per_step():
             assert drafts[i] == t and np.array_equal(hid[i], h), (t0, i)
     with pytest.raises(ValueError):
         o.draft(np.zeros(64), 512, 1)
+
+
+def test_draft_block_groups_equal_one_dense_ffn():
+    """The draft block held as 8 shared experts (its intermediate units in 8
+    groups, weight 1 each) is the dense SwiGLU FFN of all the units: the same
+    weights as one expert of width 8 x 32 (top-1 of 1, weight exactly 1) give
+    the same state."""
+    import dataclasses
+    tw = S.make_weights(S.TINY)
+    dw = S.make_draft_weights(S.DRAFT_TINY, tw)
+    grouped = O.Oracle(S.DRAFT_TINY, dw)
+    S8, Is, d = S.DRAFT_TINY.n_shared, S.DRAFT_TINY.shared_inter, S.DRAFT_TINY.hidden
+    dense_cfg = dataclasses.replace(S.DRAFT_TINY, n_shared=0, expert_inter=S8 * Is)
+    dense_w = dict(dw)
+    dense_w["w_gate"] = dw["s_gate"].reshape(1, 1, S8 * Is, d)
+    dense_w["w_up"] = dw["s_up"].reshape(1, 1, S8 * Is, d)
+    dense_w["w_down"] = np.ascontiguousarray(
+        np.concatenate([dw["s_down"][0, s] for s in range(S8)], axis=1)).reshape(1, 1, d, S8 * Is)
+    for k in ("s_gate", "s_up", "s_down"):
+        dense_w[k] = np.zeros((1, 0) + dw[k].shape[2:], np.uint16)
+    dense = O.Oracle(dense_cfg, dense_w)
+    h0 = S.bf16_bits_to_f32(S.normal_bf16((d,), 77, 0, 0.5)).astype(np.float64)
+    a, ha, _ = grouped.draft(h0, 3, 3)
+    b, hb, _ = dense.draft(h0, 3, 3)
+    assert np.array_equal(a, b)
+    assert np.max(np.abs(ha - hb)) <= 1e-12 * np.max(np.abs(hb))
