@@ -85,3 +85,20 @@ def test_bounded_wait_check_rejects_limits_on_the_host():
     """Out-of-range limits are refused before any device work."""
     assert B.check_bounded_wait(10)[0] == B.ERR_ARG
     assert B.check_bounded_wait(2_000_000_000)[0] == B.ERR_ARG
+
+
+def test_entry_points_refuse_null_and_out_of_range_arguments_on_the_host():
+    """Argument errors come back as MOE_VERIFY_ERR_ARG before any device work
+    (so they need no GPU): null contexts and pointers, sizes out of range."""
+    L = B.load()
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails its checks first
+    assert L.moe_verify_step(None, p, p, 1, 0, p, None, None) == B.ERR_ARG
+    assert L.moe_verify_accept(None, p, p, 1, 0, p, p, None) == B.ERR_ARG
+    assert L.moe_verify_layer(None, 0, p, 1, p, None, None) == B.ERR_ARG
+    assert L.moe_verify_decode_host(None, p, p, 1, 0, p, p, None) == B.ERR_ARG
+    assert L.moe_verify_draft(None, p, p, 1, 1, p, None, None) == B.ERR_ARG
+    assert L.moe_verify_draft_inputs(None, p, p, 1, 0, p, p, None) == B.ERR_ARG
+    assert L.moe_verify_greedy_head_noalloc(None, p, p, 1, 64, 512, 1e-6, p, None) == B.ERR_ARG
+    assert L.moe_verify_check_bounded_wait(999, None, None) == B.ERR_ARG
+    assert L.moe_verify_check_bounded_wait(1_000_000_001, None, None) == B.ERR_ARG
+    assert L.moe_verify_sync_status(None) == B.ERR_ARG
