@@ -217,7 +217,8 @@ MOE_VERIFY_API int moe_verify_draft_inputs(moe_verify_ctx* ctx, const int32_t* c
  * NULL) holds the device time of the two waits.  Returns MOE_VERIFY_OK when
  * both waits gave up and raised the timeout bit, MOE_VERIFY_ERR_TIMEOUT
  * never, MOE_VERIFY_ERR_CUDA when a wait did not report (or on a CUDA error),
- * MOE_VERIFY_ERR_ARG for a limit out of range.  Synchronises cuda_stream. */
+ * MOE_VERIFY_ERR_ARG for a limit out of range.  Synchronises cuda_stream.
+ * Uses a few bytes of file-scope device memory: calls must not overlap. */
 MOE_VERIFY_API int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns,
                                                  void* cuda_stream);
 
