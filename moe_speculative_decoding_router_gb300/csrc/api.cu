@@ -244,6 +244,7 @@ struct Timed {
 
 struct StepShape {
   int T, tpb, grid_route, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
+  mv::LmLayout lm;
   bool wr_smem;
   size_t route_smem;
   // activation tiles of the expert FFN and the lm_head: one TMA box per stage,
@@ -267,10 +268,10 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
   s.nch = round_up(avg < 16 ? 16 : avg, 16);
   if (s.nch > 256) s.nch = 256;
   s.stages = mv::gemm_max_stages(s.nch);
-  s.n_chunks_lm = (T + 255) / 256;
-  s.nch_lm = round_up((T + s.n_chunks_lm - 1) / s.n_chunks_lm, 16);
-  int need = 2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm);
-  s.tmem_cols = pow2_at_least(need);
+  s.lm = mv::lm_layout(T);
+  s.n_chunks_lm = s.lm.n_chunks;
+  s.nch_lm = s.lm.nch;
+  s.tmem_cols = pow2_at_least(2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm));
   s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E, c->k, c->S);
   s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, c->k, c->S, s.wr_smem);
   if (encode_map(&s.map_x, c->xperm, c->d, c->rows_max, (uint32_t)s.nch) ||
@@ -593,8 +594,8 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   gp.n_items_static = (ctx->V_pad / 128) * sh.n_chunks_lm;
   gp.kblocks = ctx->d / 64;
   gp.nch = sh.nch_lm;
-  gp.stages = mv::gemm_max_stages(sh.nch_lm);
-  gp.tmem_cols = pow2_at_least(2 * sh.nch_lm);
+  gp.stages = sh.lm.stages;
+  gp.tmem_cols = sh.lm.tmem_cols;
   gp.status = ctx->status;
   gp.T = T;
   gp.V = ctx->V;
@@ -607,7 +608,7 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   gp.done = ctx->done_lm;
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, ctx->num_sms, s, pdl));
+    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, ctx->num_sms, s, pdl));
   }
   return MOE_VERIFY_OK;
 }

@@ -14,9 +14,16 @@
 // Once a CTA has issued its last load it pulls into L2 the weight item its
 // index starts with in the next kernel (next layer, or the lm_head).
 // lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
-// epilogue the running greedy argmax over the vocabulary.  The chunk's
-// normalised rows arrive as one TMA box per stage (the tensor map's box is
-// the chunk width): many small boxes per stage throttled the TMA unit.
+// epilogue the running greedy argmax over the vocabulary (two warp
+// reductions per token column, then across the four epilogue warps).
+// lmhead_tokm_kernel: the same product with the tokens on the MMA's M side
+// (65..128 tokens), so each epilogue thread holds one token's logits and
+// keeps its argmax in registers across the CTA's tiles.  Measured on the full
+// step, the second is faster from ~96 to 128 tokens and the first at 64
+// tokens or fewer and above 128 (there the vocabulary-on-M form loads each
+// tile once for up to 256 tokens).  Both load a chunk's normalised rows as
+// one TMA box per stage (the tensor map's box is the chunk width): many small
+// boxes per stage throttled the TMA unit.
 //
 // The weight rows sit on the MMA's M side (128) and the few tokens of an
 // expert on its N side (16..256), so every weight byte is streamed from HBM
@@ -52,11 +59,16 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   return v;
 }
 
+// Orderable 32-bit image of a float: larger float, larger unsigned value.
+__device__ __forceinline__ uint32_t orderable(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Orderable key of (logit, vocabulary id): larger logit first, then lower id.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
+  return ((unsigned long long)orderable(v) << 32) |
+         (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 
 // Barriers and flags at the start of the control area.
@@ -563,7 +575,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // the counters this launch used are cleared by the next routing kernel
 }
 
-// ------------------------------------------------------------- lm_head
+// ------------------------------------ lm_head, vocabulary rows on M (any T)
 
 struct LmItem {
   int a_row, b_row, n;
@@ -782,6 +794,238 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ------------------------------------------- lm_head, tokens on M (65..128)
+//
+// Tokens on the MMA's M side (a chunk of <= 128 rows; rows past the chunk's
+// box are whatever the stage holds next and their accumulator lanes are never
+// read), 128 vocabulary rows on N.  Each epilogue thread owns one token's TMEM
+// lane, so the greedy argmax over a tile is a running maximum in registers: no
+// cross-lane reduction, and one atomic per token per CTA and token chunk.
+// Items run vocabulary-major (item i: tile i / n_chunks, chunk i % n_chunks),
+// so the CTAs that read one vocabulary tile run side by side and share it
+// through L2; when n_chunks divides the grid a CTA keeps one chunk throughout.
+
+struct TokItem {
+  int x_row, w_row, n;  // first token of the chunk, first vocabulary row, tokens in the chunk
+};
+
+__device__ __forceinline__ TokItem tok_item(const GemmParams& p, int i) {
+  TokItem it;
+  const int vt = i / p.n_chunks, c = i - vt * p.n_chunks;
+  it.x_row = c * 128;
+  it.w_row = vt * 128;
+  it.n = min(128, p.T - it.x_row);
+  return it;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_tokm_kernel(const __grid_constant__ CUtensorMap map_w,
+                  const __grid_constant__ CUtensorMap map_x, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  // stage: [p.nch token rows x 64 columns][128 vocabulary rows x 64 columns]
+  const int x_bytes = p.nch * 128;
+  const int stage_bytes = x_bytes + kStageA;
+  uint8_t* stages = smem;
+  uint8_t* ctrl_base = smem + (size_t)p.stages * stage_bytes;
+  const Ctrl C = ctrl_at(ctrl_base, p.stages);
+  __shared__ int is_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.n_items_static;
+  const bool has_work = (int)blockIdx.x < n_items;
+
+  if (threadIdx.x == 0) {
+    init_ctrl(C, p.stages, 4, 1);
+    tma_prefetch_desc(&map_w);
+    tma_prefetch_desc(&map_x);
+  }
+  if (has_work && warp == 1) {
+    tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = has_work ? *C.tmem_slot : 0u;
+
+  if (has_work && warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    // The first ring of vocabulary tiles does not depend on earlier kernels:
+    // issue it before waiting for the final RMSNorm.
+    int i = blockIdx.x, kb = 0;
+    TokItem it = tok_item(p, i);
+    int pre = 0;
+    {
+      int pi = i, pk = kb;
+      TokItem pt = it;
+      while (pre < p.stages && pi < n_items) {
+        mbar_arrive_expect_tx(&C.full[pre], (uint32_t)stage_bytes);
+        tma_load_2d(stages + (size_t)pre * stage_bytes + x_bytes, &map_w, &C.full[pre], pk * 64,
+                    pt.w_row, pol_w);
+        ++pre;
+        if (++pk == p.kblocks) {
+          pk = 0;
+          pi += gridDim.x;
+          if (pi < n_items) pt = tok_item(p, pi);
+        }
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int s = 0; s < pre; ++s) {
+      tma_load_2d(stages + (size_t)s * stage_bytes, &map_x, &C.full[s], kb * 64, it.x_row, pol_x);
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = tok_item(p, i);
+      }
+    }
+    int stage = pre, issued = pre;
+    uint32_t phase = 0;
+    if (stage == p.stages) {
+      stage = 0;
+      phase = 1;
+    }
+    bool ok = true;
+    while (i < n_items) {
+      if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + (size_t)stage * stage_bytes;
+      mbar_arrive_expect_tx(&C.full[stage], (uint32_t)stage_bytes);
+      tma_load_2d(sa + x_bytes, &map_w, &C.full[stage], kb * 64, it.w_row, pol_w);
+      tma_load_2d(sa, &map_x, &C.full[stage], kb * 64, it.x_row, pol_x);
+      ++issued;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = tok_item(p, i);
+      }
+    }
+    if (!ok) producer_drain(C, issued, p.stages);
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (has_work && warp == 1 && lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = umma_idesc_bf16(128, 128);
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * 128);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(&C.full[stage], phase, C.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sx = smem_u32(stages + (size_t)stage * stage_bytes);
+          const uint32_t sw = sx + (uint32_t)x_bytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem_d, umma_desc_sw128(sx + kk * 32), umma_desc_sw128(sw + kk * 32), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&C.empty[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&C.tfull[buf]);
+      }
+      mma_drain(C);
+    } else if (has_work && warp >= 2) {
+      // ------------------------------------------------ epilogue warps 2..5
+      // thread = one token of the chunk (TMEM lane q*32 + lane)
+      const int q = warp & 3;
+      int local = 0, cur_x = -1;
+      uint32_t best_u = 0u;
+      int best_id = 0;
+      auto flush = [&]() {
+        const int tok = cur_x + q * 32 + lane;
+        if (cur_x >= 0 && tok < p.T && best_u != 0u)
+          atomicMax(p.keys + tok, ((unsigned long long)best_u << 32) |
+                                      (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_id));
+        best_u = 0u;
+      };
+      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+        const TokItem it = tok_item(p, i);
+        if (it.x_row != cur_x) {
+          flush();
+          cur_x = it.x_row;
+        }
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        if (q * 32 < it.n) {
+          const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 128);
+          const int vlim = min(128, p.V - it.w_row);  // vocabulary rows of this tile
+          const int tok = it.x_row + q * 32 + lane;
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16(tb + (uint32_t)c0, v0);
+            tmem_ld16(tb + (uint32_t)(c0 + 16), v1);
+            tmem_ld_wait();
+            // increasing vocabulary order with a strict comparison keeps the
+            // lowest id among equal logits
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float lv = __uint_as_float(j < 16 ? v0[j] : v1[j - 16]);
+              const int col = c0 + j;
+              if (col < vlim) {
+                const uint32_t u = orderable(lv);
+                if (u > best_u) {
+                  best_u = u;
+                  best_id = it.w_row + col;
+                }
+                if (p.logits && tok < p.T) p.logits[(size_t)tok * p.V + it.w_row + col] = lv;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.tempty[buf]);
+      }
+      flush();
+    }
+  }
+
+  __syncthreads();
+  if (has_work && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+  }
+  // the last CTA turns the argmax keys into token ids
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+      const unsigned long long key = __ldcg(p.keys + t);
+      const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+      p.targets[t] = (__ldg(p.bad + t) || key == 0ull) ? -1 : id;
+    }
+    if (threadIdx.x == 0) *p.done = 0u;
+  }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, bool pdl,
                            Args... args) {
@@ -822,10 +1066,30 @@ cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                         map_dn, map_a, map_pf, p);
 }
 
-cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
-                          int grid, cudaStream_t s, bool pdl) {
-  return launch_gemm_ex(lmhead_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, mapA, mapB,
-                        p);
+LmLayout lm_layout(int T) {
+  LmLayout l;
+  l.tokens_on_m = T > 64 && T <= 128;
+  if (l.tokens_on_m) {
+    l.n_chunks = 1;
+    l.nch = (T + 15) / 16 * 16;
+    l.tmem_cols = 256;  // two accumulators of 128 vocabulary columns
+  } else {
+    l.n_chunks = (T + 255) / 256;
+    l.nch = ((T + l.n_chunks - 1) / l.n_chunks + 15) / 16 * 16;
+    l.tmem_cols = 32;  // two accumulators of nch token columns
+    while (l.tmem_cols < 2 * l.nch) l.tmem_cols <<= 1;
+  }
+  l.stages = gemm_max_stages(l.nch);
+  return l;
+}
+
+cudaError_t launch_lmhead(const CUtensorMap& map_w, const CUtensorMap& map_x, const GemmParams& p,
+                          bool tokens_on_m, int grid, cudaStream_t s, bool pdl) {
+  if (tokens_on_m)
+    return launch_gemm_ex(lmhead_tokm_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl,
+                          map_w, map_x, p);
+  return launch_gemm_ex(lmhead_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_w,
+                        map_x, p);
 }
 
 }  // namespace mv

@@ -97,13 +97,13 @@ struct FinalParams {
 
 // The lm_head GEMM with its argmax epilogue.
 struct GemmParams {
-  int n_items_static;          // vocabulary tiles x token chunks
+  int n_items_static;          // vocabulary tiles (of 128) x token chunks
   int kblocks;                 // d / 64
-  int nch;                     // tokens per item (multiple of 16)
+  int nch;                     // token rows loaded per stage (multiple of 16)
   int stages;
   int tmem_cols;
   uint32_t* status;
-  int T, V, n_chunks, nch_lm;
+  int T, V, n_chunks, nch_lm;  // token chunks of nch_lm (= nch) rows
   unsigned long long* keys;    // [T]
   float* logits;               // [T, V] or nullptr
   int32_t* targets;            // [T]
@@ -133,8 +133,15 @@ cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_dn, const CUtensorMap& map_a,
                        const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
                        bool pdl);
-cudaError_t launch_lmhead(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmParams& p,
-                          int grid, cudaStream_t s, bool pdl);
+// The lm_head launch for T tokens: tokens on the MMA's M side for 65..128
+// tokens (one chunk), else vocabulary rows on M with chunks of <= 256 tokens.
+struct LmLayout {
+  bool tokens_on_m;
+  int nch, n_chunks, tmem_cols, stages;
+};
+LmLayout lm_layout(int T);
+cudaError_t launch_lmhead(const CUtensorMap& map_w, const CUtensorMap& map_x, const GemmParams& p,
+                          bool tokens_on_m, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
 

@@ -149,10 +149,11 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
-  const int nch = (T + 15) / 16 * 16;
+  // a chunk's normalised rows arrive as one box of nch rows
+  const mv::LmLayout lay = mv::lm_layout(T);
+  const int nch = lay.nch;
   CUtensorMap map_lm, map_xf;
-  // rows past V (the last vocabulary tile) and past T are read as zeros; the
-  // T normalised rows arrive as one box of nch rows
+  // rows past V (the last vocabulary tile) and past T are read as zeros
   if (!encode(&map_lm, lm_head, (uint64_t)d, (uint64_t)V, 128) ||
       !encode(&map_xf, scratch, (uint64_t)d, (uint64_t)kMaxTokens, (uint32_t)nch))
     return MOE_VERIFY_ERR_CUDA;
@@ -162,25 +163,23 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
                                          rms_eps, scratch);
   if (cudaGetLastError() != cudaSuccess) return MOE_VERIFY_ERR_CUDA;
 
-  int cols = 32;
-  while (cols < 2 * nch) cols <<= 1;
   mv::GemmParams gp = {};
-  gp.n_items_static = (V + 127) / 128;
+  gp.n_items_static = ((V + 127) / 128) * lay.n_chunks;
   gp.kblocks = d / 64;
   gp.nch = nch;
-  gp.stages = mv::gemm_max_stages(nch);
-  gp.tmem_cols = cols;
+  gp.stages = lay.stages;
+  gp.tmem_cols = lay.tmem_cols;
   gp.status = reinterpret_cast<uint32_t*>(scratch + kStatusOff);
   gp.T = T;
   gp.V = V;
-  gp.n_chunks = 1;
+  gp.n_chunks = lay.n_chunks;
   gp.nch_lm = nch;
   gp.keys = reinterpret_cast<unsigned long long*>(scratch + kKeysOff);
   gp.logits = nullptr;
   gp.targets = target_ids;
   gp.bad = reinterpret_cast<const int32_t*>(scratch + kBadOff);
   gp.done = reinterpret_cast<unsigned int*>(scratch + kDoneOff);
-  if (mv::launch_lmhead(map_lm, map_xf, gp, sms, s, false) != cudaSuccess)
+  if (mv::launch_lmhead(map_lm, map_xf, gp, lay.tokens_on_m, sms, s, false) != cudaSuccess)
     return MOE_VERIFY_ERR_CUDA;
   return MOE_VERIFY_OK;
 }

@@ -75,7 +75,9 @@ def test_tiny_every_id_matches_oracle(tiny):
     print("tiny:", stats)
 
 
-@pytest.mark.parametrize("Bn,K", [(1, 0), (1, 3), (3, 1), (4, 3), (128, 0), (77, 2)])
+# T = 68 and 96 reach the tokens-on-M lm_head with ragged chunks (65..128 tokens)
+@pytest.mark.parametrize("Bn,K", [(1, 0), (1, 3), (3, 1), (4, 3), (17, 3), (24, 3), (128, 0),
+                                  (77, 2)])
 def test_tiny_batch_shapes(tiny, Bn, K):
     ctx, orc = tiny
     ids = S.uniform_ids(Bn * (K + 1), 41 + Bn, K, 512).reshape(Bn, K + 1)
@@ -84,16 +86,23 @@ def test_tiny_batch_shapes(tiny, Bn, K):
     check_tokens(orc, ids.reshape(-1), got)
 
 
-def test_tiny_logits_probe(tiny):
+@pytest.mark.parametrize("Bn", [1, 20])  # T = 4: vocabulary rows on M; T = 80: tokens on M
+def test_tiny_logits_probe(tiny, Bn):
     ctx, orc = tiny
     B = _B()
-    ids = np.array([[5, 9, 300, 511]], dtype=np.int32)
-    probe, pt = B.make_probe(S.TINY.n_layers, 4, S.TINY, logits=True)
-    ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=probe)
+    if Bn == 1:
+        ids = np.array([[5, 9, 300, 511]], dtype=np.int32)
+    else:
+        ids = S.uniform_ids(Bn * 4, 61, 3, 512).reshape(Bn, 4)
+    T = ids.size
+    probe, pt = B.make_probe(S.TINY.n_layers, T, S.TINY, logits=True)
+    tg = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=probe)
     lg = pt["logits"].cpu().numpy()
-    for t in range(4):
-        r = orc.forward_token(int(ids[0, t]), force_sel=pt["topk_idx"].cpu().numpy()[:, t, :],
-                              logits=True)
+    # the argmax is the probe's own logits' argmax (ties to the lowest id)
+    assert np.array_equal(tg.cpu().numpy().reshape(-1), np.argmax(lg, axis=1))
+    for t in range(T):
+        r = orc.forward_token(int(ids.reshape(-1)[t]),
+                              force_sel=pt["topk_idx"].cpu().numpy()[:, t, :], logits=True)
         assert rel_err(lg[t], r["logits"]) <= REL
 
 
