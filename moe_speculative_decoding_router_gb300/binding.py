@@ -140,10 +140,32 @@ def _stream_handle(stream) -> Optional[int]:
     return s.cuda_stream
 
 
-def _dev_i32(t):
+def _check_dev(t, dtype, name: str, shape=None):
+    """t must be a contiguous CUDA tensor of `dtype` (and `shape`, where given):
+    the library reads and writes it as a dense array from its data pointer."""
     import torch
-    assert t.is_cuda and t.dtype == torch.int32 and t.is_contiguous(), "int32 contiguous CUDA tensor expected"
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype
+            or not t.is_contiguous()):
+        raise ValueError(f"{name}: a contiguous CUDA tensor of {dtype} is expected")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(shape)} expected, got {tuple(t.shape)}")
     return t
+
+
+def _dev_i32(t, name: str = "ids", shape=None):
+    import torch
+    return _check_dev(t, torch.int32, name, shape)
+
+
+def _host_i32(a, name: str, shape, writable: bool = False):
+    """a must be a C-contiguous int32 numpy array of `shape` (pinned memory
+    makes the library's copies asynchronous; pageable memory also works)."""
+    if (not isinstance(a, np.ndarray) or a.dtype != np.int32 or not a.flags["C_CONTIGUOUS"]
+            or a.shape != tuple(shape)):
+        raise ValueError(f"{name}: a C-contiguous int32 array of shape {tuple(shape)} is expected")
+    if writable and not a.flags["WRITEABLE"]:
+        raise ValueError(f"{name}: a writable array is expected")
+    return a
 
 
 def weights_to_device(w: Dict[str, np.ndarray], device="cuda") -> Dict[str, object]:
@@ -199,11 +221,16 @@ class MoeVerify:
     def step(self, context_ids, draft_ids, target_ids=None, probe: Optional[Probe] = None,
              stream=None):
         import torch
-        context_ids = _dev_i32(context_ids)
+        if getattr(context_ids, "ndim", 0) != 1:
+            raise ValueError("context_ids: a 1-D tensor [B] is expected")
+        context_ids = _dev_i32(context_ids, "context_ids")
         B = context_ids.shape[0]
         K = 0 if draft_ids is None else draft_ids.shape[1]
+        if K > 0:
+            _dev_i32(draft_ids, "draft_ids", (B, K))
         if target_ids is None:
             target_ids = torch.empty((B, K + 1), dtype=torch.int32, device=context_ids.device)
+        _dev_i32(target_ids, "target_ids", (B, K + 1))
         rc = self.lib.moe_verify_step(self.handle, _ptr(context_ids),
                                       _ptr(draft_ids) if K > 0 else None, B, K, _ptr(target_ids),
                                       ctypes.byref(probe) if probe is not None else None,
@@ -214,12 +241,19 @@ class MoeVerify:
 
     def accept(self, draft_ids, target_ids, committed=None, accept_len=None, stream=None):
         import torch
+        if getattr(target_ids, "ndim", 0) != 2:
+            raise ValueError("target_ids: a 2-D tensor [B, K + 1] is expected")
         B, K1 = target_ids.shape
         K = K1 - 1
+        _dev_i32(target_ids, "target_ids")
+        if K > 0 and draft_ids is not None:
+            _dev_i32(draft_ids, "draft_ids", (B, K))
         if committed is None:
             committed = torch.empty((B, K1), dtype=torch.int32, device=target_ids.device)
         if accept_len is None:
             accept_len = torch.empty((B,), dtype=torch.int32, device=target_ids.device)
+        _dev_i32(committed, "committed", (B, K1))
+        _dev_i32(accept_len, "accept_len", (B,))
         rc = self.lib.moe_verify_accept(self.handle, _ptr(draft_ids) if K > 0 else None,
                                         _ptr(target_ids), B, K, _ptr(committed), _ptr(accept_len),
                                         _stream_handle(stream))
@@ -229,9 +263,13 @@ class MoeVerify:
 
     def layer(self, layer: int, h_in, h_out=None, probe: Optional[Probe] = None, stream=None):
         import torch
+        if getattr(h_in, "ndim", 0) != 2:
+            raise ValueError("h_in: a 2-D tensor [T, hidden] is expected")
         T = h_in.shape[0]
+        _check_dev(h_in, torch.bfloat16, "h_in", (T, self.cfg.hidden))
         if h_out is None:
             h_out = torch.empty_like(h_in)
+        _check_dev(h_out, torch.bfloat16, "h_out", (T, self.cfg.hidden))
         rc = self.lib.moe_verify_layer(self.handle, int(layer), _ptr(h_in), T, _ptr(h_out),
                                        ctypes.byref(probe) if probe is not None else None,
                                        _stream_handle(stream))
@@ -243,14 +281,20 @@ class MoeVerify:
         """moe_verify_draft_inputs: (h [B, d] fp32, t [B] int32) of each
         sequence's last accepted position after step + accept."""
         import torch
+        if getattr(committed, "ndim", 0) != 2:
+            raise ValueError("committed: a 2-D tensor [B, K + 1] is expected")
         B, K1 = committed.shape
+        _dev_i32(committed, "committed")
+        _dev_i32(accept_len, "accept_len", (B,))
         if h_out is None:
             h_out = torch.empty((B, self.cfg.hidden), dtype=torch.float32, device=committed.device)
         if t_out is None:
             t_out = torch.empty((B,), dtype=torch.int32, device=committed.device)
-        rc = self.lib.moe_verify_draft_inputs(self.handle, _ptr(_dev_i32(committed)),
-                                              _ptr(_dev_i32(accept_len)), B, K1 - 1, _ptr(h_out),
-                                              _ptr(t_out), _stream_handle(stream))
+        _check_dev(h_out, torch.float32, "h_out", (B, self.cfg.hidden))
+        _dev_i32(t_out, "t_out", (B,))
+        rc = self.lib.moe_verify_draft_inputs(self.handle, _ptr(committed), _ptr(accept_len), B,
+                                              K1 - 1, _ptr(h_out), _ptr(t_out),
+                                              _stream_handle(stream))
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_draft_inputs")
         return h_out, t_out
@@ -259,12 +303,17 @@ class MoeVerify:
         """moe_verify_draft on this (one-layer draft-block) context: drafts
         [B, K] int32, and the state after each step [K, B, d] when hidden."""
         import torch
+        if getattr(t_prev, "ndim", 0) != 1:
+            raise ValueError("t_prev: a 1-D tensor [B] is expected")
         B = t_prev.shape[0]
+        _dev_i32(t_prev, "t_prev")
+        _check_dev(h_prev, torch.float32, "h_prev", (B, self.cfg.hidden))
         if drafts is None:
             drafts = torch.empty((B, K), dtype=torch.int32, device=t_prev.device)
+        _dev_i32(drafts, "drafts", (B, K))
         hid = (torch.empty((K, B, self.cfg.hidden), dtype=torch.float32, device=t_prev.device)
                if hidden else None)
-        rc = self.lib.moe_verify_draft(self.handle, _ptr(h_prev), _ptr(_dev_i32(t_prev)), B, int(K),
+        rc = self.lib.moe_verify_draft(self.handle, _ptr(h_prev), _ptr(t_prev), B, int(K),
                                        _ptr(drafts), _ptr(hid), _stream_handle(stream))
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_draft")
@@ -273,8 +322,15 @@ class MoeVerify:
     def decode_host(self, context_ids: np.ndarray, draft_ids: Optional[np.ndarray],
                     committed: np.ndarray, accept_len: np.ndarray, stream=None):
         """Host buffers in and out (pinned numpy views make the copies asynchronous)."""
+        if getattr(context_ids, "ndim", 0) != 1:
+            raise ValueError("context_ids: a 1-D array [B] is expected")
         B = context_ids.shape[0]
         K = 0 if draft_ids is None else draft_ids.shape[1]
+        _host_i32(context_ids, "context_ids", (B,))
+        if K > 0:
+            _host_i32(draft_ids, "draft_ids", (B, K))
+        _host_i32(committed, "committed", (B, K + 1), writable=True)
+        _host_i32(accept_len, "accept_len", (B,), writable=True)
         rc = self.lib.moe_verify_decode_host(
             self.handle, context_ids.ctypes.data,
             draft_ids.ctypes.data if K > 0 else None, B, K, committed.ctypes.data,
@@ -316,10 +372,16 @@ def greedy_head_noalloc(h, final_norm, lm_head, rms_eps: float, target_ids=None,
     for each row of h [T, d] (fp32 CUDA tensor), with no device allocation
     inside the call (target_ids may be passed preallocated)."""
     import torch
+    if getattr(h, "ndim", 0) != 2 or getattr(lm_head, "ndim", 0) != 2:
+        raise ValueError("h [T, d] and lm_head [V, d] are expected")
     T, d = h.shape
     V = lm_head.shape[0]
+    _check_dev(h, torch.float32, "h")
+    _check_dev(final_norm, torch.bfloat16, "final_norm", (d,))
+    _check_dev(lm_head, torch.bfloat16, "lm_head", (V, d))
     if target_ids is None:
         target_ids = torch.empty((T,), dtype=torch.int32, device=h.device)
+    _dev_i32(target_ids, "target_ids", (T,))
     rc = load().moe_verify_greedy_head_noalloc(_ptr(h), _ptr(final_norm), _ptr(lm_head), T, d, V,
                                                 float(rms_eps), _ptr(target_ids),
                                                 _stream_handle(stream))
