@@ -57,6 +57,26 @@ MUTANTS = {
                                    " memcpy(h, h_prev, sizeof(double) * (size_t)d); continue; }\n"),
     "draft block applied once": ("    oracle_layer(c, w, 0, h, NULL, NULL, NULL, NULL, NULL);",
                                  "    if (i == 0) oracle_layer(c, w, 0, h, NULL, NULL, NULL, NULL, NULL);"),
+    "rmsnorm gain ignored": ("out[i] = oracle_round_bf16(h[i] / s * oracle_bf16_value(g[i]));",
+                             "out[i] = oracle_round_bf16(h[i] / s);"),
+    "rmsnorm divides by d - 1": ("double s = sqrt(ss / (double)d + eps);",
+                                 "double s = sqrt(ss / (double)(d - 1) + eps);"),
+    "routed outputs unweighted": ("for (int m = 0; m < d; ++m) acc[m] += psel[j] * y[m];",
+                                  "for (int m = 0; m < d; ++m) acc[m] += y[m];"),
+    "every slot weighted like the first": ("    p_sel[j] = p[best];", "    p_sel[j] = p[sel[0]];"),
+    "final norm with the first block's gain": (
+        "oracle_rmsnorm_bf16(h, w->final_norm, d, c->rms_eps, xf);",
+        "oracle_rmsnorm_bf16(h, w->norm[0], d, c->rms_eps, xf);"),
+    "lm_head on the unnormalised state": (
+        "oracle_rmsnorm_bf16(h, w->final_norm, d, c->rms_eps, xf);",
+        "for (int i = 0; i < d; ++i) xf[i] = oracle_round_bf16(h[i]);"),
+    "block uses the next block's router": ("oracle_router(xhat, w->router[l],",
+                                           "oracle_router(xhat, w->router[(l + 1) % c->n_layers],"),
+    "accept ignores bad targets": ("for (int i = 0; i <= K; ++i) bad |= (y[i] < 0 || y[i] >= V);",
+                                   "(void)0;"),
+    "accept takes id V as valid": ("bad |= (d[i] < 0 || d[i] >= V);", "bad |= (d[i] < 0 || d[i] > V);"),
+    "draft embeds the first token every step": ("const uint16_t* erow = w->embed + (size_t)t * d;",
+                                                "const uint16_t* erow = w->embed + (size_t)t_prev * d;"),
 }
 
 

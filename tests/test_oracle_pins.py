@@ -361,6 +361,27 @@ def test_forward_token_embedding_lm_head_and_argmax_ties():
     assert r["target"] == 0                   # every logit <= 0; lowest id among the zeros
 
 
+def test_final_norm_uses_its_own_gain():
+    """The greedy head normalises with the final RMSNorm's gain, not a block's.
+    With identity blocks and an all-ones embedding row, RMSNorm(h) = h / sqrt(1
+    + eps), which rounds to 1 in bf16, so xhat_f = g_f. One-hot lm_head rows
+    then make logit v = g_f[v]."""
+    cfg = S.TINY
+    d = cfg.hidden
+    w = _tiny_zero_down()                     # blocks add nothing: h_L = E[x]
+    w["embed"][:] = _bf(1.0)
+    w["final_norm"][:] = _bf(1.0)
+    w["final_norm"][5] = _bf(3.0)             # the final gain peaks at 5
+    w["norm"][:] = _bf(1.0)
+    w["norm"][:, 9] = _bf(5.0)                # the blocks' gains peak at 9
+    w["lm_head"][:] = 0
+    for v in range(d):
+        w["lm_head"][v, v] = _bf(1.0)
+    r = O.Oracle(cfg, w).forward_token(3, logits=True)
+    assert r["target"] == 5
+    assert r["logits"][5] == 3.0 and r["logits"][9] == 1.0 and r["logits"][0] == 1.0
+
+
 # -------------------------------------------------- acceptance and the loop
 
 def _ids(s):
