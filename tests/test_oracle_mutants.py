@@ -77,6 +77,12 @@ MUTANTS = {
     "accept takes id V as valid": ("bad |= (d[i] < 0 || d[i] >= V);", "bad |= (d[i] < 0 || d[i] > V);"),
     "draft embeds the first token every step": ("const uint16_t* erow = w->embed + (size_t)t * d;",
                                                 "const uint16_t* erow = w->embed + (size_t)t_prev * d;"),
+    "routed expert off by one": ("    int e = sel[j];", "    int e = (sel[j] + 1) % E;"),
+    "shared experts read the routed weights": (
+        "oracle_swiglu_expert(xhat, w->s_gate[l] + s * sh_in, w->s_up[l] + s * sh_in,",
+        "oracle_swiglu_expert(xhat, w->w_gate[l] + s * sh_in, w->w_up[l] + s * sh_in,"),
+    "gate projection rounded before SiLU": ("    double silu = g / (1.0 + exp(-g));\n",
+                                            "    g = q_bf16(g);\n    double silu = g / (1.0 + exp(-g));\n"),
 }
 
 
