@@ -199,8 +199,10 @@ int encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
 void free_all(moe_verify_ctx* c) {
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
+  // timing pairs not yet read back by moe_verify_get_timing are outside the pool
   for (auto& tp : c->pending) {
-    (void)tp;
+    cudaEventDestroy(tp.a);
+    cudaEventDestroy(tp.b);
   }
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
   c->event_pool.clear();
