@@ -71,15 +71,16 @@ class Trajectory:
         self.last = S.start_ids(B, self.V, first=rank * 1_000_000).astype(np.int64)
         self.done = np.zeros(B, dtype=np.int64)
         self.steps = np.zeros(B, dtype=np.int64)
+        self._rows = np.arange(B)
 
     def drafts(self):
         truth = np.empty((self.B, self.K), dtype=np.int64)
-        x = self.last.copy()
+        x = self.last
         for i in range(self.K):
             x = self.g[x]
             truth[:, i] = x
         d = self.src.drafts_batch(self.page_id, self.steps, truth)
-        return self.last.astype(np.int32).copy(), d
+        return self.last.astype(np.int32), d
 
     def advance(self, committed: np.ndarray, alen: np.ndarray) -> int:
         """Apply one step's outcome; returns the committed tokens it counts."""
@@ -87,8 +88,8 @@ class Trajectory:
         take = np.minimum(n + 1, self.page - self.done)
         self.done += take
         self.steps += 1
-        self.last = np.asarray(committed, dtype=np.int64)[np.arange(self.B), n]
-        for b in np.nonzero(self.done >= self.page)[0]:
+        self.last = np.asarray(committed, dtype=np.int64)[self._rows, n]
+        for b in np.flatnonzero(self.done >= self.page):
             self.page_id[b] = self.rank * 1_000_000 + self.next_page
             self.next_page += 1
             self.last[b] = int(S.start_ids(1, self.V, first=int(self.page_id[b]))[0])

@@ -245,6 +245,7 @@ class DraftSource:
 
     def __init__(self, p: float, V: int, K: int, seed: int = SEED_DRAFTS):
         self.p, self.V, self.K, self.seed = float(p), int(V), int(K), seed
+        self._lanes = np.arange(self.K, dtype=np.uint64).reshape(1, -1)
 
     def _index(self, seq: int, step: int, i: int) -> int:
         return ((seq * 1_000_003 + step) * 16 + i)
@@ -252,17 +253,19 @@ class DraftSource:
     def drafts_batch(self, seqs, steps, truth) -> np.ndarray:
         """drafts() for many sequences at once: seqs [B], steps [B],
         truth [B, K] -> [B, K] int32 (the same draws, counter-indexed)."""
-        seqs = np.asarray(seqs, dtype=np.uint64).reshape(-1, 1)
-        steps = np.asarray(steps, dtype=np.uint64).reshape(-1, 1)
+        seqs = np.asarray(seqs, dtype=np.uint64)
+        steps = np.asarray(steps, dtype=np.uint64)
         truth = np.asarray(truth).reshape(len(seqs), self.K)
-        j = np.ascontiguousarray((seqs * np.uint64(1_000_003) + steps) * np.uint64(16) +
-                                 np.arange(self.K, dtype=np.uint64).reshape(1, -1))
+        # counter index of (sequence, step, i), as in _index
+        j = ((seqs * np.uint64(1_000_003) + steps) * np.uint64(16))[:, None] + self._lanes
         u = np.empty(j.shape, dtype=np.float64)
         ids = np.empty(j.shape, dtype=np.int32)
         L = lib()
         L.synth_uniform_at(u.ctypes.data, j.ctypes.data, j.size, self.seed, TID_DRAFT_COIN)
         L.synth_ids_at(ids.ctypes.data, j.ctypes.data, j.size, self.seed, TID_DRAFT_ID, self.V)
-        return np.where(u < self.p, truth, ids).astype(np.int32)
+        hit = u < self.p
+        ids[hit] = truth[hit]
+        return ids
 
     def drafts(self, seq: int, step: int, truth) -> np.ndarray:
         """truth[i] = the greedy token the i-th draft should predict."""
