@@ -73,7 +73,7 @@ typedef enum {
 
 /* Shape of the target stack and the workspace bounds. */
 typedef struct {
-  int32_t n_layers;     /* L >= 1 (the decoder: 12) */
+  int32_t n_layers;     /* L: 1..256 (the decoder: 12) */
   int32_t hidden;       /* d: multiple of 64, <= 8192 (1280) */
   int32_t n_experts;    /* E routed experts: 1..256 (64) */
   int32_t top_k;        /* k: 1..min(E, 16) (6) */
@@ -81,9 +81,10 @@ typedef struct {
   int32_t expert_inter; /* I of a routed expert: 1..8192 (896) */
   int32_t shared_inter; /* I of a shared expert: 1..8192 (896) */
   int32_t vocab;        /* V: 2..2^30 (129280) */
-  float rms_eps;        /* RMSNorm epsilon (1e-6) */
+  float rms_eps;        /* RMSNorm epsilon, in (0, 1) (1e-6) */
   int32_t max_batch;    /* largest B a step may be given, >= 1 */
-  int32_t max_k;        /* largest K (drafts per sequence), 0..15 */
+  int32_t max_k;        /* largest K (drafts per sequence), 0..15;
+                           max_batch * (max_k + 1) <= 4096 (UNSUPPORTED above) */
 } moe_verify_config;
 
 /* Weights, all device pointers of bf16 patterns unless noted.  The per-layer

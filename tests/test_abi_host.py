@@ -61,6 +61,40 @@ def test_check_config():
     assert B.device_bytes(S.FULL, 0, 3) == 0
 
 
+_ARG, _UNS = "arg", "unsupported"
+
+
+@pytest.mark.parametrize("field,value,want", [
+    ("n_layers", 0, _ARG), ("n_layers", 257, _ARG), ("n_layers", 256, None),
+    ("hidden", 63, _ARG), ("hidden", 8256, _ARG), ("hidden", 1000, _UNS), ("hidden", 64, None),
+    ("n_experts", 0, _ARG), ("n_experts", 257, _ARG),
+    ("top_k", 0, _ARG), ("top_k", 17, _ARG), ("top_k", 64, _ARG),   # more than n_experts = 8
+    ("top_k", 8, None),                                               # every expert selected
+    ("n_shared", -1, _ARG), ("n_shared", 9, _ARG), ("n_shared", 0, None),
+    ("expert_inter", 0, _ARG), ("expert_inter", 8193, _ARG),
+    ("shared_inter", 0, _ARG), ("shared_inter", 8193, _ARG),
+    ("vocab", 1, _ARG), ("vocab", (1 << 30) + 1, _ARG), ("vocab", 2, None),
+    ("rms_eps", 0.0, _ARG), ("rms_eps", float("nan"), _ARG), ("rms_eps", 1.0, _ARG),
+    ("rms_eps", -1e-6, _ARG),
+])
+def test_check_config_refusals(field, value, want):
+    """Each refusal rule of moe_verify_check_config at its boundary, on the
+    tiny shape (8 experts, top-2, one shared expert, d = 64)."""
+    import dataclasses
+    cfg = dataclasses.replace(S.TINY, **{field: value})
+    code = {None: B.OK, _ARG: B.ERR_ARG, _UNS: B.ERR_UNSUPPORTED}[want]
+    assert B.check_config(cfg, 4, 3) == code
+
+
+@pytest.mark.parametrize("max_batch,max_k,want", [
+    (0, 3, B.ERR_ARG), (4, -1, B.ERR_ARG), (4, 16, B.ERR_ARG),
+    (256, 15, B.OK),                   # 4096 verify tokens: the largest workspace
+    (257, 15, B.ERR_UNSUPPORTED), (4097, 0, B.ERR_UNSUPPORTED), (4096, 0, B.OK),
+])
+def test_check_config_workspace_limits(max_batch, max_k, want):
+    assert B.check_config(S.TINY, max_batch, max_k) == want
+
+
 def test_device_bytes_is_weights_plus_workspace():
     n = B.device_bytes(S.FULL, 32, 3)
     per_expert = 3 * 896 * 1280 * 2
