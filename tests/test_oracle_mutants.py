@@ -83,6 +83,21 @@ MUTANTS = {
         "oracle_swiglu_expert(xhat, w->w_gate[l] + s * sh_in, w->w_up[l] + s * sh_in,"),
     "gate projection rounded before SiLU": ("    double silu = g / (1.0 + exp(-g));\n",
                                             "    g = q_bf16(g);\n    double silu = g / (1.0 + exp(-g));\n"),
+    "top-k selects one expert k times": ("    taken[best] = 1;", "    (void)taken;"),
+    "top-k never considers the last expert": ("      if (taken[e]) continue;",
+                                              "      if (taken[e] || e == E - 1) continue;"),
+    "lm_head read transposed": ("const uint16_t* row = w->lm_head + (size_t)v * d;",
+                                "const uint16_t* row = w->lm_head + (size_t)v;"),
+    "argmax never considers the last id": ("  for (int v = 0; v < V; ++v) {\n    double acc = 0.0;",
+                                           "  for (int v = 0; v < V - 1; ++v) {\n    double acc = 0.0;"),
+    "gate projection transposed": ("g += x * oracle_bf16_value(Wg[(size_t)j * d + i]);",
+                                   "g += x * oracle_bf16_value(Wg[(size_t)i * I + j]);"),
+    "up projection transposed": ("u += x * oracle_bf16_value(Wu[(size_t)j * d + i]);",
+                                 "u += x * oracle_bf16_value(Wu[(size_t)i * I + j]);"),
+    "combine added twice": ("for (int m = 0; m < d; ++m) h[m] += acc[m];",
+                            "for (int m = 0; m < d; ++m) h[m] += 2.0 * acc[m];"),
+    "eps added after the square root": ("double s = sqrt(ss / (double)d + eps);",
+                                        "double s = sqrt(ss / (double)d) + eps;"),
 }
 
 
