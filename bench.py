@@ -166,24 +166,216 @@ class ClockSampler:
 # ----------------------------------------------------------------- our arm
 
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def algorithmic_ffn_bytes(topk_idx: np.ndarray, cfg) -> float:
-    """Bytes one expert-FFN launch (one layer) must move at least: the gate,
-    up and down weights of every touched expert (routed + shared) once, the
-    expert-major normalised inputs read once, the SwiGLU rows written and read
-    once (bf16), and the weighted fp32 outputs written once.  topk_idx: [T, k]."""
-    T = topk_idx.shape[0]
-    touched = len(np.unique(topk_idx)) + cfg.n_shared
-    rows = T * (cfg.top_k + cfg.n_shared)
-    d, I = cfg.hidden, cfg.expert_inter
-    return touched * 3 * I * d * 2 + rows * d * 2 + 2 * rows * I * 2 + rows * d * 4
+def expert_weight_bytes(topk_idx_layer: np.ndarray, cfg) -> float:
+    """Algorithmic bytes of one expert-FFN launch (one layer): the gate, up and
+    down weights of every touched expert (routed + shared), once.
+    Intermediate activations are not counted.  topk_idx_layer: [T, k]."""
+    touched = len(np.unique(topk_idx_layer)) + cfg.n_shared
+    return float(touched * 3 * cfg.expert_inter * cfg.hidden * 2)
+
+
+def step_bytes(topk_idx: np.ndarray, cfg, T: int) -> float:
+    """Algorithmic bytes of one verify step: the touched experts' weights of
+    every layer, the routers, the norms' gains, the whole lm_head, the
+    embedding rows of the verify tokens, ids in and out.  topk_idx: [L, T, k]."""
+    L, d, E, V = cfg.n_layers, cfg.hidden, cfg.n_experts, cfg.vocab
+    b = sum(expert_weight_bytes(topk_idx[l], cfg) for l in range(L))
+    return b + L * E * d * 2 + (L + 1) * d * 2 + V * d * 2 + T * d * 2 + T * 4 * 3
+
+
+def step_flops(cfg, T: int) -> float:
+    """Flops of one verify step, selected-expert work only: routed and shared
+    expert rows (gate, up, down), the routers, the lm_head."""
+    L, d, E, k, S, I, V = (cfg.n_layers, cfg.hidden, cfg.n_experts, cfg.top_k, cfg.n_shared,
+                           cfg.expert_inter, cfg.vocab)
+    return float(L * (T * (k + S) * 6 * d * I + 2 * T * d * E) + 2 * T * d * V)
+
+
+def kernel_digest() -> str:
+    """Digest of the CUDA sources of the kernels, to tell whether a stored ncu
+    figure was taken on the kernels that run now."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_speculative_decoding_router_gb300", "csrc")
+    for name in ("gemm.cu", "route.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def greedy_table(ctx, V: int, K: int, dev, max_batch: int):
+    """The library's own greedy target of every id, max_batch * (K+1) ids per call."""
+    import torch
+    g = np.empty(V, dtype=np.int32)
+    chunk = max_batch * (K + 1)
+    all_ids = torch.arange(V, dtype=torch.int32, device=dev)
+    for s0 in range(0, V, chunk):
+        n = min(chunk, V - s0)
+        Bn = (n + K) // (K + 1)
+        ids = torch.zeros(Bn * (K + 1), dtype=torch.int32, device=dev)
+        ids[:n] = all_ids[s0:s0 + n]
+        ids = ids.view(Bn, K + 1)
+        tg = ctx.step(ids[:, 0].contiguous(), ids[:, 1:].contiguous() if K else None)
+        g[s0:s0 + n] = tg.view(-1)[:n].cpu().numpy()
+    return g
+
+
+class Plan:
+    """A decode trajectory planned on the host from a greedy table: every
+    step's inputs, its expected commits and the tokens it counts."""
+
+    def __init__(self, g, rank, B, K, p, total):
+        traj = Trajectory(g, rank, B=B, K=K, p=p)
+        self.ctx = np.empty((total, B), np.int32)
+        self.dr = np.empty((total, B, K), np.int32)
+        self.com = np.empty((total, B, K + 1), np.int32)
+        self.alen = np.empty((total, B), np.int32)
+        self.counted = np.zeros(total, np.int64)
+        for i in range(total):
+            c, d = traj.drafts()
+            com, n = traj.expected(c, d)
+            self.ctx[i], self.dr[i], self.com[i], self.alen[i] = c, d, com, n
+            self.counted[i] = traj.advance(com, n)
+
+
+class StepGraph:
+    """step + accept on fixed buffers, captured as one CUDA graph; each replay
+    copies the step's inputs in from HBM and its outputs out."""
+
+    def __init__(self, ctx, B, K, dev, stamps=None):
+        import torch
+        self.B, self.K = B, K
+        self.in_ctx = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.in_dr = torch.zeros((B, K), dtype=torch.int32, device=dev)
+        self.tg = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        self.com = torch.empty_like(self.tg)
+        self.alen = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.stream.wait_stream(torch.cuda.current_stream())
+        dr = self.in_dr if K else None
+
+        def body():
+            ctx.step(self.in_ctx, dr, target_ids=self.tg, stream=self.stream)
+            ctx.accept(dr, self.tg, committed=self.com, accept_len=self.alen, stream=self.stream)
+
+        with torch.cuda.stream(self.stream):
+            body()
+        self.stream.synchronize()
+        if stamps is not None:
+            ctx.set_stamps(stamps)
+        try:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                body()
+        finally:
+            if stamps is not None:
+                ctx.set_stamps(None)
+        torch.cuda.current_stream().wait_stream(self.stream)
+
+    def run(self, d_ctx, d_dr, i, d_com=None, d_alen=None):
+        self.in_ctx.copy_(d_ctx[i], non_blocking=True)
+        if self.K:
+            self.in_dr.copy_(d_dr[i], non_blocking=True)
+        self.graph.replay()
+        if d_com is not None:
+            d_com[i].copy_(self.com, non_blocking=True)
+            d_alen[i].copy_(self.alen, non_blocking=True)
+
+
+def timed_plan(ctx, plan, B, K, warmup, steps, dev, dist=None, clocks=None):
+    """Replays the plan's steps through one step graph; returns (ms for the
+    timed steps, commits [steps, B, K+1], accept lengths [steps, B], clocks)."""
+    import torch
+    d_ctx = torch.from_numpy(plan.ctx).to(dev)
+    d_dr = torch.from_numpy(plan.dr).to(dev)
+    total = warmup + steps
+    d_com = torch.empty((total, B, K + 1), dtype=torch.int32, device=dev)
+    d_alen = torch.empty((total, B), dtype=torch.int32, device=dev)
+    sg = StepGraph(ctx, B, K, dev)
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        sg.run(d_ctx, d_dr, i, d_com, d_alen)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(warmup, total):
+        sg.run(d_ctx, d_dr, i, d_com, d_alen)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    if dist:
+        dist.barrier()
+    clk = None
+    if clocks:
+        time.sleep(0.2)
+        clocks.stop()
+        clk = clocks.summary(w0, w1)
+    ms = ev0.elapsed_time(ev1)
+    return ms, d_com[warmup:].cpu().numpy(), d_alen[warmup:].cpu().numpy(), clk
+
+
+def probe_pass(ctx, cfg, plan, B, K, first, n, dev):
+    """Routing of steps first .. first+n-1 of a plan (eager, with the probe):
+    returns a list of topk_idx [L, T, k] arrays."""
+    import torch
+    from moe_speculative_decoding_router_gb300 import binding as BND
+    T = B * (K + 1)
+    probe, pt = BND.make_probe(cfg.n_layers, T, cfg, topk=True, hidden=False, device=dev)
+    out = []
+    for i in range(first, first + n):
+        ctx.step(torch.from_numpy(plan.ctx[i]).to(dev),
+                 torch.from_numpy(plan.dr[i]).to(dev) if K else None, probe=probe)
+        out.append(pt["topk_idx"].cpu().numpy())
+    return out
+
+
+def fractions(bytes_per_step, flops_per_step, ms_per_step, peaks):
+    hbm, _, tf_sus, _ = peaks
+    gbs = bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    tfs = flops_per_step / (ms_per_step * 1e-3) / 1e12
+    return {"hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+            "tensor_tflops": round(tfs, 1), "tensor_frac": round(tfs / tf_sus, 4)}
+
+
+def in_graph_stamps(ctx, cfg, plan, B, K, first, n, dev):
+    """Per-launch device times of the step's kernels inside a graph-replayed
+    step (launch timestamps): returns arrays [n, 2L+1, 3] of (start, ready,
+    end) in ns relative to each step's first start."""
+    import torch
+    L = cfg.n_layers
+    stamps = torch.zeros((2 * L + 1, 4), dtype=torch.int64, device=dev)
+    init = torch.zeros_like(stamps)
+    init[:, 0] = -1
+    sg = StepGraph(ctx, B, K, dev, stamps=stamps)
+    d_ctx = torch.from_numpy(plan.ctx).to(dev)
+    d_dr = torch.from_numpy(plan.dr).to(dev)
+    out = []
+    for i in range(first, first + n):
+        stamps.copy_(init)
+        sg.run(d_ctx, d_dr, i)
+        torch.cuda.synchronize()
+        st = stamps.cpu().numpy().view(np.uint64)[:, :3].astype(np.float64)
+        out.append(st - st[0, 0])
+    return np.stack(out)
 
 
 def run_ours(args, rank, world, local):
@@ -209,104 +401,24 @@ def run_ours(args, rank, world, local):
     del w_dev
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
 
-    # greedy table g over the whole vocabulary, 4,096 verify tokens per call
-    # (profiling runs use a random table instead: same kernels, same shapes)
+    # the library's greedy table over the whole vocabulary (profiling runs use
+    # a random table instead: same kernels, same shapes)
     V = cfg.vocab
-    g = np.empty(V, dtype=np.int32)
     if args.profile:
-        g[:] = S.uniform_ids(V, 99, 0, V)
-    chunk = 1024 * (Kq + 1)
-    all_ids = torch.arange(V, dtype=torch.int32, device=dev)
-    for s0 in (range(0, V, chunk) if not args.profile else ()):
-        n = min(chunk, V - s0)
-        Bn = (n + Kq) // (Kq + 1)
-        ids = torch.zeros(Bn * (Kq + 1), dtype=torch.int32, device=dev)
-        ids[:n] = all_ids[s0:s0 + n]
-        ids = ids.view(Bn, Kq + 1)
-        tg = ctx.step(ids[:, 0].contiguous(), ids[:, 1:].contiguous())
-        g[s0:s0 + n] = tg.view(-1)[:n].cpu().numpy()
+        g = S.uniform_ids(V, 99, 0, V).astype(np.int32)
+    else:
+        g = greedy_table(ctx, V, Kq, dev, 1024)
     assert ctx.sync_status() == BND.OK
 
-    # the decode trajectory, planned on the host
     total = args.warmup + args.steps
-    traj = Trajectory(g, rank, B=Bq, K=Kq)
-    plan_ctx = np.empty((total, Bq), np.int32)
-    plan_dr = np.empty((total, Bq, Kq), np.int32)
-    plan_com = np.empty((total, Bq, Kq + 1), np.int32)
-    plan_alen = np.empty((total, Bq), np.int32)
-    counted = np.zeros(total, np.int64)
-    for i in range(total):
-        c, d = traj.drafts()
-        com, n = traj.expected(c, d)
-        plan_ctx[i], plan_dr[i], plan_com[i], plan_alen[i] = c, d, com, n
-        counted[i] = traj.advance(com, n)
+    plan = Plan(g, rank, Bq, Kq, P_MATCH, total)
     setup_s = time.perf_counter() - t_setup
 
-    d_ctx = torch.from_numpy(plan_ctx).to(dev)
-    d_dr = torch.from_numpy(plan_dr).to(dev)
-    d_tg = torch.empty((total, Bq, Kq + 1), dtype=torch.int32, device=dev)
-    d_com = torch.empty_like(d_tg)
-    d_alen = torch.empty((total, Bq), dtype=torch.int32, device=dev)
-
-    # one CUDA graph per step: step + accept on fixed buffers, inputs copied in
-    in_ctx = torch.empty((Bq,), dtype=torch.int32, device=dev)
-    in_dr = torch.empty((Bq, Kq), dtype=torch.int32, device=dev)
-    out_tg = torch.empty((Bq, Kq + 1), dtype=torch.int32, device=dev)
-    out_com = torch.empty_like(out_tg)
-    out_alen = torch.empty((Bq,), dtype=torch.int32, device=dev)
-    in_ctx.copy_(d_ctx[0])
-    in_dr.copy_(d_dr[0])
-    cs = torch.cuda.Stream(device=dev)
-    cs.wait_stream(stream)
-    graph = None
-    if not args.no_graph:
-        with torch.cuda.stream(cs):
-            ctx.step(in_ctx, in_dr, target_ids=out_tg, stream=cs)
-            ctx.accept(in_dr, out_tg, committed=out_com, accept_len=out_alen, stream=cs)
-        cs.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cs):
-            ctx.step(in_ctx, in_dr, target_ids=out_tg, stream=cs)
-            ctx.accept(in_dr, out_tg, committed=out_com, accept_len=out_alen, stream=cs)
-    stream.wait_stream(cs)
-
-    def run_step(i):
-        if graph is not None:
-            in_ctx.copy_(d_ctx[i], non_blocking=True)
-            in_dr.copy_(d_dr[i], non_blocking=True)
-            graph.replay()
-            d_com[i].copy_(out_com, non_blocking=True)
-            d_alen[i].copy_(out_alen, non_blocking=True)
-        else:
-            ctx.step(d_ctx[i], d_dr[i], target_ids=d_tg[i])
-            ctx.accept(d_dr[i], d_tg[i], committed=d_com[i], accept_len=d_alen[i])
-
-    for i in range(args.warmup):
-        run_step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0 = time.perf_counter()
-    ev0.record(stream)
-    for i in range(args.warmup, total):
-        run_step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    w1 = time.perf_counter()
-    if dist:
-        dist.barrier()
-    time.sleep(0.2)
-    clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    clk = clocks.summary(w0, w1)
+    ms, got_com, got_alen, clk = timed_plan(ctx, plan, Bq, Kq, args.warmup, args.steps, dev,
+                                            dist, clocks)
 
     if args.profile and args.draft_head:
         line = run_decode_iteration(args, ctx, cfg, w_host, dev, Bq, Kq, stream)
@@ -325,72 +437,59 @@ def run_ours(args, rank, world, local):
         return
 
     # every timed step committed exactly what the planned trajectory says
-    got_com = d_com[args.warmup:].cpu().numpy()
-    got_alen = d_alen[args.warmup:].cpu().numpy()
-    mism = int(np.sum(np.any(got_com != plan_com[args.warmup:], axis=2)) +
-               np.sum(got_alen != plan_alen[args.warmup:]))
+    mism = int(np.sum(np.any(got_com != plan.com[args.warmup:], axis=2)) +
+               np.sum(got_alen != plan.alen[args.warmup:]))
     status = ctx.sync_status()
-    tokens = float(counted[args.warmup:].sum())
+    tokens = float(plan.counted[args.warmup:].sum())
 
     # end to end: the same steps through the host-buffer entry point
-    h_ctx = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
-    h_dr = torch.empty((Bq, Kq), dtype=torch.int32, pin_memory=True).numpy()
-    h_com = torch.empty((Bq, Kq + 1), dtype=torch.int32, pin_memory=True).numpy()
-    h_alen = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
-    etraj = Trajectory(g, rank, B=Bq, K=Kq)
-    cur = torch.cuda.current_stream()
-    pre = [etraj.drafts()]
-    for i in range(args.warmup):
-        c, d = pre[-1]
-        h_ctx[:], h_dr[:] = c, d
-        ctx.decode_host(h_ctx, h_dr, h_com, h_alen, stream=cur)
-        etraj.advance(h_com, h_alen)
-        pre.append(etraj.drafts())
-    e_tokens = 0
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0 = time.perf_counter()
-    c, d = pre[-1]
-    for i in range(args.steps):
-        h_ctx[:], h_dr[:] = c, d
-        ctx.decode_host(h_ctx, h_dr, h_com, h_alen, stream=cur)
-        e_tokens += etraj.advance(h_com, h_alen)
-        c, d = etraj.drafts()
-    e1 = time.perf_counter()
-    e_s = e1 - e0
+    e_tokens, e_s = run_e2e(ctx, g, rank, Bq, Kq, args, dist)
 
-    # roofline of the dominant kernel (the expert FFN): CUDA events around
-    # each of its launches over the same steps, probes give the touched experts
-    peak_gbs, peak_tf, peak_kind = measured_peaks()
+    # roofline of the dominant kernel (the expert FFN), weights-only bytes:
+    # in-graph launch times from the launch timestamps, and the
+    # event-bracketed (serialised) launch times beside them
+    T = Bq * (Kq + 1)
+    routing = probe_pass(ctx, cfg, plan, Bq, Kq, args.warmup, args.steps, dev)
+    ffn_bytes = [expert_weight_bytes(idx[l], cfg) for idx in routing for l in range(cfg.n_layers)]
+    st = in_graph_stamps(ctx, cfg, plan, Bq, Kq, args.warmup, args.steps, dev)
+    L = cfg.n_layers
+    ffn_win = (st[:, 1:2 * L:2, 2] - st[:, 1:2 * L:2, 1]) * 1e-6      # ms, [steps, L]
+    ffn_start = (st[:, 1:2 * L:2, 2] - st[:, 1:2 * L:2, 0]) * 1e-6
+    layer_period = np.diff(np.concatenate([np.zeros((st.shape[0], 1)), st[:, 1:2 * L:2, 2]],
+                                          axis=1), axis=1) * 1e-6
+    lm_win = (st[:, 2 * L, 2] - st[:, 2 * L, 1]) * 1e-6
+    route_win = (st[:, 0:2 * L:2, 2] - st[:, 0:2 * L:2, 1]) * 1e-6
+    ffn_ms_graph = float(np.mean(ffn_win))
     ctx.set_timing(True)
     ctx.get_timing(reset=True)
-    alg_bytes = 0.0
-    probe, pt = BND.make_probe(cfg.n_layers, Bq * (Kq + 1), cfg, topk=True, hidden=False,
-                               device=dev)
+    d_ctx = torch.from_numpy(plan.ctx).to(dev)
+    d_dr = torch.from_numpy(plan.dr).to(dev)
     for i in range(args.warmup, total):
-        ctx.step(d_ctx[i], d_dr[i], target_ids=d_tg[i], probe=probe)
-        ctx.accept(d_dr[i], d_tg[i], committed=d_com[i], accept_len=d_alen[i])
-        idx = pt["topk_idx"].cpu().numpy()
-        for l in range(cfg.n_layers):
-            alg_bytes += algorithmic_ffn_bytes(idx[l], cfg)
+        tg = ctx.step(d_ctx[i], d_dr[i])
+        ctx.accept(d_dr[i], tg)
     fam_ms, fam_n = ctx.get_timing(reset=True)
     ctx.set_timing(False)
-    ffn_launch_ms = fam_ms[0] / max(1, fam_n[0])
-    ffn_bytes = alg_bytes / max(1, fam_n[0])
-    achieved = ffn_bytes / (ffn_launch_ms * 1e-3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "ffn_traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get("bytes_per_launch")
+    ffn_ms_events = fam_ms[0] / max(1, fam_n[0])
+    mean_ffn_bytes = float(np.mean(ffn_bytes))
+    achieved = mean_ffn_bytes / (ffn_ms_graph * 1e-3) / 1e9
+    traffic, traffic_note = stored_traffic()
+    flops = step_flops(cfg, T)
+    sbytes = float(np.mean([step_bytes(idx, cfg, T) for idx in routing]))
+
+    # the other workloads, measured in the same run
+    configs = {
+        "single_layer_t4": run_single_layer(ctx, cfg, dev, peaks),
+        "zipf_b256_k3_p0.576": run_zipf(w_host, rank, args, dev, peaks),
+        "sweep": run_sweep(ctx, cfg, g, rank, dev, peaks),
+    }
 
     if dist:
         ms, e_s, tokens, e_tokens = whole_job(ms, e_s, tokens, e_tokens, dev)
     value = tokens / (ms / 1e3)
+    ms_step = ms / args.steps
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform start ids, drafts right w.p. 0.75)",
         "config": {"workload": WORKLOAD, "layers": cfg.n_layers, "hidden": cfg.hidden,
@@ -399,32 +498,205 @@ def run_ours(args, rank, world, local):
                    "drafts": Kq, "p_match": P_MATCH, "page_tokens": PAGE_TOKENS,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (5.8 GB of weights per step)",
-                   "cuda_graph": graph is not None},
+                   "cuda_graph": True},
         "e2e": {"value": round(e_tokens / e_s, 1), "unit": UNIT,
                 "h2d_bytes_per_step": Bq * 4 + Bq * Kq * 4,
                 "d2h_bytes_per_step": Bq * (Kq + 1) * 4 + Bq * 4},
         "gpu_launches": int(args.steps * (2 * cfg.n_layers + 3)),
         "roofline": {"kernel": "expert FFN (gate/up + SwiGLU + down + combine)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
-                     "frac": round(achieved / peak_gbs, 4), "peak_source": peak_kind,
-                     "traffic": traffic, "launch_ms": round(ffn_launch_ms, 5),
-                     "alg_bytes_per_launch": round(ffn_bytes)},
+                     "achieved": round(achieved, 1), "peak": peaks[0], "unit": "GB/s",
+                     "frac": round(achieved / peaks[0], 4), "peak_source": peaks[3],
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "alg_bytes_per_launch": round(mean_ffn_bytes),
+                     "alg_bytes": "touched experts' gate, up and down weights, once",
+                     "launch_ms": round(ffn_ms_graph, 5),
+                     "launch_ms_source": "in-graph launch timestamps: last CTA end minus the "
+                                         "return of the wait for the routing kernel",
+                     "launch_ms_from_cta_start": round(float(np.mean(ffn_start)), 5),
+                     "launch_ms_events": round(ffn_ms_events, 5),
+                     "tensor": dict(scope="whole step, selected-expert flops",
+                                    flops_per_step=round(flops),
+                                    **{k: v for k, v in fractions(sbytes, flops, ms_step,
+                                                                  peaks).items()
+                                       if k.startswith("tensor")},
+                                    peak_tflops=peaks[2], peak_kind="bf16 sustained")},
+        "step": dict(alg_bytes_per_step=round(sbytes), **fractions(sbytes, flops, ms_step, peaks)),
+        "in_graph_ms": {"ffn_per_layer": round(ffn_ms_graph, 5),
+                        "layer_period": round(float(np.mean(layer_period[:, 1:])), 5),
+                        "routing_per_layer": round(float(np.mean(route_win)), 5),
+                        "lm_head": round(float(np.mean(lm_win)), 5)},
+        "configs": configs,
         "clocks": clk,
         "committed_per_step": round(tokens / args.steps / world, 3),
         "check": {"mismatched_rows": mism, "status": status},
-        "kernel_ms_per_step": {"expert_ffn": round(fam_ms[0] / args.steps, 4),
-                               "lm_head": round(fam_ms[2] / args.steps, 4),
-                               "routing_and_norm": round(fam_ms[3] / args.steps, 4),
-                               "note": "serialised by the per-launch events"},
         "setup_s": round(setup_s, 1),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, w_host, plan_ctx, plan_dr, counted, args.cpu_seconds)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(cfg, w_host, plan, g,
+                                                            args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     ctx.close()
     if dist:
         dist.destroy_process_group()
+
+
+def stored_traffic():
+    """ncu's DRAM bytes per expert-FFN launch, if they were taken on the
+    kernels that run now (else None, with the reason)."""
+    prof = os.path.join(ROOT, "profiles", "ffn_traffic.json")
+    if not os.path.exists(prof):
+        return None, "no ncu capture stored"
+    with open(prof) as f:
+        d = json.load(f)
+    if d.get("kernel_digest") != kernel_digest():
+        return None, "kernel sources changed since the ncu capture"
+    return d.get("bytes_per_launch"), d.get("note", "")
+
+
+def run_e2e(ctx, g, rank, Bq, Kq, args, dist):
+    """The timed steps through moe_verify_decode_host on pinned host buffers,
+    with the host building each next step's drafts."""
+    import torch
+    h_ctx = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
+    h_dr = torch.empty((Bq, Kq), dtype=torch.int32, pin_memory=True).numpy()
+    h_com = torch.empty((Bq, Kq + 1), dtype=torch.int32, pin_memory=True).numpy()
+    h_alen = torch.empty((Bq,), dtype=torch.int32, pin_memory=True).numpy()
+    etraj = Trajectory(g, rank, B=Bq, K=Kq)
+    cur = torch.cuda.current_stream()
+    c, d = etraj.drafts()
+    for i in range(args.warmup):
+        h_ctx[:], h_dr[:] = c, d
+        ctx.decode_host(h_ctx, h_dr, h_com, h_alen, stream=cur)
+        etraj.advance(h_com, h_alen)
+        c, d = etraj.drafts()
+    e_tokens = 0
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = time.perf_counter()
+    for i in range(args.steps):
+        h_ctx[:], h_dr[:] = c, d
+        ctx.decode_host(h_ctx, h_dr, h_com, h_alen, stream=cur)
+        e_tokens += etraj.advance(h_com, h_alen)
+        c, d = etraj.drafts()
+    e1 = time.perf_counter()
+    return e_tokens, e1 - e0
+
+
+def run_single_layer(ctx, cfg, dev, peaks, reps=20):
+    """One decoder block on T = 4 bf16 hidden rows through moe_verify_layer,
+    cycling over the 12 distinct layers of the stack (12 x ~160 MB, far more
+    than L2, so no repeat is served from L2): device time per call and the
+    touched weights' bytes per second."""
+    import torch
+    from moe_speculative_decoding_router_gb300 import binding as BND
+    T, L = 4, cfg.n_layers
+    hin = S.hidden_input(T, cfg.hidden, seed=S.SEED_HIDDEN)
+    h_in = torch.from_numpy(hin.view(np.int16)).to(dev).view(torch.bfloat16)
+    h_out = torch.empty_like(h_in)
+    probe, pt = BND.make_probe(1, T, cfg, topk=True, hidden=False, device=dev)
+    nbytes = []
+    for l in range(L):
+        ctx.layer(l, h_in, h_out=h_out, probe=probe)
+        idx = pt["topk_idx"].cpu().numpy()[0]
+        nbytes.append(expert_weight_bytes(idx, cfg) + cfg.n_experts * cfg.hidden * 2 +
+                      cfg.hidden * 2 + 2 * T * cfg.hidden * 2)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for l in range(L):
+            ctx.layer(l, h_in, h_out=h_out, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for l in range(L):
+            ctx.layer(l, h_in, h_out=h_out, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms_call = e0.elapsed_time(e1) / (reps * L)
+    b = float(np.mean(nbytes))
+    gbs = b / (ms_call * 1e-3) / 1e9
+    return {"tokens": T, "layers_cycled": L, "calls": reps * L, "ms_per_call": round(ms_call, 5),
+            "alg_bytes_per_call": round(b), "hbm_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks[0], 4),
+            "entry_point": "moe_verify_layer (routing + expert FFN + bf16 output), graph-replayed"}
+
+
+def run_zipf(w_host, rank, args, dev, peaks):
+    """Batch 256 x (1 + 3 drafts) on the stack with the Zipf(s=1.2) router
+    bias, drafts right with probability 0.576: committed tokens/s, time per
+    step and both roofline fractions (touched experts' bytes; selected-expert
+    flops against the sustained bf16 peak)."""
+    import torch
+    from moe_speculative_decoding_router_gb300 import binding as BND
+    cfg = S.FULL_ZIPF
+    B, K, p = 256, 3, 0.576
+    w = dict(w_host)
+    w["router_bias"] = S.router_bias(cfg)
+    ctx = BND.MoeVerify(cfg, BND.weights_to_device(w, device=dev), max_batch=B, max_k=K)
+    torch.cuda.empty_cache()
+    try:
+        g = greedy_table(ctx, cfg.vocab, K, dev, B)
+        total = args.warmup + args.steps
+        plan = Plan(g, rank, B, K, p, total)
+        ms, com, alen, _ = timed_plan(ctx, plan, B, K, args.warmup, args.steps, dev)
+        mism = int(np.sum(np.any(com != plan.com[args.warmup:], axis=2)) +
+                   np.sum(alen != plan.alen[args.warmup:]))
+        routing = probe_pass(ctx, cfg, plan, B, K, args.warmup, min(args.steps, 5), dev)
+        T = B * (K + 1)
+        sbytes = float(np.mean([step_bytes(idx, cfg, T) for idx in routing]))
+        touched = float(np.mean([[len(np.unique(idx[l])) for l in range(cfg.n_layers)]
+                                 for idx in routing]))
+        top_share = float(np.mean([np.bincount(idx[l].reshape(-1), minlength=cfg.n_experts).max()
+                                   / T for idx in routing for l in range(cfg.n_layers)]))
+        ms_step = ms / args.steps
+        fr = fractions(sbytes, step_flops(cfg, T), ms_step, peaks)
+        status = ctx.sync_status()
+    finally:
+        ctx.close()
+    tokens = float(plan.counted[args.warmup:].sum())
+    out = {"batch": B, "drafts": K, "p_match": p, "steps": args.steps,
+           "value": round(tokens / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms_step, 4),
+           "committed_per_step": round(tokens / args.steps, 2),
+           "alg_bytes_per_step": round(sbytes), "flops_per_step": round(step_flops(cfg, T)),
+           "touched_routed_experts_per_layer": round(touched, 1),
+           "busiest_expert_token_share": round(top_share, 3)}
+    out.update(fr)
+    out["binding"] = "tensor" if fr["tensor_frac"] > fr["hbm_frac"] else "hbm"
+    out["check"] = {"mismatched_rows": mism, "status": status}
+    return out
+
+
+def run_sweep(ctx, cfg, g, rank, dev, peaks, warmup=3, steps=10):
+    """B in {1, 8, 32, 128} x K in {1, 2, 3} x p in {0.576, 0.75}: committed
+    tokens/s, time per step and roofline fractions per point.  Each entry is
+    [B, K, p, ms_per_step, tokens_per_s, hbm_frac, tensor_frac]."""
+    out, mism = [], 0
+    for B in (1, 8, 32, 128):
+        for K in (1, 2, 3):
+            for p in (0.576, 0.75):
+                plan = Plan(g, rank, B, K, p, warmup + steps)
+                ms, com, alen, _ = timed_plan(ctx, plan, B, K, warmup, steps, dev)
+                mism += int(np.sum(np.any(com != plan.com[warmup:], axis=2)) +
+                            np.sum(alen != plan.alen[warmup:]))
+                T = B * (K + 1)
+                routing = probe_pass(ctx, cfg, plan, B, K, warmup, 2, dev)
+                sbytes = float(np.mean([step_bytes(idx, cfg, T) for idx in routing]))
+                fr = fractions(sbytes, step_flops(cfg, T), ms / steps, peaks)
+                tok = float(plan.counted[warmup:].sum())
+                out.append([B, K, p, round(ms / steps, 4), round(tok / (ms / 1e3), 1),
+                            fr["hbm_frac"], fr["tensor_frac"]])
+    return {"columns": ["batch", "drafts", "p_match", "ms_per_step", "tokens_per_s", "hbm_frac",
+                        "tensor_frac"], "steps_per_point": steps, "points": out,
+            "check": {"mismatched_rows": mism}}
 
 
 def whole_job(ms, e_s, tokens, e_tokens, device):
@@ -518,28 +790,38 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, w_host, plan_ctx, plan_dr, counted, budget_s=20.0):
+def cpu_baseline(cfg, w_host, plan, g, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the workload's verify
-    tokens (one token per thread at a time), scaled to committed tokens/s."""
+    tokens (one token per thread at a time), scaled to committed tokens/s.
+    Its targets are also compared with the library's greedy table, which the
+    timed steps' commits were checked against: returns (baseline, parity)."""
     import oracle as O
     orc = O.Oracle(cfg, w_host)
-    toks = np.concatenate([plan_ctx[..., None], plan_dr], axis=2).reshape(-1)
+    toks = np.concatenate([plan.ctx[..., None], plan.dr], axis=2).reshape(-1)
     cores = _cores()
     import concurrent.futures as fut
     done = 0
+    res = []
     t0 = time.perf_counter()
     with fut.ThreadPoolExecutor(max_workers=cores) as ex:
         while time.perf_counter() - t0 < budget_s and done < len(toks):
             batch = toks[done:done + cores]
-            list(ex.map(orc.target, batch))
+            res += list(ex.map(orc.forward_token, batch))
             done += len(batch)
     dt = time.perf_counter() - t0
-    per_verify_token = float(counted.sum()) / (len(counted) * B_SEQ * (K_DRAFT + 1))
+    per_verify_token = float(plan.counted.sum()) / (len(plan.counted) * B_SEQ * (K_DRAFT + 1))
     value = done / dt * per_verify_token
-    return {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+    base = {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done} verify tokens of the workload's first steps in {dt:.1f} s "
                       f"(fp64, one token per thread), scaled by {per_verify_token:.3f} committed "
                       f"tokens per verify token"}
+    diffs = [(int(x), r["logit_gap"]) for x, r in zip(toks[:done], res)
+             if r["target"] != int(g[int(x)])]
+    parity = {"verify_tokens": done, "target_diffs": len(diffs),
+              "diff_logit_gaps": [round(gap, 5) for _, gap in diffs],
+              "what": "free-running fp64 oracle targets vs the library's targets for the same "
+                      "tokens of the timed trajectory (a difference needs a small oracle gap)"}
+    return base, parity
 
 
 # -------------------------------------------------------- reference arm

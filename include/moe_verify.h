@@ -134,7 +134,10 @@ MOE_VERIFY_API int moe_verify_init(const moe_verify_config* config, const moe_ve
  *   target_ids   [B, K+1] int32, written
  *   probe        NULL or diagnostics (see moe_verify_probe)
  * 1 <= B <= max_batch, 0 <= K <= max_k.  A verify token outside [0, V) sets
- * the sticky MOE_VERIFY_ERR_ID_RANGE flag and its target is -1. */
+ * the sticky MOE_VERIFY_ERR_ID_RANGE flag and its target is -1.  If a bounded
+ * wait of the lm_head launch runs out, every target of the step is -1 (its
+ * argmax is incomplete) and the sticky MOE_VERIFY_ERR_TIMEOUT flag is set; a
+ * wait of an earlier kernel of the step that runs out sets that flag only. */
 MOE_VERIFY_API int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
                     int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
                     void* cuda_stream);
@@ -261,6 +264,29 @@ MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
 MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] host*/, int64_t* n /*[4] host*/,
                           int32_t reset);
 
+/* Diagnostic (no counterpart in the method): the number of CTAs that later
+ * calls give the persistent kernels (the expert FFN and the lm_head); 0, the
+ * initial value, means one per SM.  0 <= ctas <= 8 x the SM count.  Results do
+ * not depend on it, bit for bit: fewer CTAs than SMs is what a context that
+ * holds only part of the GPU runs with, and more CTAs than fit on the GPU at
+ * once shows that no CTA waits for one that has not started (every expert-FFN
+ * work item is claimed in order by a running CTA).  Host-buffer decode graphs
+ * already captured keep the grid they were captured with. */
+MOE_VERIFY_API int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas);
+
+/* Profiling (no counterpart in the method): launch timestamps inside later
+ * moe_verify_step calls, for timing kernels in a graph-replayed step without
+ * breaking the overlap of consecutive launches.  stamps is a device array of
+ * (2 L + 1) x 4 uint64 (8-byte aligned, caller-owned), or NULL to stop.
+ * Launch j of a step (routing of layer l: j = 2l; expert FFN of layer l:
+ * j = 2l + 1; lm_head: j = 2L) updates stamps[4j + 0] = min over its CTAs of
+ * the start time, stamps[4j + 1] = max of the time its wait for the
+ * preceding launch returned, stamps[4j + 2] = max of the end time (global
+ * timer, ns); stamps[4j + 3] is unused.  The caller sets stamps[4j] to
+ * UINT64_MAX and the others to 0 before each step it wants to read.  The
+ * pointer is recorded in graphs captured while it is set. */
+MOE_VERIFY_API int moe_verify_set_stamps(moe_verify_ctx* ctx, uint64_t* stamps);
+
 /* ----------------------------------------------------------------------
  * Greedy head without allocation.  The pages have no counterpart of this
  * entry point: it exists for callers that cannot allocate device memory,
@@ -274,8 +300,10 @@ MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] h
  * with final_norm g [d] and lm_head W_lm [V, d] as bf16 device arrays
  * (h and lm_head 16-byte aligned), the same kernels as moe_verify_step's
  * last stage.
- * target_ids [T] int32 (device) is written; -1 marks a row whose device-side
- * work gave up after a bounded wait.
+ * target_ids [T] int32 (device) is written.  If any part of the call's
+ * lm_head gives up a bounded wait, every row of that call is -1: this entry
+ * point has no context and no sticky status, so the -1 rows are the report.
+ * The next call starts afresh (the call clears its status before it runs).
  *
  * Its scratch (normalised rows, argmax keys, a completion counter) is a
  * fixed array of about 1 MB in the library's device memory; every GPU that

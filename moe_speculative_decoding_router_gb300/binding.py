@@ -30,7 +30,8 @@ EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_veri
             "moe_verify_decode_host", "moe_verify_sync_status", "moe_verify_destroy",
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
             "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc",
-            "moe_verify_check_bounded_wait", "moe_verify_draft", "moe_verify_draft_inputs")
+            "moe_verify_check_bounded_wait", "moe_verify_draft", "moe_verify_draft_inputs",
+            "moe_verify_set_grid", "moe_verify_set_stamps")
 
 
 class Config(ctypes.Structure):
@@ -100,6 +101,10 @@ def load(build_if_missing: bool = True):
     L.moe_verify_draft_inputs.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
     L.moe_verify_check_bounded_wait.restype = _i32
     L.moe_verify_check_bounded_wait.argtypes = [ctypes.c_int64, _P, _P]
+    L.moe_verify_set_grid.restype = _i32
+    L.moe_verify_set_grid.argtypes = [_P, _i32]
+    L.moe_verify_set_stamps.restype = _i32
+    L.moe_verify_set_stamps.argtypes = [_P, _P]
     L.moe_verify_greedy_head_noalloc.restype = _i32
     L.moe_verify_greedy_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P,
                                                  _P]
@@ -346,6 +351,22 @@ class MoeVerify:
         rc = self.lib.moe_verify_set_timing(self.handle, 1 if enable else 0)
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_set_timing")
+
+    def set_grid(self, ctas: int):
+        """moe_verify_set_grid: CTAs of the persistent kernels (0: one per SM)."""
+        rc = self.lib.moe_verify_set_grid(self.handle, int(ctas))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_set_grid")
+
+    def set_stamps(self, stamps):
+        """moe_verify_set_stamps: a device int64 tensor [2L + 1, 4] (viewed as
+        uint64 by the library), or None to stop."""
+        import torch
+        if stamps is not None:
+            _check_dev(stamps, torch.int64, "stamps", (2 * self.cfg.n_layers + 1, 4))
+        rc = self.lib.moe_verify_set_stamps(self.handle, _ptr(stamps) if stamps is not None else None)
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_set_stamps")
 
     def get_timing(self, reset: bool = True):
         ms = (ctypes.c_double * 4)()

@@ -49,7 +49,10 @@ struct moe_verify_ctx {
   };
   std::vector<DecodeGraph> decode_graphs;
   cudaStream_t capture_stream = nullptr;
+  // CTAs of the persistent kernels (expert FFN, lm_head); 0: one per SM
+  int grid_ctas = 0;
   // profiling
+  unsigned long long* stamps = nullptr;  // caller-owned [2L + 1][kStampSlots] or nullptr
   bool timing = false;
   std::vector<TimingPair> pending;
   std::vector<cudaEvent_t> event_pool;
@@ -168,16 +171,19 @@ int dalloc(moe_verify_ctx* c, T** p, uint64_t bytes) {
   return MOE_VERIFY_OK;
 }
 
+// The driver's tensor-map encoder, looked up once (a function-local static's
+// initialisation is thread safe).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -286,13 +292,31 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
 // Expert counters alternate between two buffers by position in the launch
 // sequence (parity): routing kernel n claims rows on buffer n % 2 and clears
 // buffer (n + 1) % 2, whose users are complete by then; the final kernel
-// clears the buffer of the last layer.
+// clears the buffer of the last layer.  The expert FFN's item counters
+// alternate the same way: expert-FFN launch n claims on counter n % 2 from
+// its first instruction, routing kernel n clears counter (n + 1) % 2 (last
+// used by launch n - 1, complete by then, and next used by launch n + 1,
+// which starts only after routing kernel n + 1 is past its wait), and the
+// final kernel clears the last layer's.
+int32_t* item_counter(moe_verify_ctx* c, int parity) {
+  return reinterpret_cast<int32_t*>(c->done_ffn + 1 + parity);
+}
+
+int persistent_grid(const moe_verify_ctx* c) { return c->grid_ctas > 0 ? c->grid_ctas : c->num_sms; }
+
+// Timer slots of launch `slot` of a step (routing of layer l: 2l, expert FFN
+// of layer l: 2l + 1, lm_head: 2L), or nullptr when stamps are off or the
+// launch is not part of a step (slot < 0).
+unsigned long long* stamp_slot(const moe_verify_ctx* c, int slot) {
+  return (c->stamps && slot >= 0) ? c->stamps + (size_t)slot * mv::kStampSlots : nullptr;
+}
+
 // next_head: the lm_head follows this layer (its first items are prefetched
 // into L2 at the end of the expert FFN, as the next layer's are otherwise).
 int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh,
               const int32_t* context_ids, const int32_t* draft_ids, int B, int K,
               const void* h_in, const moe_verify_probe* probe, int probe_layer, cudaStream_t s,
-              bool pdl, bool next_head) {
+              bool pdl, bool next_head, bool stamped = false) {
   const int T = sh.T;
   mv::RouteParams rp = {};
   rp.T = T;
@@ -328,11 +352,12 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   rp.cnt_other = c->cnt + (size_t)(1 - parity) * c->E;
   rp.dep_clear = c->dep;
   rp.n_dep_clear = c->chunks_cap;
-  rp.next_item_clear = reinterpret_cast<int32_t*>(c->done_ffn + 1);
+  rp.next_item_clear = item_counter(c, 1 - parity);
   rp.xperm = c->xperm;
   rp.perm_token = c->perm_token;
   rp.perm_slot = c->perm_slot;
   rp.perm_w = c->perm_w;
+  rp.stamps = stamp_slot(c, stamped ? 2 * l : -1);
   {
     Timed tm(c, 3, s);
     CK(mv::launch_route(c->map_wr, rp, sh.grid_route, sh.route_smem, s, pdl));
@@ -361,7 +386,7 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   fp.d = c->d;
   fp.kS = c->kS;
   fp.status = c->status;
-  fp.next_item = reinterpret_cast<int32_t*>(c->done_ffn + 1);
+  fp.next_item = item_counter(c, parity);
   // the guessed first items are right when every routed expert holds one
   // chunk.  Loading them early costs little when a guess misses (the loads
   // overlap the routing), so it is on from one expected row per expert; the
@@ -382,9 +407,11 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.pf_div = 1;
     fp.pf_limit = c->nE * c->mt_gu;
   }
+  fp.stamps = stamp_slot(c, stamped ? 2 * l + 1 : -1);
   {
     Timed tm(c, 0, s);
-    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, fp, c->num_sms, s, pdl));
+    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, fp, persistent_grid(c), s,
+                      pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -573,7 +600,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
 // (parity `last_parity`).  probe_hidden [T, d] and logits [T, V] may be NULL.
 static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int last_parity,
                         int32_t* target_ids, float* probe_hidden, float* logits, cudaStream_t s,
-                        bool pdl) {
+                        bool pdl, bool stamped = false) {
   mv::FinalParams fp = {};
   fp.T = T;
   fp.d = ctx->d;
@@ -588,6 +615,7 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   fp.keys = ctx->keys;
   fp.cnt_clear = ctx->cnt + (size_t)last_parity * ctx->E;
   fp.n_cnt_clear = ctx->E;
+  fp.item_clear = item_counter(ctx, last_parity);
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, pdl));
@@ -608,9 +636,12 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   gp.targets = target_ids;
   gp.bad = ctx->bad;
   gp.done = ctx->done_lm;
+  gp.aborted = ctx->done_lm + 1;
+  gp.stamps = stamp_slot(ctx, stamped ? 2 * ctx->L : -1);
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, ctx->num_sms, s, pdl));
+    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, persistent_grid(ctx), s,
+                         pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -624,12 +655,12 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
     int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
-                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1);
+                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1, true);
     if (rc != MOE_VERIFY_OK) return rc;
   }
   float* ph = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
   return enqueue_head(ctx, T, sh, (ctx->L - 1) & 1, target_ids, ph, probe ? probe->logits : nullptr,
-                      s, pdl);
+                      s, pdl, true);
 }
 
 int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
@@ -686,6 +717,7 @@ int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32
   fp.keys = ctx->keys;
   fp.cnt_clear = ctx->cnt;
   fp.n_cnt_clear = ctx->E;
+  fp.item_clear = item_counter(ctx, 0);
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, true));
@@ -835,6 +867,19 @@ void moe_verify_destroy(moe_verify_ctx* ctx) {
   if (ctx->capture_stream) cudaStreamDestroy(ctx->capture_stream);
   free_all(ctx);
   delete ctx;
+}
+
+int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas) {
+  if (!ctx || ctas < 0 || ctas > 8 * ctx->num_sms) return MOE_VERIFY_ERR_ARG;
+  ctx->grid_ctas = ctas;
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_set_stamps(moe_verify_ctx* ctx, uint64_t* stamps) {
+  if (!ctx) return MOE_VERIFY_ERR_ARG;
+  if (stamps && (reinterpret_cast<uintptr_t>(stamps) & 7u) != 0) return MOE_VERIFY_ERR_ARG;
+  ctx->stamps = reinterpret_cast<unsigned long long*>(stamps);
+  return MOE_VERIFY_OK;
 }
 
 int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable) {

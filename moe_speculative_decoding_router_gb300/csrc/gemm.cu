@@ -5,12 +5,13 @@
 //            epilogue a = bf16(silu(g) * u)                  (SwiGLU)
 //   down     [128 rows of one expert's down projection] x [the same rows' a]
 //            epilogue y[token, slot] = p * (a W_d^T)         (weighted combine)
-// All gate/up items come first, then all down items.  CTA c starts with item
-// c; later items are claimed in order from a global counter (one claim ahead
-// of use), so CTAs that stream faster take more items and all finish within
-// about one item of each other.  A down item waits (bounded) until both
-// SwiGLU halves of every gate/up tile of its chunk of rows are written; the
-// items it waits for were claimed earlier and have no waits of their own.
+// All gate/up items come first, then all down items.  Items are claimed in
+// order from a global counter (the first as the CTA starts, the next one
+// claim ahead of use), so CTAs that stream faster take more items and all
+// finish within about one item of each other.  A down item waits (bounded)
+// until both SwiGLU halves of every gate/up tile of its chunk of rows are
+// written; the items it waits for were claimed earlier, by CTAs that are
+// running, and have no waits of their own.
 // Once a CTA has issued its last load it pulls into L2 the weight item its
 // index starts with in the next kernel (next layer, or the lm_head).
 // lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
@@ -265,15 +266,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   L.igu = L.cb + nE + 1;
   L.idn = L.igu + nE + 1;
 
-  // Speculation: when every expert holds one chunk, the first item of CTA c
-  // is gate/up tile c of this layer.  Its weight tiles do not depend on the
-  // routing, so they start streaming before waiting for it.  The host turns
+  // Every item is claimed from one counter in increasing order, the CTA's
+  // first included: its ticket, taken as the CTA starts (before the wait, the
+  // counter was cleared two launches back).  So any gate/up item that a down
+  // item waits for belongs to a CTA that is already running, and the kernel
+  // makes progress whatever number of its CTAs the GPU runs at once.
+  // Speculation: when every expert holds one chunk, item c is gate/up tile c
+  // of this layer, so the weight tiles of the ticket's item do not depend on
+  // the routing and start streaming before waiting for it.  The host turns
   // this on only when every routed expert expects several rows (else most
   // guesses would miss and their loads would only take bandwidth).
-  const int guess_row = p.a_base_gu + blockIdx.x * 128;
-  const bool guess_valid = p.spec && (int)blockIdx.x < nE * p.mt_gu;
-  const int pre = guess_valid ? min(p.stages, p.kb_gu) : 0;
+  int first = 0, guess_row = 0, pre = 0;
   if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
+    first = atomicAdd(p.next_item, 1);
+    guess_row = p.a_base_gu + first * 128;
+    pre = (p.spec && first < nE * p.mt_gu) ? min(p.stages, p.kb_gu) : 0;
     init_ctrl(C, p.stages, 2, 2);
     tma_prefetch_desc(&map_gu);
     tma_prefetch_desc(&map_x);
@@ -295,11 +303,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // and rows are read; dependents may start once this grid is past its wait.
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
   if (threadIdx.x == 0 && pre > 0) {
     // the speculated first item's activation rows (chunk 0 of expert
-    // blockIdx / mt_gu) load while the item lists are built
+    // first / mt_gu) load while the item lists are built
     const uint64_t pol_x = policy_evict_last();
-    const int row0 = (int)(blockIdx.x / p.mt_gu) * p.T;
+    const int row0 = (first / p.mt_gu) * p.T;
     mbar_arrive_expect_tx(C.spec_b, (uint32_t)(pre * p.nch * 128));
     for (int s = 0; s < pre; ++s)
       tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &map_x, C.spec_b, s * 64, row0, pol_x);
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      int i = (int)blockIdx.x < n_items ? (int)blockIdx.x : -1, kb = 0;
+      int i = first < n_items ? first : -1, kb = 0;
       FItem it = {};
       // announce item `item` to the MMA issuer and the epilogue, and claim
       // the item after it (the claim's result is first used when `item` is
@@ -379,17 +388,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         return true;
       };
-      auto next_item = [&]() -> int {
-        const int c = next_raw + (int)gridDim.x;
-        return c < n_items ? c : -1;
-      };
+      auto next_item = [&]() -> int { return next_raw < n_items ? next_raw : -1; };
       bool ok = true;
       // the speculative tiles have landed (kept on a hit, overwritten otherwise)
       if (pre > 0) ok = mbar_wait(C.spec, 0, C.abort_flag, p.status) &&
                         mbar_wait(C.spec_b, 0, C.abort_flag, p.status);
       ok = ok && start_item(i);
       const bool hit = ok && pre > 0 && i >= 0 && !it.down && it.a_row == guess_row &&
-                       it.row0 == (int)(blockIdx.x / p.mt_gu) * p.T;
+                       it.row0 == (first / p.mt_gu) * p.T;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -450,9 +456,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (ok && (int)blockIdx.x < p.pf_limit) {
-        // every load of this CTA is issued: pull the next kernel's first
-        // weight item for this CTA index into L2 while HBM has room (the
-        // last items of other CTAs and the routing in between)
+        // every load of this CTA is issued: pull into L2 the next kernel's
+        // weight item numbered like this CTA (the first items of the next
+        // kernel's CTAs together), while HBM has room (the last items of
+        // other CTAs and the routing in between)
         const int row = p.pf_base + (int)(blockIdx.x / p.pf_div) * 128;
         for (int k = 0; k < p.pf_kb; ++k) tma_prefetch_l2_2d(&map_pf, k * 64, row);
       }
@@ -572,7 +579,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
   // the counters this launch used are cleared by the next routing kernel
+}
+
+// End of an lm_head launch: the last CTA to finish turns the argmax keys into
+// token ids.  A row is -1 when its token was invalid, when no key reached it,
+// or when any CTA of this launch gave up a bounded wait (its tiles are then
+// missing from the argmax, so no row of the launch can be trusted).  The last
+// CTA resets the launch counters for the next launch.
+__device__ __forceinline__ void lm_finish(const GemmParams& p, bool cta_aborted, int* is_last) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (cta_aborted) atomicAdd(p.aborted, 1u);
+    __threadfence();
+    *is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*is_last) {
+    __threadfence();
+    const bool any_aborted = __ldcg(p.aborted) != 0u;
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+      const unsigned long long key = __ldcg(p.keys + t);
+      const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+      p.targets[t] = (any_aborted || __ldg(p.bad + t) || key == 0ull) ? -1 : id;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      *p.done = 0u;
+      *p.aborted = 0u;
+    }
+  }
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
 }
 
 // ------------------------------------ lm_head, vocabulary rows on M (any T)
@@ -606,6 +645,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool has_work = (int)blockIdx.x < n_items;
 
   if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
     init_ctrl(C, p.stages, 4, 1);
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
@@ -645,6 +685,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (p.stamps) stamp_max(p.stamps + 1);
     for (int s = 0; s < pre; ++s) {
       tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &mapB, &C.full[s], kb * 64,
                   it.b_row, pol_x);
@@ -685,6 +726,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
     if (has_work && warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
       int stage = 0, local = 0;
@@ -778,20 +820,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
-  // the last CTA turns the argmax keys into token ids
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (is_last) {
-    __threadfence();
-    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
-      const unsigned long long key = __ldcg(p.keys + t);
-      const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-      p.targets[t] = (__ldg(p.bad + t) || key == 0ull) ? -1 : id;
-    }
-    if (threadIdx.x == 0) *p.done = 0u;
-  }
+  lm_finish(p, *C.abort_flag != 0, &is_last);
 }
 
 // ------------------------------------------- lm_head, tokens on M (65..128)
@@ -835,6 +864,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool has_work = (int)blockIdx.x < n_items;
 
   if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
     init_ctrl(C, p.stages, 4, 1);
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_x);
@@ -874,6 +904,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (p.stamps) stamp_max(p.stamps + 1);
     for (int s = 0; s < pre; ++s) {
       tma_load_2d(stages + (size_t)s * stage_bytes, &map_x, &C.full[s], kb * 64, it.x_row, pol_x);
       if (++kb == p.kblocks) {
@@ -913,6 +944,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
     if (has_work && warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc = umma_idesc_bf16(128, 128);
@@ -1010,20 +1042,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
-  // the last CTA turns the argmax keys into token ids
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (is_last) {
-    __threadfence();
-    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
-      const unsigned long long key = __ldcg(p.keys + t);
-      const int id = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-      p.targets[t] = (__ldg(p.bad + t) || key == 0ull) ? -1 : id;
-    }
-    if (threadIdx.x == 0) *p.done = 0u;
-  }
+  lm_finish(p, *C.abort_flag != 0, &is_last);
 }
 
 template <typename Kern, typename... Args>

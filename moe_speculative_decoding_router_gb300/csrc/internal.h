@@ -8,6 +8,12 @@
 
 namespace mv {
 
+// Launch timestamps for profiling inside a graph-replayed step (global timer,
+// ns): slot[0] = earliest CTA start (atomicMin), slot[1] = latest return from
+// the wait for the preceding kernel (atomicMax), slot[2] = latest CTA end
+// (atomicMax).  The caller initialises slot[0] to ~0 and the others to 0.
+constexpr int kStampSlots = 4;
+
 // Bits of the device status word.
 constexpr uint32_t kErrIdRange = 1u;
 constexpr uint32_t kErrTimeout = 2u;
@@ -43,12 +49,14 @@ struct RouteParams {
   // expert-major rows: expert e owns rows [e*T, e*T + cnt[e])
   int32_t* cnt;                // [E] rows claimed per routed expert (zero on entry)
   // cleared after the wait (the kernels that used them are complete): the
-  // other parity's expert counters and the previous expert-FFN launch's
-  // dependency counters and item counter
+  // other parity's expert counters, the previous expert-FFN launch's
+  // dependency counters, and the other parity's item counter (the next
+  // expert-FFN launch claims from it, before its own wait)
   int32_t* cnt_other;          // [E]
   int32_t* dep_clear;          // [n_dep_clear]
   int n_dep_clear;
   int32_t* next_item_clear;
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
   __nv_bfloat16* xperm;        // [(E+S)*T, d] normalised inputs
   int32_t* perm_token;         // [(E+S)*T] token of each row
   int32_t* perm_slot;          // [(E+S)*T] its slot: routed rank, or k + s
@@ -73,12 +81,13 @@ struct FfnParams {
   float* y;                    // [T, kS, d]
   int d, kS;
   uint32_t* status;
-  int* next_item;              // items claimed past the first gridDim (zero on entry)
+  int* next_item;              // items claimed so far, every CTA's first included (zero on entry)
   // L2 prefetch of the next kernel's first weight item of this CTA index c,
   // issued once this CTA has no items left: rows pf_base + (c / pf_div) * 128
   // of the prefetch tensor map, pf_kb 64-column boxes, for c < pf_limit
   int pf_base, pf_div, pf_limit, pf_kb;
   int spec;                    // 1: load the guessed first item's tiles before the wait
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
 struct FinalParams {
@@ -93,6 +102,7 @@ struct FinalParams {
   unsigned long long* keys;    // [T] argmax keys, cleared in mode 0
   int32_t* cnt_clear;          // [n_cnt_clear] expert counters of the last layer, cleared
   int n_cnt_clear;
+  int32_t* item_clear;         // item counter of the last layer's expert FFN, cleared
 };
 
 // The lm_head GEMM with its argmax epilogue.
@@ -108,7 +118,9 @@ struct GemmParams {
   float* logits;               // [T, V] or nullptr
   int32_t* targets;            // [T]
   const int32_t* bad;          // [T]
-  unsigned int* done;
+  unsigned int* done;          // CTAs finished with this launch (the last one resets it)
+  unsigned int* aborted;       // CTAs of this launch whose bounded wait ran out (reset with done)
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
 struct AcceptParams {

@@ -28,7 +28,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kXfBytes = (size_t)kMaxTokens * kMaxHidden * 2;  // bf16 rows
 constexpr size_t kKeysOff = kXfBytes;
 constexpr size_t kBadOff = kKeysOff + (size_t)kMaxTokens * 8;
-constexpr size_t kDoneOff = kBadOff + (size_t)kMaxTokens * 4;
+constexpr size_t kDoneOff = kBadOff + (size_t)kMaxTokens * 4;  // [0] done, [1] aborted
 constexpr size_t kStatusOff = kDoneOff + 16;
 constexpr size_t kScratchBytes = kStatusOff + 16;
 
@@ -37,13 +37,27 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;  // guarded by g_setup_mu
 
-// Device address of g_scratch on the current device.  In host code the name
-// g_scratch is only a host-side stand-in, so the address is asked for once per
-// device, with that device current.
-int scratch_address(int dev, unsigned char** out) {
+// Device address of g_scratch on the current device, and the driver's
+// tensor-map encoder.  In host code the name g_scratch is only a host-side
+// stand-in, so the address is asked for once per device, with that device
+// current.
+int scratch_address(int dev, unsigned char** out, PFN_cuTensorMapEncodeTiled_v12000* encode) {
   if (dev < 0 || dev >= kMaxDevices) return MOE_VERIFY_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p) {
+      cudaGetLastError();
+      return MOE_VERIFY_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *encode = g_encode;
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
@@ -60,8 +74,8 @@ int scratch_address(int dev, unsigned char** out) {
 // with the sum of squares reduced in the same order as the verify step's
 // final RMSNorm (per thread over 4-float chunks c = tid, tid + 256, ..., then
 // per warp, then over the warps in order), so both give the same bits.  Also
-// clears the token's argmax key and invalid flag, and the completion counter:
-// they must start at zero.
+// clears what must start at zero: the token's argmax key and invalid flag, and
+// (block 0) the lm_head's completion and abort counters and the status word.
 __global__ void __launch_bounds__(256) noalloc_norm_kernel(const float* __restrict__ h,
                                                            const __nv_bfloat16* __restrict__ gain,
                                                            int T, int d, float eps,
@@ -73,7 +87,11 @@ __global__ void __launch_bounds__(256) noalloc_norm_kernel(const float* __restri
   unsigned int* done = reinterpret_cast<unsigned int*>(scratch + kDoneOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;
-  if (t == 0 && tid == 0) *done = 0u;
+  if (t == 0 && tid == 0) {
+    done[0] = 0u;
+    done[1] = 0u;
+    *reinterpret_cast<uint32_t*>(scratch + kStatusOff) = 0u;
+  }
   const float4* row = reinterpret_cast<const float4*>(h + (size_t)t * d);
   const int nc = d / 4;
   float ss = 0.f;
@@ -126,21 +144,12 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_VERIFY_ERR_CUDA;
   unsigned char* scratch = nullptr;
-  int rc = scratch_address(dev, &scratch);
+  PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  int rc = scratch_address(dev, &scratch, &fn);
   if (rc != MOE_VERIFY_OK) return rc;
 
-  auto encode = [](CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
-                   uint32_t box_rows) -> bool {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-      void* p = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                           cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess)
-        return false;
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+  auto encode = [fn](CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                     uint32_t box_rows) -> bool {
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {64, box_rows};
@@ -179,6 +188,7 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
   gp.targets = target_ids;
   gp.bad = reinterpret_cast<const int32_t*>(scratch + kBadOff);
   gp.done = reinterpret_cast<unsigned int*>(scratch + kDoneOff);
+  gp.aborted = reinterpret_cast<unsigned int*>(scratch + kDoneOff) + 1;
   if (mv::launch_lmhead(map_lm, map_xf, gp, lay.tokens_on_m, sms, s, false) != cudaSuccess)
     return MOE_VERIFY_ERR_CUDA;
   return MOE_VERIFY_OK;

@@ -27,6 +27,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Profiling stamps (see kStampSlots): one thread per CTA records.
+__device__ __forceinline__ void stamp_min(unsigned long long* slot) {
+  if (slot) atomicMin(slot, (unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void stamp_max(unsigned long long* slot) {
+  if (slot) atomicMax(slot, (unsigned long long)globaltimer_ns());
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
 __device__ __forceinline__ bool elect_one() { return lane_id() == 0; }

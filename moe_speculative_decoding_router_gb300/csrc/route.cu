@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // routing kernel two launches back wrote (a kernel lets its dependents start
   // only after its own wait, so that kernel is complete here).
   if (tid == 0) {
+    if (p.stamps) stamp_min(p.stamps);
     abort_flag = 0;
     mbar_init(&hx_bar, 1);
     mbar_init(&wr_bar, 1);
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // launches later may then read what the kernel before this one wrote.
   pdl_wait();
   pdl_launch_dependents();
+  if (p.stamps && tid == 0) stamp_max(p.stamps + 1);
   if (blockIdx.x == 0) {
     // counters of kernels that are complete now (the expert FFN before this
     // kernel, the routing kernel before that); the expert FFN after this
@@ -446,6 +448,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             reinterpret_cast<const uint4*>(xb + tt * pitch)[c];
     }
   }
+  if (p.stamps) {
+    __syncthreads();
+    if (tid == 0) stamp_max(p.stamps + 2);
+  }
 }
 
 // Residual update after the last block, then either the final RMSNorm (the
@@ -456,8 +462,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
   pdl_wait();
   pdl_launch_dependents();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int e = threadIdx.x; e < p.n_cnt_clear; e += 256) p.cnt_clear[e] = 0;
+    if (threadIdx.x == 0) *p.item_clear = 0;
+  }
   __shared__ float red[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;

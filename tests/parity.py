@@ -7,14 +7,33 @@ counted and reported.
 
 Each decoder block and the final argmax are checked teacher-forced: the
 oracle evaluates block l on the GPU's own residual stream entering block l
-(read from the hidden-state probe, fp32 values taken exactly in fp64).  A
-free-running comparison over all 12 blocks cannot hold at 1e-3: the bf16
-rounding of the normalised input and of the SwiGLU product turns last-bit
-differences between fp32 and fp64 into whole-ulp steps that grow from block
-to block (an fp32 emulation on the CPU drifts by up to ~1e-2 in router logits
-by the last blocks).  The whole trajectory is held instead to the hidden-state
-tolerance: max relative error 2e-2 per token and block, taken as
-max|gpu - ref| / max|ref| against the oracle run along the GPU's routing.
+(read from the hidden-state probe, fp32 values taken exactly in fp64).  The
+whole trajectory is held to the hidden-state tolerance: max relative error
+2e-2 per token and block, taken as max|gpu - ref| / max|ref| against the
+oracle run along the GPU's routing.
+
+Every checked token is also run through the oracle free-running (its own
+routing from the token id on).  Over 12 blocks the fp32 path drifts from
+fp64: the bf16 rounding of the normalised input and of the SwiGLU product
+turns last-bit differences into whole-ulp steps that compound, so free-running
+routing and targets can differ from the GPU's where the oracle's own gap is
+small.  Such differences are bounded, not just counted:
+  - the first block where the free-running routing set differs from the GPU's
+    must have an oracle selection gap below FREE_ROUTE_BAND (logit units);
+  - a target that differs while every block's routing agrees must have an
+    oracle top-2 logit gap below FREE_LOGIT_BAND.
+A difference at a larger gap fails.  The bands come from the drift measured
+on the GPU at full size: along the same routing the lm_head logits of the GPU
+and of the oracle differ by at most 0.033 (max relative error 1.1e-2; the
+full-size logits test re-measures it on every run and checks it against the
+band), and a flip needs an oracle top-2 gap below the sum of the two
+candidates' errors, so at most 0.067; the band is that, rounded up.  Router
+logits have the same scale (a bf16-normalised row times N(0, 0.02) weights
+over d = 1280, standard deviation ~0.72) and drift alike, so the routing band
+is the same.
+
+Every call's counts are kept in RECORD; the conftest prints them at the end
+of the run (and writes them as JSON where PARITY_RECORD names a file).
 """
 import concurrent.futures as fut
 import os
@@ -26,6 +45,11 @@ REL = 2e-2
 # one block, teacher-forced: only last-bit differences of the inputs' bf16
 # rounding separate the two sides
 BLOCK_REL = 2e-3
+# free-running differences must sit below these gaps (logit units)
+FREE_ROUTE_BAND = 8e-2
+FREE_LOGIT_BAND = 8e-2
+
+RECORD = []
 
 
 def threads():
@@ -43,22 +67,29 @@ def rel_err(got, ref):
     return np.max(np.abs(got - ref), axis=-1) / np.maximum(den, 1e-30)
 
 
+def _same_sets(a, b):
+    return set(np.asarray(a).tolist()) == set(np.asarray(b).tolist())
+
+
 def check_tokens(orc, ids, gpu_targets, probe_idx=None, probe_w=None, probe_hidden=None,
-                 sample=None, nthreads=None):
+                 sample=None, nthreads=None, label=None):
     """Check verify tokens ids[t] with GPU targets gpu_targets[t].
 
     With probes (topk_idx [L,T,k], topk_w [L,T,k], hidden [L+1,T,d]) every
-    block and the final argmax are checked teacher-forced, and the whole
-    trajectory against the oracle run along the GPU's routing.  Without
-    probes only the targets are compared (free-running).  Returns counts of
-    near ties, of free-running target differences, and worst errors."""
+    block and the final argmax are checked teacher-forced, the whole
+    trajectory against the oracle run along the GPU's routing, and the
+    free-running oracle's routing and target against the GPU's within the
+    bands.  Without probes the targets are compared with the free-running
+    oracle (exact outside the tie band).  Returns the counts, which are also
+    appended to RECORD under `label`."""
     T = len(ids)
     sample = list(range(T) if sample is None else sample)
     nthreads = nthreads or threads()
 
     def one(t):
         out = {"route_ties": 0, "logit_tie": 0, "free_diff": 0, "free_gap": None,
-               "max_rel": 0.0, "max_block_rel": 0.0, "fail": None}
+               "free_route_layers": 0, "free_route_gap": None, "free_diff_route_agrees": None,
+               "max_rel": 0.0, "max_block_rel": 0.0, "max_free_rel": 0.0, "fail": None}
         x = int(ids[t])
         if probe_hidden is None:
             r = orc.forward_token(x)
@@ -80,7 +111,7 @@ def check_tokens(orc, ids, gpu_targets, probe_idx=None, probe_w=None, probe_hidd
         for l in range(L):
             gsel = np.ascontiguousarray(probe_idx[l, t, :])
             h_new, sel, wts, gap, _ = orc.layer(l, H[l], force_sel=gsel)
-            if set(gsel.tolist()) != set(sel.tolist()):
+            if not _same_sets(gsel, sel):
                 if gap < TIE:
                     out["route_ties"] += 1
                 else:
@@ -106,25 +137,64 @@ def check_tokens(orc, ids, gpu_targets, probe_idx=None, probe_w=None, probe_hidd
                 out["fail"] = (f"token {t} (id {x}): gpu target {int(gpu_targets[t])} oracle on "
                                f"the gpu's final residual {tgt}, logit gap {lgap:.3g}")
                 return out
-        # the whole trajectory, oracle following the GPU's routing
-        r = orc.forward_token(x, force_sel=np.ascontiguousarray(probe_idx[:, t, :]))
-        e = rel_err(H, r["hidden"])
+        # free-running: the oracle's own routing from the token id on
+        free = orc.forward_token(x)
+        gsel_all = np.ascontiguousarray(probe_idx[:, t, :])
+        differ = [l for l in range(L) if not _same_sets(gsel_all[l], free["sel"][l])]
+        out["free_route_layers"] = len(differ)
+        if differ:
+            l0 = differ[0]
+            out["free_route_gap"] = float(free["route_gap"][l0])
+            if out["free_route_gap"] >= FREE_ROUTE_BAND:
+                out["fail"] = (f"token {t} (id {x}): free-running routing first differs at block "
+                               f"{l0} with oracle selection gap {out['free_route_gap']:.3g} "
+                               f">= {FREE_ROUTE_BAND}")
+                return out
+            # the whole trajectory along the GPU's routing
+            forced = orc.forward_token(x, force_sel=gsel_all)
+        else:
+            forced = free
+            out["max_free_rel"] = float(np.max(rel_err(H, free["hidden"])))
+        e = rel_err(H, forced["hidden"])
         out["max_rel"] = float(np.max(e))
         if out["max_rel"] > REL:
             out["fail"] = f"token {t}: hidden rel err per block {np.round(e, 5).tolist()}"
             return out
-        if r["target"] != int(gpu_targets[t]):
+        if free["target"] != int(gpu_targets[t]):
             out["free_diff"] = 1
-            out["free_gap"] = r["logit_gap"]
+            out["free_gap"] = free["logit_gap"]
+            out["free_diff_route_agrees"] = not differ
+            if not differ and free["logit_gap"] >= FREE_LOGIT_BAND:
+                out["fail"] = (f"token {t} (id {x}): free-running target {free['target']} vs gpu "
+                               f"{int(gpu_targets[t])} with identical routing, oracle logit gap "
+                               f"{free['logit_gap']:.3g} >= {FREE_LOGIT_BAND}")
+                return out
         return out
 
     with fut.ThreadPoolExecutor(max_workers=nthreads) as ex:
         res = list(ex.map(one, sample))
     fails = [r["fail"] for r in res if r["fail"]]
     assert not fails, "\n".join(fails[:10])
-    return {"tokens": len(res), "route_ties": sum(r["route_ties"] for r in res),
-            "logit_ties": sum(r["logit_tie"] for r in res),
+    stats = {"label": label, "tokens": len(res),
+             "route_ties": sum(r["route_ties"] for r in res),
+             "logit_ties": sum(r["logit_tie"] for r in res)}
+    if probe_hidden is not None:
+        stats.update({
             "free_running_target_diffs": sum(r["free_diff"] for r in res),
-            "free_running_diff_gaps": [r["free_gap"] for r in res if r["free_diff"]],
+            "free_running_diff_logit_gaps": [round(r["free_gap"], 5) for r in res
+                                             if r["free_diff"]],
+            "free_running_diffs_with_same_routing": sum(1 for r in res if r["free_diff"]
+                                                        and r["free_diff_route_agrees"]),
+            "free_running_route_diff_tokens": sum(1 for r in res if r["free_route_layers"]),
+            "free_running_first_route_gaps": [round(r["free_route_gap"], 5) for r in res
+                                              if r["free_route_gap"] is not None],
             "max_hidden_rel": max([r["max_rel"] for r in res] + [0.0]),
-            "max_block_rel": max([r["max_block_rel"] for r in res] + [0.0])}
+            "max_free_hidden_rel": max([r["max_free_rel"] for r in res] + [0.0]),
+            "max_block_rel": max([r["max_block_rel"] for r in res] + [0.0])})
+    RECORD.append(stats)
+    return stats
+
+
+def record(label, **counts):
+    """Adds counts of a test that does not go through check_tokens."""
+    RECORD.append(dict(label=label, **counts))
