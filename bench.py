@@ -389,7 +389,8 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    cfg = S.FULL if not args.layers else __import__("dataclasses").replace(S.FULL, n_layers=args.layers)
+    base = S.FULL_ZIPF if args.zipf else S.FULL
+    cfg = base if not args.layers else __import__("dataclasses").replace(base, n_layers=args.layers)
     # the workload's batch shape; profiling runs may time another one
     Bq = args.batch if (args.profile and args.batch) else B_SEQ
     Kq = args.drafts if (args.profile and args.drafts is not None) else K_DRAFT
@@ -429,9 +430,20 @@ def run_ours(args, rank, world, local):
         return
 
     if args.profile:
+        # per-launch windows inside the graph-replayed step (launch timestamps)
+        st = in_graph_stamps(ctx, cfg, plan, Bq, Kq, args.warmup, args.steps, dev)
+        L = cfg.n_layers
+        win = (st[:, :, 2] - st[:, :, 1]) * 1e-3  # us
         if rank == 0:
             print(json.dumps({"profile": True, "layers": cfg.n_layers, "batch": Bq, "drafts": Kq,
-                              "steps": args.steps, "ms_per_step": round(ms / args.steps, 4),
+                              "zipf": bool(args.zipf), "steps": args.steps,
+                              "ms_per_step": round(ms / args.steps, 4),
+                              "in_graph_us": {
+                                  "ffn_per_layer": [round(x, 2) for x in win[:, 1:2 * L:2].mean(0)],
+                                  "routing_per_layer": [round(x, 2)
+                                                        for x in win[:, 0:2 * L:2].mean(0)],
+                                  "lm_head": round(float(win[:, 2 * L].mean()), 2),
+                                  "step_span": round(float(st[:, 2 * L, 2].mean()) * 1e-3, 2)},
                               "clocks": clk}), flush=True)
         ctx.close()
         return
@@ -886,13 +898,17 @@ def main():
                     help="profiling only: sequences per step (default 32)")
     ap.add_argument("--drafts", type=int, default=None,
                     help="profiling only: drafts per sequence, 0..15 (default 3)")
+    ap.add_argument("--zipf", action="store_true",
+                    help="profiling only: the stack with the Zipf(s=1.2) router bias")
     ap.add_argument("--draft-head", action="store_true",
                     help="profiling only: time whole decode iterations with the FastMTP draft head")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if (args.layers or args.batch or args.drafts is not None or args.draft_head) and not args.profile:
-        ap.error("--layers, --batch, --drafts and --draft-head are for profiling runs only (--profile)")
+    if (args.layers or args.batch or args.drafts is not None or args.draft_head
+            or args.zipf) and not args.profile:
+        ap.error("--layers, --batch, --drafts, --zipf and --draft-head are for profiling runs "
+                 "only (--profile)")
     if args.draft_head and (args.layers or (args.drafts is not None and args.drafts < 1)):
         ap.error("--draft-head needs the full stack and at least one draft")
     if args.drafts is not None and not 0 <= args.drafts <= 15:

@@ -41,6 +41,8 @@ struct moe_verify_ctx {
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
           *io_alen = nullptr;
   CUtensorMap map_gu, map_dn, map_lm, map_wr;
+  // the expert weights with 256-row boxes (the token-major expert FFN)
+  CUtensorMap map_gu256, map_dn256;
   std::vector<void*> allocs;
   // host-buffer decode: one captured graph (step + accept) per (B, K)
   struct DecodeGraph {
@@ -250,8 +252,16 @@ struct Timed {
 
 // --------------------------------------------------------------- launches
 
+// The expert FFN runs token-major (the chunk's rows on the MMA's M side) from
+// this many verify tokens on: there each expert holds many rows, and the
+// weight-major form's epilogue (columns = rows, gate and up in different
+// warps) bounds it.  Measured on the 12-layer step: weight-major is ahead by
+// ~1.5% at 256 tokens, token-major by 4.5% at 384 and 10% at 512.
+constexpr int kTokmMinT = 320;
+
 struct StepShape {
   int T, tpb, grid_route, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
+  bool tokm;
   mv::LmLayout lm;
   bool wr_smem;
   size_t route_smem;
@@ -273,13 +283,14 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
   // that the shared-memory stages stay small and many of them fit (bytes in
   // flight per SM are what keep HBM busy).
   int avg = (int)((3LL * T * c->k + 2LL * c->E - 1) / (2LL * c->E));
-  s.nch = round_up(avg < 16 ? 16 : avg, 16);
+  s.tokm = T >= kTokmMinT && c->mt_gu % 2 == 0;
+  s.nch = s.tokm ? mv::kTokmChunk : round_up(avg < 16 ? 16 : avg, 16);
   if (s.nch > 256) s.nch = 256;
-  s.stages = mv::gemm_max_stages(s.nch);
+  s.stages = s.tokm ? mv::ffn_tokm_max_stages() : mv::gemm_max_stages(s.nch);
   s.lm = mv::lm_layout(T);
   s.n_chunks_lm = s.lm.n_chunks;
   s.nch_lm = s.lm.nch;
-  s.tmem_cols = pow2_at_least(2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm));
+  s.tmem_cols = s.tokm ? 512 : pow2_at_least(2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm));
   s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E, c->k, c->S);
   s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, c->k, c->S, s.wr_smem);
   if (encode_map(&s.map_x, c->xperm, c->d, c->rows_max, (uint32_t)s.nch) ||
@@ -369,8 +380,12 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   fp.S = c->S;
   fp.T = T;
   fp.nch = sh.nch;
-  fp.mt_gu = c->mt_gu;
-  fp.mt_dn = c->mt_dn;
+  fp.tile_gu = c->mt_gu;
+  fp.tile_dn = c->mt_dn;
+  // items per chunk: one per 128-row weight tile (weight-major) or per
+  // 256-row pair of tiles (token-major)
+  fp.mt_gu = sh.tokm ? c->mt_gu / 2 : c->mt_gu;
+  fp.mt_dn = sh.tokm ? (c->mt_dn + 1) / 2 : c->mt_dn;
   fp.kb_gu = c->d / 64;
   fp.kb_dn = c->I_pad / 64;
   fp.a_base_gu = l * c->nE * c->mt_gu * 128;
@@ -408,7 +423,13 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.pf_limit = c->nE * c->mt_gu;
   }
   fp.stamps = stamp_slot(c, stamped ? 2 * l + 1 : -1);
-  {
+  if (sh.tokm) {
+    fp.spec = 0;
+    fp.pf_limit = 0;
+    Timed tm(c, 0, s);
+    CK(mv::launch_ffn_tokm(c->map_gu256, sh.map_x, c->map_dn256, sh.map_a, fp, persistent_grid(c),
+                           s, pdl));
+  } else {
     Timed tm(c, 0, s);
     CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, fp, persistent_grid(c), s,
                       pdl));
@@ -586,9 +607,11 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   int e1 = encode_map(&c->map_gu, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 128);
   int e2 = encode_map(&c->map_dn, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 128);
   int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
+  int e5 = encode_map(&c->map_gu256, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 256);
+  int e6 = encode_map(&c->map_dn256, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 256);
   // router weights of all layers: boxes of 64 columns x E rows
   int e4 = encode_map(&c->map_wr, c->router, d, (uint64_t)L * E, (uint32_t)E);
-  if (e1 || e2 || e3 || e4) return fail(MOE_VERIFY_ERR_CUDA);
+  if (e1 || e2 || e3 || e4 || e5 || e6) return fail(MOE_VERIFY_ERR_CUDA);
 #undef AL
 #undef CKF
   *out = c;

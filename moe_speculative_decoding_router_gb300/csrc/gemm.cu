@@ -14,6 +14,10 @@
 // running, and have no waits of their own.
 // Once a CTA has issued its last load it pulls into L2 the weight item its
 // index starts with in the next kernel (next layer, or the lm_head).
+// ffn_tokm_kernel: the same layer's work with the operands swapped, for large
+// T: a chunk of <= 128 of an expert's rows on the MMA's M side, 256 weight rows
+// on N, so that each epilogue thread owns one row and the SwiGLU and the
+// weighted combine need no exchange between warps.
 // lmhead_kernel: [128 vocabulary rows] x [a chunk of <= 256 verify tokens],
 // epilogue the running greedy argmax over the vocabulary (two warp
 // reductions per token column, then across the four epilogue warps).
@@ -244,6 +248,60 @@ __device__ __forceinline__ FItem decode(const FfnParams& p, const Lists& L, int 
   return it;
 }
 
+// Per-expert rows, chunk and item prefix sums of one expert-FFN launch, by
+// one warp: 32 experts per round, shuffle scans with a running carry, all
+// counts loaded before the scans (one memory round trip).  Experts E ..
+// E+S-1 are the shared experts (T rows each).  An expert of c rows has
+// ceil(c / nch) chunks, each with mt_gu gate/up items and mt_dn down items.
+// totals: [0] gate/up items, [1] down items, [2] chunks.
+__device__ __forceinline__ void build_lists(const FfnParams& p, const Lists& L, int* totals) {
+  const int lane = threadIdx.x & 31, E = p.E, nE = p.E + p.S;
+  constexpr int kMaxRounds = (kMaxExperts + 31) / 32;
+  int craw[kMaxRounds];
+#pragma unroll
+  for (int r = 0; r < kMaxRounds; ++r) {
+    const int e = r * 32 + lane;
+    craw[r] = (e < E) ? __ldcg(p.cnt + e) : p.T;
+  }
+  int cc = 0, cg = 0, cd = 0;
+#pragma unroll
+  for (int r = 0; r < kMaxRounds; ++r) {
+    const int e0 = r * 32;
+    if (e0 >= nE) break;
+    const int e = e0 + lane;
+    int c = 0, ch = 0;
+    if (e < nE) {
+      c = min(craw[r], p.T);
+      ch = (c + p.nch - 1) / p.nch;
+      L.cnt[e] = c;
+    }
+    int ich = ch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ich, o);
+      if (lane >= o) ich += a;
+    }
+    if (e < nE) {
+      const int before = ich - ch;
+      L.cb[e] = cc + before;
+      L.igu[e] = cg + before * p.mt_gu;
+      L.idn[e] = cd + before * p.mt_dn;
+    }
+    const int tot = __shfl_sync(0xffffffffu, ich, 31);
+    cc += tot;
+    cg += tot * p.mt_gu;
+    cd += tot * p.mt_dn;
+  }
+  if (lane == 0) {
+    L.cb[nE] = cc;
+    L.igu[nE] = cg;
+    L.idn[nE] = cd;
+    totals[0] = cg;
+    totals[1] = cd;
+    totals[2] = cc;
+  }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
                const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
@@ -259,7 +317,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ int s_totals[3];  // gate/up items, down items, chunks
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = p.E, nE = p.E + p.S;
+  const int nE = p.E + p.S;
   Lists L;
   L.cnt = list_base;
   L.cb = L.cnt + nE;
@@ -313,55 +371,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < pre; ++s)
       tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &map_x, C.spec_b, s * 64, row0, pol_x);
   }
-  if (warp == 0) {
-    // per-expert rows, chunk and item prefix sums: one warp, 32 experts per
-    // round, shuffle scans with a running carry
-    // all counts are loaded before the scans (one memory round trip)
-    constexpr int kMaxRounds = (kMaxExperts + 31) / 32;
-    int craw[kMaxRounds];
-#pragma unroll
-    for (int r = 0; r < kMaxRounds; ++r) {
-      const int e = r * 32 + lane;
-      craw[r] = (e < E) ? __ldcg(p.cnt + e) : p.T;
-    }
-    int cc = 0, cg = 0, cd = 0;
-#pragma unroll
-    for (int r = 0; r < kMaxRounds; ++r) {
-      const int e0 = r * 32;
-      if (e0 >= nE) break;
-      const int e = e0 + lane;
-      int c = 0, ch = 0;
-      if (e < nE) {
-        c = min(craw[r], p.T);
-        ch = (c + p.nch - 1) / p.nch;
-        L.cnt[e] = c;
-      }
-      int ich = ch;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, ich, o);
-        if (lane >= o) ich += a;
-      }
-      if (e < nE) {
-        const int before = ich - ch;
-        L.cb[e] = cc + before;
-        L.igu[e] = cg + before * p.mt_gu;
-        L.idn[e] = cd + before * p.mt_dn;
-      }
-      const int tot = __shfl_sync(0xffffffffu, ich, 31);
-      cc += tot;
-      cg += tot * p.mt_gu;
-      cd += tot * p.mt_dn;
-    }
-    if (lane == 0) {
-      L.cb[nE] = cc;
-      L.igu[nE] = cg;
-      L.idn[nE] = cd;
-      s_totals[0] = cg;
-      s_totals[1] = cd;
-      s_totals[2] = cc;
-    }
-  }
+  if (warp == 0) build_lists(p, L, s_totals);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -610,6 +620,263 @@ __device__ __forceinline__ void lm_finish(const GemmParams& p, bool cta_aborted,
       *p.done = 0u;
       *p.aborted = 0u;
     }
+  }
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
+}
+
+// ----------------------------------------------- expert FFN, token-major
+//
+// The same work as ffn_kernel with the roles of the operands swapped, for
+// large T (many rows per expert): a chunk of <= 128 of an expert's rows on the
+// MMA's M side, 256 weight rows on N.  A gate/up item covers 128 intermediate
+// units: two consecutive repacked 128-row tiles, i.e. accumulator columns
+// [gate u0..u0+63 | up u0..u0+63 | gate u0+64..u0+127 | up u0+64..u0+127].  A
+// down item covers 256 output dimensions.  Each epilogue thread owns one row
+// (one TMEM lane), so SwiGLU pairs column c with column c + 64 in registers and
+// the down epilogue looks up its row's token, slot and weight once per item:
+// no exchange between warps.  Items run expert-major as in ffn_kernel and are
+// claimed in the same order; a down item waits until the four epilogue warps
+// of every gate/up item of its chunk have published their rows.
+
+__device__ __forceinline__ FItem decode_tokm(const FfnParams& p, const Lists& L, int nE, int n_gu,
+                                             int i) {
+  FItem it;
+  it.down = i >= n_gu ? 1 : 0;
+  const int r = it.down ? i - n_gu : i;
+  const int* io = it.down ? L.idn : L.igu;
+  const int mt_n = it.down ? p.mt_dn : p.mt_gu;  // 256-row tiles per chunk
+  int lo = 0, hi = nE - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (io[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  it.e = lo;
+  const int q = r - io[lo];
+  const int ch = q / mt_n;
+  it.mt = q - ch * mt_n;
+  it.n = min(p.nch, L.cnt[lo] - ch * p.nch);
+  it.row0 = lo * p.T + ch * p.nch;
+  it.chunk = L.cb[lo] + ch;
+  const int tiles = it.down ? p.tile_dn : p.tile_gu;
+  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (lo * tiles + 2 * it.mt) * 128;
+  it.kblocks = it.down ? p.kb_dn : p.kb_gu;
+  return it;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ffn_tokm_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
+                    const FfnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  constexpr int kStageX = kTokmChunk * 128;  // 128 rows x 64 bf16
+  constexpr int kStageW = 256 * 128;         // 256 weight rows x 64 bf16
+  constexpr int stage_bytes = kStageX + kStageW;
+  uint8_t* stages = smem;
+  uint8_t* ctrl_base = smem + (size_t)p.stages * stage_bytes;
+  const Ctrl C = ctrl_at(ctrl_base, p.stages);
+  int* list_base = reinterpret_cast<int*>(ctrl_base + kCtrlBytes);
+  __shared__ int s_totals[3];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nE = p.E + p.S;
+  Lists L;
+  L.cnt = list_base;
+  L.cb = L.cnt + nE;
+  L.igu = L.cb + nE + 1;
+  L.idn = L.igu + nE + 1;
+
+  // every item, the first included, is claimed in order (see ffn_kernel)
+  int first = 0;
+  if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
+    first = atomicAdd(p.next_item, 1);
+    init_ctrl(C, p.stages, 2, 2);
+    tma_prefetch_desc(&map_gu);
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_dn);
+    tma_prefetch_desc(&map_a);
+  }
+  if (warp == 1) {
+    tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
+  if (warp == 0) build_lists(p, L, s_totals);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *C.tmem_slot;
+  const int n_gu = s_totals[0];
+  const int n_items = n_gu + s_totals[1];
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int i = first < n_items ? first : -1, kb = 0;
+      FItem it = {};
+      int nq = 0, next_raw = 0;
+      auto start_item = [&](int item) -> bool {
+        if (!queue_push(C, nq++, item, p.status)) return false;
+        if (item >= 0) {
+          it = decode_tokm(p, L, nE, n_gu, item);
+          next_raw = atomicAdd(p.next_item, 1);
+        }
+        return true;
+      };
+      bool ok = start_item(i);
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      while (ok && i >= 0) {
+        if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sx = stages + (size_t)stage * stage_bytes;
+        uint8_t* sw = sx + kStageX;
+        mbar_arrive_expect_tx(&C.full[stage], (uint32_t)stage_bytes);
+        tma_load_2d(sw, it.down ? &map_dn : &map_gu, &C.full[stage], kb * 64, it.a_row, pol_w);
+        if (it.down && kb == 0) {
+          // every gate/up item of this chunk is published (four warps each)
+          const int want = 4 * p.mt_gu;
+          const uint64_t t0 = globaltimer_ns();
+          uint32_t n = 0;
+          while (ld_acquire(p.dep + it.chunk) < want) {
+            if ((++n & 63u) == 0 && (*C.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+              if (!*C.abort_flag) {
+                *C.abort_flag = 1;
+                atomicOr(p.status, kErrTimeout);
+              }
+              ok = false;
+              break;
+            }
+          }
+          fence_proxy_async_global();
+        }
+        // on a failed wait the rows are still loaded (stale), so that the
+        // stage's byte count completes and the drain ends
+        tma_load_2d(sx, it.down ? &map_a : &map_x, &C.full[stage], kb * 64, it.row0, pol_x);
+        ++issued;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++kb == it.kblocks) {
+          kb = 0;
+          i = next_raw < n_items ? next_raw : -1;
+          if (!start_item(i)) ok = false;
+        }
+      }
+      if (!ok) producer_drain(C, issued, p.stages);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t idesc = umma_idesc_bf16(128, 256);
+      for (int local = 0;; ++local) {
+        const int i = queue_pop(C, local, p.status, false);
+        if (i < 0) break;
+        const FItem it = decode_tokm(p, L, nE, n_gu, i);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        // A = the chunk's rows (stage offset 0), B = the weight rows (kStageX on)
+        if (!mma_item(C, stages, stage_bytes, p.stages, stage, phase, it.kblocks,
+                      tmem_base + (uint32_t)(buf * 256), idesc, p.status))
+          break;
+        umma_commit(&C.tfull[buf]);
+      }
+      mma_drain(C);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;      // TMEM lane quarter: rows q*32 .. q*32+31 of the chunk
+    const int rr = q * 32 + lane;
+    for (int local = 0;; ++local) {
+      const int i = queue_pop(C, local, p.status, true);
+      if (i < 0) break;
+      const FItem it = decode_tokm(p, L, nE, n_gu, i);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
+      const bool valid = rr < it.n;
+      const int row = it.row0 + rr;
+      if (!it.down) {
+        // a = bf16(silu(g) * u) for units it.mt*128 + [0, 128) of this row
+        __nv_bfloat16* out = p.a_out + (size_t)row * p.I_pad + it.mt * 128;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < 64; c0 += 16) {
+            uint32_t g[16], u[16];
+            tmem_ld16(tb + (uint32_t)(h * 128 + c0), g);
+            tmem_ld16(tb + (uint32_t)(h * 128 + 64 + c0), u);
+            tmem_ld_wait();
+            if (valid) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                const float a0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                const float a1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+                pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(out + h * 64 + c0);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        }
+        // publish this warp's rows of the chunk to its down items
+        __threadfence();
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.dep + it.chunk, 1);
+      } else {
+        int tok = 0, slot = 0;
+        float w = 0.f;
+        if (valid) {
+          tok = __ldg(p.perm_token + row);
+          slot = __ldg(p.perm_slot + row);
+          w = __ldg(p.perm_w + row);
+        }
+        const int m0 = it.mt * 256;  // first output dimension of this item
+        float* out = p.y + ((size_t)tok * p.kS + slot) * p.d + m0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+          if (valid && m0 + c0 < p.d) {
+            float4* dst = reinterpret_cast<float4*>(out + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(w * __uint_as_float(v[4 * j]), w * __uint_as_float(v[4 * j + 1]),
+                                   w * __uint_as_float(v[4 * j + 2]),
+                                   w * __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.tempty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
   if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
 }
@@ -1083,6 +1350,24 @@ cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        bool pdl) {
   return launch_gemm_ex(ffn_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu, map_x,
                         map_dn, map_a, map_pf, p);
+}
+
+size_t ffn_tokm_smem_bytes(int stages) {
+  return 1024 /* alignment slack */ + (size_t)stages * (kTokmChunk * 128 + 256 * 128) +
+         kCtrlBytes + kListBytes;
+}
+
+int ffn_tokm_max_stages() {
+  int s = 8;
+  while (s > 2 && ffn_tokm_smem_bytes(s) > 227 * 1024) --s;
+  return s;
+}
+
+cudaError_t launch_ffn_tokm(const CUtensorMap& map_gu256, const CUtensorMap& map_x,
+                            const CUtensorMap& map_dn256, const CUtensorMap& map_a,
+                            const FfnParams& p, int grid, cudaStream_t s, bool pdl) {
+  return launch_gemm_ex(ffn_tokm_kernel, grid, ffn_tokm_smem_bytes(p.stages), s, pdl, map_gu256,
+                        map_x, map_dn256, map_a, p);
 }
 
 LmLayout lm_layout(int T) {

@@ -69,7 +69,9 @@ struct FfnParams {
   const int32_t* cnt;          // [E] routed rows per expert (shared experts: T)
   int32_t* dep;                // [chunks] finished gate/up halves per chunk (zero on entry)
   int E, S, T, nch;
-  int mt_gu, mt_dn;            // 128-row tiles per expert
+  int mt_gu, mt_dn;            // items per chunk: gate/up, down (the weight-major form: the
+                               // expert's 128-row weight tiles; token-major: 256-row tiles)
+  int tile_gu, tile_dn;        // 128-row weight tiles per expert in the tensor maps
   int kb_gu, kb_dn;            // 64-wide K blocks: d/64 and I_pad/64
   int a_base_gu, a_base_dn;    // first weight row of this layer in the tensor maps
   int stages, tmem_cols;
@@ -135,6 +137,8 @@ struct AcceptParams {
 // Shared memory the GEMM kernels need for a given item width and stage count.
 size_t gemm_smem_bytes(int nch, int stages);
 int gemm_max_stages(int nch);
+size_t ffn_tokm_smem_bytes(int stages);
+int ffn_tokm_max_stages();
 size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem);
 bool route_wr_fits(int tpb, int d, int E, int k, int S);
 
@@ -145,6 +149,14 @@ cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_dn, const CUtensorMap& map_a,
                        const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
                        bool pdl);
+// The token-major form of the layer's expert FFN (large T): 128 of an
+// expert's rows on the MMA's M side, 256 weight rows on N.  map_gu256 and
+// map_dn256 are the weight maps with 256-row boxes, map_x and map_a the
+// activation maps with 128-row boxes.  Needs tile_gu even.
+constexpr int kTokmChunk = 128;
+cudaError_t launch_ffn_tokm(const CUtensorMap& map_gu256, const CUtensorMap& map_x,
+                            const CUtensorMap& map_dn256, const CUtensorMap& map_a,
+                            const FfnParams& p, int grid, cudaStream_t s, bool pdl);
 // The lm_head launch for T tokens: tokens on the MMA's M side for 65..128
 // tokens (one chunk), else vocabulary rows on M with chunks of <= 256 tokens.
 struct LmLayout {

@@ -499,6 +499,23 @@ def test_sweep_batch128_sampled(full_zipf_free, K):
                  label=f"sweep B=128 K={K}")
 
 
+def test_full_batch_invariance_across_ffn_forms(full_zipf_free):
+    """Inside a batch of 512 verify tokens the expert FFN runs token-major
+    (rows on the MMA's M side); alone, a sequence's 4 tokens run weight-major.
+    Targets and every block's residual stream are the same bits either way."""
+    ctx, _ = full_zipf_free
+    B = _B()
+    ids = S.uniform_ids(128 * 4, 78, 1, S.FULL.vocab).reshape(128, 4)
+    pa, ta = B.make_probe(S.FULL.n_layers, 512, S.FULL, topk=False)
+    big = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=pa).cpu().numpy()
+    ha = ta["hidden"].cpu().numpy()
+    for b in (0, 77, 127):
+        pb, tb = B.make_probe(S.FULL.n_layers, 4, S.FULL, topk=False)
+        one = ctx.step(_i32(ids[b:b + 1, 0]), _i32(ids[b:b + 1, 1:]), probe=pb).cpu().numpy()
+        assert np.array_equal(tb["hidden"].cpu().numpy(), ha[:, 4 * b:4 * b + 4, :]), b
+        assert np.array_equal(one[0], big[b]), b
+
+
 @pytest.fixture(scope="module")
 def full_zipf_free(full):
     """The full stack without bias, room for 128 x 4 tokens."""
