@@ -222,6 +222,12 @@ struct Lists {
   int* idn;  // [nE+1] first down item per expert
 };
 
+// Expert of list position j: the shared experts (E .. E+S-1) come first,
+// then the routed experts in index order.
+__device__ __forceinline__ int list_expert(const FfnParams& p, int j) {
+  return j < p.S ? p.E + j : j - p.S;
+}
+
 __device__ __forceinline__ FItem decode(const FfnParams& p, const Lists& L, int nE, int n_gu,
                                         int i) {
   FItem it;
@@ -236,32 +242,33 @@ __device__ __forceinline__ FItem decode(const FfnParams& p, const Lists& L, int 
     const int mid = (lo + hi + 1) >> 1;
     if (io[mid] <= r) lo = mid; else hi = mid - 1;
   }
-  it.e = lo;
+  const int ex = list_expert(p, lo);
+  it.e = ex;
   const int q = r - io[lo];
   const int ch = q / mt_n;
   it.mt = q - ch * mt_n;
   it.n = min(p.nch, L.cnt[lo] - ch * p.nch);
-  it.row0 = lo * p.T + ch * p.nch;
+  it.row0 = ex * p.T + ch * p.nch;
   it.chunk = L.cb[lo] + ch;
-  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (lo * mt_n + it.mt) * 128;
+  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (ex * mt_n + it.mt) * 128;
   it.kblocks = it.down ? p.kb_dn : p.kb_gu;
   return it;
 }
 
 // Per-expert rows, chunk and item prefix sums of one expert-FFN launch, by
-// one warp: 32 experts per round, shuffle scans with a running carry, all
-// counts loaded before the scans (one memory round trip).  Experts E ..
-// E+S-1 are the shared experts (T rows each).  An expert of c rows has
+// one warp: 32 list positions per round, shuffle scans with a running carry,
+// all counts loaded before the scans (one memory round trip).  Lists are in
+// list order (shared experts first, T rows each).  An expert of c rows has
 // ceil(c / nch) chunks, each with mt_gu gate/up items and mt_dn down items.
 // totals: [0] gate/up items, [1] down items, [2] chunks.
 __device__ __forceinline__ void build_lists(const FfnParams& p, const Lists& L, int* totals) {
-  const int lane = threadIdx.x & 31, E = p.E, nE = p.E + p.S;
+  const int lane = threadIdx.x & 31, nE = p.E + p.S;
   constexpr int kMaxRounds = (kMaxExperts + 31) / 32;
   int craw[kMaxRounds];
 #pragma unroll
   for (int r = 0; r < kMaxRounds; ++r) {
-    const int e = r * 32 + lane;
-    craw[r] = (e < E) ? __ldcg(p.cnt + e) : p.T;
+    const int j = r * 32 + lane;
+    craw[r] = (j < p.S || j >= nE) ? p.T : __ldcg(p.cnt + (j - p.S));
   }
   int cc = 0, cg = 0, cd = 0;
 #pragma unroll
@@ -302,6 +309,30 @@ __device__ __forceinline__ void build_lists(const FfnParams& p, const Lists& L, 
   }
 }
 
+// Weight row (in the gate/up tensor map, layer base `base`) and first
+// expert-major row of gate/up item c as the first items run: the shared
+// experts' items (ceil(T / nch) chunks each) are always where this says; a
+// routed expert's are when each routed expert holds one chunk (then routed
+// item c is tile c % mt_gu of expert c / mt_gu).  Returns false past the
+// gate/up items such a layout has, or for routed items when routed = false.
+__device__ __forceinline__ bool guess_gu_item(const FfnParams& p, int c, int base, bool routed,
+                                              int* a_row, int* row0) {
+  const int ch_s = (p.T + p.nch - 1) / p.nch;
+  const int n_sh = p.S * ch_s * p.mt_gu;
+  if (c < n_sh) {
+    const int s = c / (ch_s * p.mt_gu), q = c - s * ch_s * p.mt_gu;
+    const int ch = q / p.mt_gu, t = q - ch * p.mt_gu;
+    *a_row = base + ((p.E + s) * p.mt_gu + t) * 128;
+    *row0 = (p.E + s) * p.T + ch * p.nch;
+    return true;
+  }
+  const int cr = c - n_sh;
+  if (!routed || cr >= p.E * p.mt_gu) return false;
+  *a_row = base + cr * 128;
+  *row0 = (cr / p.mt_gu) * p.T;
+  return true;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
                const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
@@ -329,17 +360,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // counter was cleared two launches back).  So any gate/up item that a down
   // item waits for belongs to a CTA that is already running, and the kernel
   // makes progress whatever number of its CTAs the GPU runs at once.
-  // Speculation: when every expert holds one chunk, item c is gate/up tile c
-  // of this layer, so the weight tiles of the ticket's item do not depend on
-  // the routing and start streaming before waiting for it.  The host turns
-  // this on only when every routed expert expects several rows (else most
-  // guesses would miss and their loads would only take bandwidth).
-  int first = 0, guess_row = 0, pre = 0;
+  // Speculation: the first items run the shared experts (their rows are all
+  // T tokens), then, when every routed expert holds one chunk, routed expert
+  // c / mt_gu's tile c % mt_gu; so the weight tiles of the ticket's item are
+  // known without the routing and start streaming before waiting for it.
+  // The host guesses routed items only when every routed expert expects
+  // several rows (else most of those guesses would miss and their loads
+  // would only take bandwidth); shared items are always right.
+  int first = 0, guess_row = 0, guess_row0 = 0, pre = 0;
   if (threadIdx.x == 0) {
     stamp_min(p.stamps);
     first = atomicAdd(p.next_item, 1);
-    guess_row = p.a_base_gu + first * 128;
-    pre = (p.spec && first < nE * p.mt_gu) ? min(p.stages, p.kb_gu) : 0;
+    if (p.spec > 0 && guess_gu_item(p, first, p.a_base_gu, p.spec > 1, &guess_row, &guess_row0))
+      pre = min(p.stages, p.kb_gu);
     init_ctrl(C, p.stages, 2, 2);
     tma_prefetch_desc(&map_gu);
     tma_prefetch_desc(&map_x);
@@ -363,13 +396,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   pdl_launch_dependents();
   if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
   if (threadIdx.x == 0 && pre > 0) {
-    // the speculated first item's activation rows (chunk 0 of expert
-    // first / mt_gu) load while the item lists are built
+    // the speculated first item's activation rows load while the item lists
+    // are built
     const uint64_t pol_x = policy_evict_last();
-    const int row0 = (first / p.mt_gu) * p.T;
     mbar_arrive_expect_tx(C.spec_b, (uint32_t)(pre * p.nch * 128));
     for (int s = 0; s < pre; ++s)
-      tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &map_x, C.spec_b, s * 64, row0, pol_x);
+      tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &map_x, C.spec_b, s * 64, guess_row0,
+                  pol_x);
   }
   if (warp == 0) build_lists(p, L, s_totals);
   tc_fence_before();
@@ -405,7 +438,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         mbar_wait(C.spec_b, 0, C.abort_flag, p.status);
       ok = ok && start_item(i);
       const bool hit = ok && pre > 0 && i >= 0 && !it.down && it.a_row == guess_row &&
-                       it.row0 == (first / p.mt_gu) * p.T;
+                       it.row0 == guess_row0;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -470,8 +503,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // weight item numbered like this CTA (the first items of the next
         // kernel's CTAs together), while HBM has room (the last items of
         // other CTAs and the routing in between)
-        const int row = p.pf_base + (int)(blockIdx.x / p.pf_div) * 128;
-        for (int k = 0; k < p.pf_kb; ++k) tma_prefetch_l2_2d(&map_pf, k * 64, row);
+        int row = p.pf_base + (int)(blockIdx.x / p.pf_div) * 128, row0 = 0;
+        const bool known = !p.pf_items || guess_gu_item(p, (int)blockIdx.x, p.pf_base, true, &row,
+                                                        &row0);
+        if (known)
+          for (int k = 0; k < p.pf_kb; ++k) tma_prefetch_l2_2d(&map_pf, k * 64, row);
       }
       if (!ok) producer_drain(C, issued, p.stages);
     }
@@ -650,15 +686,16 @@ __device__ __forceinline__ FItem decode_tokm(const FfnParams& p, const Lists& L,
     const int mid = (lo + hi + 1) >> 1;
     if (io[mid] <= r) lo = mid; else hi = mid - 1;
   }
-  it.e = lo;
+  const int ex = list_expert(p, lo);
+  it.e = ex;
   const int q = r - io[lo];
   const int ch = q / mt_n;
   it.mt = q - ch * mt_n;
   it.n = min(p.nch, L.cnt[lo] - ch * p.nch);
-  it.row0 = lo * p.T + ch * p.nch;
+  it.row0 = ex * p.T + ch * p.nch;
   it.chunk = L.cb[lo] + ch;
   const int tiles = it.down ? p.tile_dn : p.tile_gu;
-  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (lo * tiles + 2 * it.mt) * 128;
+  it.a_row = (it.down ? p.a_base_dn : p.a_base_gu) + (ex * tiles + 2 * it.mt) * 128;
   it.kblocks = it.down ? p.kb_dn : p.kb_gu;
   return it;
 }

@@ -85,10 +85,16 @@ struct FfnParams {
   uint32_t* status;
   int* next_item;              // items claimed so far, every CTA's first included (zero on entry)
   // L2 prefetch of the next kernel's first weight item of this CTA index c,
-  // issued once this CTA has no items left: rows pf_base + (c / pf_div) * 128
-  // of the prefetch tensor map, pf_kb 64-column boxes, for c < pf_limit
-  int pf_base, pf_div, pf_limit, pf_kb;
-  int spec;                    // 1: load the guessed first item's tiles before the wait
+  // issued once this CTA has no items left, for c < pf_limit, pf_kb 64-column
+  // boxes of the prefetch tensor map: pf_items = 1, the next layer's gate/up
+  // item c as guessed for the first items (pf_base = that layer's first
+  // gate/up row); pf_items = 0, rows pf_base + (c / pf_div) * 128
+  int pf_base, pf_div, pf_limit, pf_kb, pf_items;
+  // Items run shared experts first, so the first items' weights are known
+  // before the routing for the shared experts always, and for the routed
+  // experts when each holds one chunk: spec = 2 guesses both, 1 the shared
+  // experts' items only, 0 none.
+  int spec;
   unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
