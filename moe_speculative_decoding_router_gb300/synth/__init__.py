@@ -58,6 +58,15 @@ def tid_lm_head(n_layers: int) -> int:
     return 2 + 8 * n_layers
 
 
+_ATTN_TENSORS = ("w_q", "w_k", "w_v", "w_o")
+
+
+def tid_attn(n_layers: int, layer: int, name: str) -> int:
+    """Attention projections come after every tensor of the attention-free
+    stack, so adding attention changes none of those streams."""
+    return 3 + 8 * n_layers + 4 * layer + _ATTN_TENSORS.index(name)
+
+
 def build(force: bool = False) -> str:
     """Compile the generator with gcc (in-tree, host only)."""
     with _lock:
@@ -144,6 +153,8 @@ class ModelConfig:
     sigma: float = 0.02          # std of every weight tensor
     zipf_s: float = 0.0          # >0: per-expert router bias -s*ln(e+1)
     name: str = ""
+    n_heads: int = 0             # >0: attention before each MoE block (head width hidden/n_heads)
+    rope_theta: float = 10000.0
 
 
 # Tiny correctness instance: 2 layers, d=64, 8 experts of 32, top-2, one
@@ -157,6 +168,10 @@ LAYER = ModelConfig(1, 1280, 64, 6, 2, 896, 896, 512, name="layer")
 FULL = ModelConfig(12, 1280, 64, 6, 2, 896, 896, 129280, name="full")
 # The full stack with Zipf(s=1.2)-skewed routing.
 FULL_ZIPF = dataclasses.replace(FULL, zipf_s=1.2, name="full_zipf")
+# The stacks with attention before each MoE block (the pages give no shape:
+# heads of width 128 at hidden 1280, 16 at hidden 64).
+TINY_ATTN = dataclasses.replace(TINY, n_heads=4, name="tiny_attn")
+FULL_ATTN = dataclasses.replace(FULL, n_heads=10, name="full_attn")
 
 
 # FastMTP draft heads: one dense block applied recursively, sharing the
@@ -221,6 +236,14 @@ def make_weights(cfg: ModelConfig, seed: int = SEED_WEIGHTS, with_embed: bool = 
     rb = router_bias(cfg)
     if rb is not None:
         w["router_bias"] = rb
+    if cfg.n_heads > 0:
+        w["attn_norm"] = np.full((L, d), one, dtype=np.uint16)
+        for name in _ATTN_TENSORS:
+            arr = np.empty((L, d, d), dtype=np.uint16)
+            for l in range(L):
+                lib().synth_normal_bf16(arr[l].ctypes.data, arr[l].size, seed, tid_attn(L, l, name),
+                                        0, float(sg), _threads(nthreads))
+            w[name] = arr
     return w
 
 

@@ -35,6 +35,11 @@ class OracleConfig(ctypes.Structure):
                 ("vocab", _i32), ("rms_eps", ctypes.c_double)]
 
 
+class OracleAttnWeights(ctypes.Structure):
+    _fields_ = [("n_heads", _i32), ("rope_theta", ctypes.c_double), ("attn_norm", _P), ("w_q", _P),
+                ("w_k", _P), ("w_v", _P), ("w_o", _P)]
+
+
 class OracleWeights(ctypes.Structure):
     _fields_ = [("embed", _P), ("final_norm", _P), ("lm_head", _P), ("norm", _P), ("router", _P),
                 ("router_bias", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
@@ -83,6 +88,12 @@ def lib():
         L.oracle_layer_bf16.argtypes = [_P, _P, _i32, _P, _P, _P, _P, _P, _P, _P]
         L.oracle_draft.restype = _i32
         L.oracle_draft.argtypes = [_P, _P, _P, _i32, _i32, _P, _P, _P]
+        L.oracle_rope.restype = None
+        L.oracle_rope.argtypes = [_P, _i32, _i32, ctypes.c_double]
+        L.oracle_attn_block.restype = None
+        L.oracle_attn_block.argtypes = [_P, _P, _i32, _P, _i32, _P, _P, _P]
+        L.oracle_forward_seq.restype = _i32
+        L.oracle_forward_seq.argtypes = [_P, _P, _P, _P, _i32, _P, _P, _P, _P, _P, _P]
         _lib = L
     return _lib
 
@@ -129,6 +140,13 @@ def swiglu_expert(xhat, Wg, Wu, Wd) -> np.ndarray:
     return y
 
 
+def rope(x: np.ndarray, pos: int, theta: float = 10000.0) -> np.ndarray:
+    """The rotary embedding of one head vector (a rotated copy)."""
+    y = np.array(x, dtype=np.float64, copy=True)
+    lib().oracle_rope(_ptr(y), y.shape[0], int(pos), float(theta))
+    return y
+
+
 def accept(drafts: np.ndarray, targets: np.ndarray, V: int):
     """Returns (committed [B,K+1], accept_len [B], bad_rows)."""
     drafts = np.ascontiguousarray(drafts, dtype=np.int32)
@@ -170,6 +188,12 @@ class Oracle:
             per_layer("s_down"))
         self._cp = ctypes.byref(self._c)
         self._wp = ctypes.byref(self._w)
+        self._ap = None
+        if getattr(cfg, "n_heads", 0) > 0:
+            self._a = OracleAttnWeights(cfg.n_heads, float(cfg.rope_theta), per_layer("attn_norm"),
+                                        per_layer("w_q"), per_layer("w_k"), per_layer("w_v"),
+                                        per_layer("w_o"))
+            self._ap = ctypes.byref(self._a)
 
     # -- one token through the whole stack --------------------------------
     def forward_token(self, x: int, force_sel: Optional[np.ndarray] = None, logits: bool = False):
@@ -257,6 +281,39 @@ class Oracle:
         if rc != 0:
             raise ValueError("draft token id outside [0, V)")
         return drafts, hid, gaps
+
+    # -- the stack with attention (configs with n_heads > 0) ---------------
+    def attn_block(self, l: int, h: np.ndarray, pos: int, kc: np.ndarray, vc: np.ndarray):
+        """Attention sub-block of layer l on one token at position pos:
+        returns (h after it, o before W_o).  kc, vc: [pos + 1, d] float64
+        caches of this layer (rows < pos read, row pos written in place)."""
+        hh = np.array(h, dtype=np.float64, copy=True)
+        assert kc.dtype == np.float64 and kc.flags["C_CONTIGUOUS"] and kc.shape[0] >= pos + 1
+        assert vc.dtype == np.float64 and vc.flags["C_CONTIGUOUS"] and vc.shape[0] >= pos + 1
+        o = np.empty(self.cfg.hidden)
+        lib().oracle_attn_block(self._cp, self._ap, int(l), _ptr(hh), int(pos), _ptr(kc), _ptr(vc),
+                                _ptr(o))
+        return hh, o
+
+    def forward_seq(self, ids: Sequence[int], caches: bool = False, hidden: bool = False):
+        """A whole sequence with attention: greedy target after every prefix,
+        top-2 logit gaps, selection gaps [n, L]; with caches=True the key and
+        value caches [L, n, d], with hidden=True the residual stream entering
+        each block and after the last, [n, L+1, d]."""
+        c = self.cfg
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        n, L, d = ids.shape[0], c.n_layers, c.hidden
+        tg = np.empty(n, np.int32)
+        lg = np.empty(n)
+        rg = np.empty((n, L))
+        kc = np.empty((L, n, d)) if caches else None
+        vc = np.empty((L, n, d)) if caches else None
+        hid = np.empty((n, L + 1, d)) if hidden else None
+        rc = lib().oracle_forward_seq(self._cp, self._wp, self._ap, _ptr(ids), n, _ptr(tg), _ptr(lg),
+                                      _ptr(rg), _ptr(kc), _ptr(vc), _ptr(hid))
+        if rc != 0:
+            raise ValueError("token id outside [0, V)")
+        return dict(targets=tg, logit_gaps=lg, route_gaps=rg, kcache=kc, vcache=vc, hidden=hid)
 
     def layer_bf16(self, l: int, h_in: np.ndarray, force_sel: Optional[np.ndarray] = None):
         """The bf16-in/bf16-out block on one token.  Returns

@@ -380,3 +380,148 @@ ORACLE_API int32_t oracle_draft(const oracle_config* c, const oracle_weights* w,
   free(h);
   return rc;
 }
+
+/* ------------------------------------------------------- attention (NEXT) --
+ * The decoder's attention, which the verify step above leaves out.  The
+ * pages name the decoder (DeepSeek-3B-MoE, 12 layers, position limit 32,768:
+ * "Jina AI Releases jina-ocr-v1, a 3.4B MoE Document Parser With Built-In
+ * Speculative Decoding", architecture paragraph) but give no attention shape.
+ * Reading taken:
+ *   - each block is pre-norm attention then the MoE block above:
+ *       h += W_o . attn(bf16(RMSNorm_a(h) * g_a));   then oracle_layer;
+ *   - multi-head attention, n_heads heads of width hd = d / n_heads, no
+ *     biases; rotary position embedding on q and k over the whole head, the
+ *     two halves of a head paired (dims i and i + hd/2), angle pos *
+ *     theta^(-2i/hd), pos = the token's 0-based index in its sequence;
+ *   - causal: the token at pos attends to positions 0 .. pos (itself
+ *     included), scores q . k_j / sqrt(hd), softmax over them;
+ *   - rounding to bf16 (nearest even) at: the attention RMSNorm output, k
+ *     after the rotation and v (the key/value cache holds bf16), and the
+ *     attention output o before W_o.  q, scores, softmax and W_o's sum stay
+ *     fp64 here.
+ */
+
+typedef struct {
+  int32_t n_heads;
+  double rope_theta;
+  const uint16_t* const* attn_norm; /* L x [d] */
+  const uint16_t* const* w_q;       /* L x [d, d] */
+  const uint16_t* const* w_k;       /* L x [d, d] */
+  const uint16_t* const* w_v;       /* L x [d, d] */
+  const uint16_t* const* w_o;       /* L x [d, d] */
+} oracle_attn_weights;
+
+/* Rotary embedding of one head vector x [hd] at position pos, in place:
+ * for i < hd/2, (x_i, x_{i+hd/2}) is turned by the angle pos * theta^(-2i/hd). */
+ORACLE_API void oracle_rope(double* x, int32_t hd, int32_t pos, double theta) {
+  const int half = hd / 2;
+  for (int i = 0; i < half; ++i) {
+    const double ang = (double)pos * pow(theta, -2.0 * (double)i / (double)hd);
+    const double c = cos(ang), s = sin(ang);
+    const double a = x[i], b = x[i + half];
+    x[i] = a * c - b * s;
+    x[i + half] = a * s + b * c;
+  }
+}
+
+/* The attention sub-block of layer l on one token at position pos, h [d]
+ * updated in place.  kc, vc: this layer's key and value cache of the token's
+ * sequence, [pos + 1, d] values of bf16 numbers; rows 0 .. pos-1 are read (the
+ * earlier tokens), row pos is written with this token's k and v.  o_out [d]
+ * (may be NULL) receives the bf16 attention output before W_o. */
+ORACLE_API void oracle_attn_block(const oracle_config* c, const oracle_attn_weights* a, int32_t l,
+                                  double* h, int32_t pos, double* kc, double* vc, double* o_out) {
+  const int d = c->hidden, H = a->n_heads, hd = d / H;
+  uint16_t* xa = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
+  double* q = (double*)malloc(sizeof(double) * (size_t)d);
+  double* k = (double*)malloc(sizeof(double) * (size_t)d);
+  double* v = (double*)malloc(sizeof(double) * (size_t)d);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  double* sc = (double*)malloc(sizeof(double) * (size_t)(pos + 1));
+  oracle_rmsnorm_bf16(h, a->attn_norm[l], d, c->rms_eps, xa);
+  for (int m = 0; m < d; ++m) {
+    double aq = 0.0, ak = 0.0, av = 0.0;
+    for (int i = 0; i < d; ++i) {
+      const double x = oracle_bf16_value(xa[i]);
+      aq += x * oracle_bf16_value(a->w_q[l][(size_t)m * d + i]);
+      ak += x * oracle_bf16_value(a->w_k[l][(size_t)m * d + i]);
+      av += x * oracle_bf16_value(a->w_v[l][(size_t)m * d + i]);
+    }
+    q[m] = aq;
+    k[m] = ak;
+    v[m] = av;
+  }
+  for (int hh = 0; hh < H; ++hh) {
+    oracle_rope(q + (size_t)hh * hd, hd, pos, a->rope_theta);
+    oracle_rope(k + (size_t)hh * hd, hd, pos, a->rope_theta);
+  }
+  for (int m = 0; m < d; ++m) {
+    kc[(size_t)pos * d + m] = q_bf16(k[m]);
+    vc[(size_t)pos * d + m] = q_bf16(v[m]);
+  }
+  const double scale = 1.0 / sqrt((double)hd);
+  const int nk = pos + 1; /* keys 0 .. pos: the earlier tokens and this one */
+  for (int hh = 0; hh < H; ++hh) {
+    const double* qh = q + (size_t)hh * hd;
+    double mx = -INFINITY;
+    for (int j = 0; j < nk; ++j) {
+      double s = 0.0;
+      for (int i = 0; i < hd; ++i) s += qh[i] * kc[(size_t)j * d + hh * hd + i];
+      sc[j] = s * scale;
+      if (sc[j] > mx) mx = sc[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < nk; ++j) {
+      sc[j] = exp(sc[j] - mx);
+      sum += sc[j];
+    }
+    for (int i = 0; i < hd; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < nk; ++j) acc += sc[j] * vc[(size_t)j * d + hh * hd + i];
+      o[hh * hd + i] = q_bf16(acc / sum);
+    }
+  }
+  if (o_out) memcpy(o_out, o, sizeof(double) * (size_t)d);
+  for (int m = 0; m < d; ++m) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i) acc += o[i] * oracle_bf16_value(a->w_o[l][(size_t)m * d + i]);
+    h[m] += acc;
+  }
+  free(xa); free(q); free(k); free(v); free(o); free(sc);
+}
+
+/* A whole sequence through the stack with attention, in order: for pos =
+ * 0 .. n-1, h = E[ids[pos]]; for each layer, the attention sub-block (with
+ * this sequence's caches) then the MoE block; targets[pos] = the greedy next
+ * id after ids[0..pos].  Optional outputs: logit_gaps [n] (top-2 gap),
+ * route_gaps [n * L] (each block's selection gap), kcache / vcache
+ * [L, n, d] (the caches after the last position; NULL: kept internally),
+ * hidden_out [n, L+1, d] (residual stream entering each block's attention,
+ * and after the last block).  Returns 0, or -1 if an id is outside [0, V). */
+ORACLE_API int32_t oracle_forward_seq(const oracle_config* c, const oracle_weights* w,
+                                      const oracle_attn_weights* a, const int32_t* ids, int32_t n,
+                                      int32_t* targets, double* logit_gaps, double* route_gaps,
+                                      double* kcache, double* vcache, double* hidden_out) {
+  const int d = c->hidden, L = c->n_layers;
+  for (int p = 0; p < n; ++p)
+    if (ids[p] < 0 || ids[p] >= c->vocab) return -1;
+  const size_t csz = (size_t)L * n * d;
+  double* kc = kcache ? kcache : (double*)malloc(sizeof(double) * csz);
+  double* vc = vcache ? vcache : (double*)malloc(sizeof(double) * csz);
+  double* h = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int p = 0; p < n; ++p) {
+    for (int i = 0; i < d; ++i) h[i] = oracle_bf16_value(w->embed[(size_t)ids[p] * d + i]);
+    for (int l = 0; l < L; ++l) {
+      if (hidden_out) memcpy(hidden_out + ((size_t)p * (L + 1) + l) * d, h, sizeof(double) * (size_t)d);
+      oracle_attn_block(c, a, l, h, p, kc + (size_t)l * n * d, vc + (size_t)l * n * d, NULL);
+      oracle_layer(c, w, l, h, NULL, NULL, NULL, route_gaps ? route_gaps + (size_t)p * L + l : NULL,
+                   NULL);
+    }
+    if (hidden_out) memcpy(hidden_out + ((size_t)p * (L + 1) + L) * d, h, sizeof(double) * (size_t)d);
+    targets[p] = oracle_head(c, w, h, NULL, logit_gaps ? logit_gaps + p : NULL);
+  }
+  free(h);
+  if (!kcache) free(kc);
+  if (!vcache) free(vc);
+  return 0;
+}

@@ -101,7 +101,46 @@ MUTANTS = {
 }
 
 
-def _run_mutant(name, old, new, tmp):
+# Mistakes in the attention of the stack with attention, run against its pins.
+ATTN_MUTANTS = {
+    "attention drops the 1/sqrt(hd) scale": ("sc[j] = s * scale;", "sc[j] = s;"),
+    "attention leaves out the current token": ("const int nk = pos + 1;", "const int nk = pos > 0 ? pos : 1;"),
+    "rope pairs neighbouring dims": (
+        "    const double a = x[i], b = x[i + half];\n    x[i] = a * c - b * s;\n    x[i + half] = a * s + b * c;",
+        "    const double a = x[2 * i], b = x[2 * i + 1];\n    x[2 * i] = a * c - b * s;\n    x[2 * i + 1] = a * s + b * c;"),
+    "rope turns the other way": ("    x[i] = a * c - b * s;\n    x[i + half] = a * s + b * c;",
+                                 "    x[i] = a * c + b * s;\n    x[i + half] = -a * s + b * c;"),
+    "rope frequency exponent halved": ("pow(theta, -2.0 * (double)i / (double)hd)",
+                                       "pow(theta, -(double)i / (double)hd)"),
+    "queries turned at the next position": ("oracle_rope(q + (size_t)hh * hd, hd, pos, a->rope_theta);",
+                                            "oracle_rope(q + (size_t)hh * hd, hd, pos + 1, a->rope_theta);"),
+    "keys turned at the next position": ("oracle_rope(k + (size_t)hh * hd, hd, pos, a->rope_theta);",
+                                         "oracle_rope(k + (size_t)hh * hd, hd, pos + 1, a->rope_theta);"),
+    "values turned like the keys": ("    oracle_rope(k + (size_t)hh * hd, hd, pos, a->rope_theta);\n  }",
+                                    "    oracle_rope(k + (size_t)hh * hd, hd, pos, a->rope_theta);\n"
+                                    "    oracle_rope(v + (size_t)hh * hd, hd, pos, a->rope_theta);\n  }"),
+    "key cache not rounded": ("kc[(size_t)pos * d + m] = q_bf16(k[m]);", "kc[(size_t)pos * d + m] = k[m];"),
+    "value cache not rounded": ("vc[(size_t)pos * d + m] = q_bf16(v[m]);", "vc[(size_t)pos * d + m] = v[m];"),
+    "attention output not rounded": ("o[hh * hd + i] = q_bf16(acc / sum);", "o[hh * hd + i] = acc / sum;"),
+    "softmax drops its normaliser": ("o[hh * hd + i] = q_bf16(acc / sum);", "o[hh * hd + i] = q_bf16(acc);"),
+    "output projection transposed": ("o[i] * oracle_bf16_value(a->w_o[l][(size_t)m * d + i])",
+                                     "o[i] * oracle_bf16_value(a->w_o[l][(size_t)i * d + m])"),
+    "value projection transposed": ("av += x * oracle_bf16_value(a->w_v[l][(size_t)m * d + i]);",
+                                    "av += x * oracle_bf16_value(a->w_v[l][(size_t)i * d + m]);"),
+    "attention residual dropped": ("    h[m] += acc;\n  }\n  free(xa);", "    h[m] = acc;\n  }\n  free(xa);"),
+    "attention attends over the other head": ("s += qh[i] * kc[(size_t)j * d + hh * hd + i];",
+                                              "s += qh[i] * kc[(size_t)j * d + ((hh + 1) % H) * hd + i];"),
+    "attention after the MoE block": (
+        "      oracle_attn_block(c, a, l, h, p, kc + (size_t)l * n * d, vc + (size_t)l * n * d, NULL);\n"
+        "      oracle_layer(c, w, l, h, NULL, NULL, NULL, route_gaps ? route_gaps + (size_t)p * L + l : NULL,\n"
+        "                   NULL);",
+        "      oracle_layer(c, w, l, h, NULL, NULL, NULL, route_gaps ? route_gaps + (size_t)p * L + l : NULL,\n"
+        "                   NULL);\n"
+        "      oracle_attn_block(c, a, l, h, p, kc + (size_t)l * n * d, vc + (size_t)l * n * d, NULL);"),
+}
+
+
+def _run_mutant(name, old, new, tmp, pins="test_oracle_pins.py"):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name!r} must occur exactly once"
     tag = "".join(c if c.isalnum() else "_" for c in name)
@@ -113,7 +152,7 @@ def _run_mutant(name, old, new, tmp):
                            "-fvisibility=hidden", "-o", so_path, c_path, "-lm"])
     env = dict(os.environ, MOE_ORACLE_LIB=so_path)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
@@ -124,3 +163,13 @@ def test_every_planted_mistake_fails_a_pin():
             results = list(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp), MUTANTS.items()))
     survivors = [n for n, rc in results if rc == 0]
     assert not survivors, f"pins did not catch: {survivors}"
+
+
+def test_every_planted_attention_mistake_fails_a_pin():
+    with tempfile.TemporaryDirectory() as tmp:
+        with fut.ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+            results = list(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp,
+                                                         pins="test_attn_oracle_pins.py"),
+                                  ATTN_MUTANTS.items()))
+    survivors = [n for n, rc in results if rc == 0]
+    assert not survivors, f"attention pins did not catch: {survivors}"
