@@ -226,6 +226,87 @@ MOE_VERIFY_API int moe_verify_draft_inputs(moe_verify_ctx* ctx, const int32_t* c
 MOE_VERIFY_API int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns,
                                                  void* cuda_stream);
 
+/* ----------------------------------------------------------------------
+ * The stack with attention (NEXT step after the verify path above).  The
+ * pages name the decoder ("Jina AI Releases jina-ocr-v1, a 3.4B MoE Document
+ * Parser With Built-In Speculative Decoding", architecture paragraph: 12
+ * layers, position limit 32,768) but give no attention shape; the reading
+ * implemented here: each block is pre-norm multi-head attention, then the MoE
+ * block,
+ *   h += W_o . attn(bf16(RMSNorm_a(h) * g_a));   then the MoE block above,
+ * with n_heads heads of width hd = d / n_heads, no biases, rotary position
+ * embedding on q and k (dims i and i + hd/2 of a head turned by the angle
+ * pos * theta^(-2i/hd), pos = the token's 0-based index in its sequence),
+ * causal attention over positions 0 .. pos with scores q . k / sqrt(hd), and
+ * bf16 (nearest even) at the attention RMSNorm output, at k (after the
+ * rotation) and v (the key/value cache is bf16), and at the attention output
+ * before W_o.  With attention a target depends on the sequence's prefix: the
+ * library keeps, per sequence slot b < max_batch, the keys and values of
+ * positions 0 .. max_pos-1 of every layer, head-major: element (l, b, head,
+ * pos, i) of the key (value) cache at (((l * max_batch + b) * n_heads + head)
+ * * max_pos + pos) * hd + i.
+ * -------------------------------------------------------------------- */
+typedef struct {
+  int32_t n_heads;  /* >= 1, hd = d / n_heads one of 8, 16, 32, 64, 128 */
+  int32_t max_pos;  /* positions held per sequence slot: 1..32768 */
+  float rope_theta; /* > 1 (10000) */
+} moe_verify_attn_config;
+
+typedef struct {                  /* HOST arrays of n_layers device pointers, bf16 */
+  const void* const* attn_norm;   /* L x [d] gain of the attention RMSNorm */
+  const void* const* w_q;         /* L x [d, d] */
+  const void* const* w_k;         /* L x [d, d] */
+  const void* const* w_v;         /* L x [d, d] */
+  const void* const* w_o;         /* L x [d, d] */
+} moe_verify_attn_weights;
+
+/* moe_verify_init for the stack with attention: the same config and MoE
+ * weights, plus the attention's shape and weights (copied and repacked: the
+ * caller's buffers may be freed after the call); allocates the key/value cache
+ * of max_batch sequence slots x max_pos positions x n_layers (bf16, 2 x L x
+ * max_batch x max_pos x d x 2 bytes, zeroed) and a rotary table (max_pos x
+ * hd/2 x 8 bytes).  Returns MOE_VERIFY_ERR_UNSUPPORTED for a head width other
+ * than 8, 16, 32, 64 or 128.  The context then runs moe_verify_step_attn
+ * (moe_verify_step, moe_verify_layer, moe_verify_decode_host and
+ * moe_verify_draft refuse it with MOE_VERIFY_ERR_ARG); moe_verify_accept,
+ * moe_verify_sync_status, the timing calls, moe_verify_set_grid and
+ * moe_verify_destroy work as for any context. */
+MOE_VERIFY_API int moe_verify_init_attn(const moe_verify_config* config,
+                                        const moe_verify_weights* weights,
+                                        const moe_verify_attn_config* attn,
+                                        const moe_verify_attn_weights* attn_weights,
+                                        void* cuda_stream, moe_verify_ctx** out);
+
+/* Greedy verification with attention.  Sequence b (slot b of the cache) has
+ * its last committed token at position positions[b] (device int32, >= 0): its
+ * verify tokens [context_ids[b], draft_ids[b, 0..K-1]] take positions
+ * positions[b] .. positions[b] + K, their keys and values are written there,
+ * and each attends to positions 0 .. its own.  Positions below positions[b]
+ * must hold the sequence's earlier tokens' keys and values (written by earlier
+ * calls; a first call at position 0 needs none).  After moe_verify_accept with
+ * n accepted drafts the cache is valid through position positions[b] + n, and
+ * the next call for the sequence passes positions[b] + n + 1 (its context id
+ * the committed bonus token).  A prompt is taken in by calls whose drafts are
+ * the prompt's next tokens: the cache then holds the prompt's tokens through
+ * positions[b] + K whatever the targets.  Outputs and limits as
+ * moe_verify_step (probe->hidden, when given, receives [2L + 1, T, d]: row 2l
+ * the residual stream entering block l's attention, row 2l + 1 entering its
+ * MoE part, row 2L after the last block).
+ * A sequence with positions[b] < 0 or positions[b] + K >= max_pos sets the
+ * sticky MOE_VERIFY_ERR_ID_RANGE flag, writes nothing to the cache and gets
+ * targets -1.  Asynchronous on cuda_stream; capturable. */
+MOE_VERIFY_API int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids,
+                                        const int32_t* draft_ids, const int32_t* positions,
+                                        int32_t B, int32_t K, int32_t* target_ids,
+                                        const moe_verify_probe* probe, void* cuda_stream);
+
+/* Diagnostic: the device address of the key/value cache of a context with
+ * attention, for reading it: *k_cache and *v_cache receive bf16 arrays
+ * [L, max_batch, n_heads, max_pos, hd] in the layout above.  The memory belongs
+ * to the context.  Returns MOE_VERIFY_ERR_ARG for a context without attention. */
+MOE_VERIFY_API int moe_verify_kv_cache(moe_verify_ctx* ctx, const void** k_cache,
+                                       const void** v_cache);
+
 /* Waits for the device, then returns and clears the sticky device error:
  * MOE_VERIFY_OK, MOE_VERIFY_ERR_ID_RANGE, MOE_VERIFY_ERR_TIMEOUT or
  * MOE_VERIFY_ERR_CUDA. */
@@ -257,7 +338,8 @@ MOE_VERIFY_API uint64_t moe_verify_device_bytes(const moe_verify_config* config)
  * and reports the sums since the last reset, in milliseconds, and the launch
  * counts:
  *   ms[0], n[0]: expert FFN (gate/up + SwiGLU + down + weighted combine)
- *   ms[1], n[1]: unused (0)
+ *   ms[1], n[1]: attention sub-block (attention RMSNorm, q/k/v and output
+ *                projections, attention; contexts with attention only)
  *   ms[2], n[2]: lm_head + argmax        ms[3], n[3]: routing + final RMSNorm
  * reset != 0 clears the sums afterwards. */
 MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
@@ -270,7 +352,9 @@ MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] h
  * not depend on it, bit for bit: fewer CTAs than SMs is what a context that
  * holds only part of the GPU runs with, and more CTAs than fit on the GPU at
  * once shows that no CTA waits for one that has not started (every expert-FFN
- * work item is claimed in order by a running CTA).  Host-buffer decode graphs
+ * work item is claimed in order by a running CTA).  With attention it also
+ * sets the CTAs of the projections (at most one per work item) and of the
+ * attention (default 4 per SM).  Host-buffer decode graphs
  * already captured keep the grid they were captured with. */
 MOE_VERIFY_API int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas);
 

@@ -31,7 +31,8 @@ EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_veri
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
             "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc",
             "moe_verify_check_bounded_wait", "moe_verify_draft", "moe_verify_draft_inputs",
-            "moe_verify_set_grid", "moe_verify_set_stamps")
+            "moe_verify_set_grid", "moe_verify_set_stamps", "moe_verify_init_attn",
+            "moe_verify_step_attn", "moe_verify_kv_cache")
 
 
 class Config(ctypes.Structure):
@@ -45,6 +46,14 @@ class Weights(ctypes.Structure):
     _fields_ = [("embed", _P), ("final_norm", _P), ("lm_head", _P), ("norm", _P),
                 ("router", _P), ("router_bias", _P), ("w_gate", _P), ("w_up", _P),
                 ("w_down", _P), ("s_gate", _P), ("s_up", _P), ("s_down", _P)]
+
+
+class AttnConfig(ctypes.Structure):
+    _fields_ = [("n_heads", _i32), ("max_pos", _i32), ("rope_theta", ctypes.c_float)]
+
+
+class AttnWeights(ctypes.Structure):
+    _fields_ = [("attn_norm", _P), ("w_q", _P), ("w_k", _P), ("w_v", _P), ("w_o", _P)]
 
 
 class Probe(ctypes.Structure):
@@ -105,6 +114,12 @@ def load(build_if_missing: bool = True):
     L.moe_verify_set_grid.argtypes = [_P, _i32]
     L.moe_verify_set_stamps.restype = _i32
     L.moe_verify_set_stamps.argtypes = [_P, _P]
+    L.moe_verify_init_attn.restype = _i32
+    L.moe_verify_init_attn.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(_P)]
+    L.moe_verify_step_attn.restype = _i32
+    L.moe_verify_step_attn.argtypes = [_P, _P, _P, _P, _i32, _i32, _P, _P, _P]
+    L.moe_verify_kv_cache.restype = _i32
+    L.moe_verify_kv_cache.argtypes = [_P, ctypes.POINTER(_P), ctypes.POINTER(_P)]
     L.moe_verify_greedy_head_noalloc.restype = _i32
     L.moe_verify_greedy_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P,
                                                  _P]
@@ -187,14 +202,31 @@ def weights_to_device(w: Dict[str, np.ndarray], device="cuda") -> Dict[str, obje
     return out
 
 
-class MoeVerify:
-    """One library context: weights and workspace on the current CUDA device."""
+class _DeviceArray:
+    """A raw device allocation seen through the CUDA array interface (int16
+    elements), for a tensor view that does not own the memory."""
 
-    def __init__(self, cfg, weights: Dict[str, object], max_batch: int, max_k: int, stream=None):
+    def __init__(self, ptr: int, shape):
+        self.__cuda_array_interface__ = {"shape": tuple(int(x) for x in shape), "typestr": "<i2",
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+class MoeVerify:
+    """One library context: weights and workspace on the current CUDA device.
+    A shape record with n_heads > 0 makes a context of the stack with
+    attention (moe_verify_init_attn), whose key/value cache holds max_pos
+    positions per sequence slot."""
+
+    def __init__(self, cfg, weights: Dict[str, object], max_batch: int, max_k: int, stream=None,
+                 max_pos: int = 0):
         import torch
         self.lib = load()
         self.cfg = cfg
         self.max_batch, self.max_k = int(max_batch), int(max_k)
+        self.attn = getattr(cfg, "n_heads", 0) > 0
+        self.max_pos = int(max_pos)
+        if self.attn and self.max_pos < 1:
+            raise ValueError("max_pos: the positions held per sequence are needed with attention")
         self._c = make_config(cfg, max_batch, max_k)
         dw = {k: (v if isinstance(v, torch.Tensor) else None) for k, v in weights.items()}
         if any(v is None for v in dw.values()):
@@ -215,10 +247,20 @@ class MoeVerify:
                     per_layer("w_gate"), per_layer("w_up"), per_layer("w_down"),
                     per_layer("s_gate"), per_layer("s_up"), per_layer("s_down"))
         h = _P()
-        rc = self.lib.moe_verify_init(ctypes.byref(self._c), ctypes.byref(W),
-                                      _stream_handle(stream), ctypes.byref(h))
-        if rc != OK:
-            raise MoeVerifyError(rc, "moe_verify_init")
+        if self.attn:
+            A = AttnConfig(int(cfg.n_heads), self.max_pos, float(cfg.rope_theta))
+            AW = AttnWeights(per_layer("attn_norm"), per_layer("w_q"), per_layer("w_k"),
+                             per_layer("w_v"), per_layer("w_o"))
+            rc = self.lib.moe_verify_init_attn(ctypes.byref(self._c), ctypes.byref(W),
+                                               ctypes.byref(A), ctypes.byref(AW),
+                                               _stream_handle(stream), ctypes.byref(h))
+            if rc != OK:
+                raise MoeVerifyError(rc, "moe_verify_init_attn")
+        else:
+            rc = self.lib.moe_verify_init(ctypes.byref(self._c), ctypes.byref(W),
+                                          _stream_handle(stream), ctypes.byref(h))
+            if rc != OK:
+                raise MoeVerifyError(rc, "moe_verify_init")
         self.handle = h
         del keep, dw
 
@@ -243,6 +285,46 @@ class MoeVerify:
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_step")
         return target_ids
+
+    def step_attn(self, context_ids, draft_ids, positions, target_ids=None,
+                  probe: Optional[Probe] = None, stream=None):
+        """moe_verify_step_attn: positions [B] int32 (device) is each
+        sequence's position of its context token."""
+        import torch
+        if getattr(context_ids, "ndim", 0) != 1:
+            raise ValueError("context_ids: a 1-D tensor [B] is expected")
+        context_ids = _dev_i32(context_ids, "context_ids")
+        B = context_ids.shape[0]
+        K = 0 if draft_ids is None else draft_ids.shape[1]
+        if K > 0:
+            _dev_i32(draft_ids, "draft_ids", (B, K))
+        _dev_i32(positions, "positions", (B,))
+        if target_ids is None:
+            target_ids = torch.empty((B, K + 1), dtype=torch.int32, device=context_ids.device)
+        _dev_i32(target_ids, "target_ids", (B, K + 1))
+        rc = self.lib.moe_verify_step_attn(self.handle, _ptr(context_ids),
+                                           _ptr(draft_ids) if K > 0 else None, _ptr(positions), B,
+                                           K, _ptr(target_ids),
+                                           ctypes.byref(probe) if probe is not None else None,
+                                           _stream_handle(stream))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_step_attn")
+        return target_ids
+
+    def kv_cache(self):
+        """moe_verify_kv_cache: (keys, values) as bf16 tensor views [L,
+        max_batch, n_heads, max_pos, head width] of the context's cache (valid
+        while the context lives)."""
+        import torch
+        kp, vp = _P(), _P()
+        rc = self.lib.moe_verify_kv_cache(self.handle, ctypes.byref(kp), ctypes.byref(vp))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_kv_cache")
+        c = self.cfg
+        shape = (c.n_layers, self.max_batch, c.n_heads, self.max_pos, c.hidden // c.n_heads)
+        k = torch.as_tensor(_DeviceArray(kp.value, shape), device="cuda").view(torch.bfloat16)
+        v = torch.as_tensor(_DeviceArray(vp.value, shape), device="cuda").view(torch.bfloat16)
+        return k, v
 
     def accept(self, draft_ids, target_ids, committed=None, accept_len=None, stream=None):
         import torch
@@ -424,14 +506,17 @@ def check_bounded_wait(limit_ns: int, stream=None):
 
 def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logits: bool = False,
                device="cuda"):
-    """Allocate probe buffers; returns (Probe struct, dict of tensors)."""
+    """Allocate probe buffers; returns (Probe struct, dict of tensors).  For
+    a shape record with attention the hidden states are [2L + 1, T, d]
+    (entering each block's attention and its MoE part, and after the last)."""
     import torch
     t = {}
+    rows = 2 * L + 1 if getattr(cfg, "n_heads", 0) > 0 else L + 1
     if topk:
         t["topk_idx"] = torch.full((L, T, cfg.top_k), -7, dtype=torch.int32, device=device)
         t["topk_w"] = torch.zeros((L, T, cfg.top_k), dtype=torch.float32, device=device)
     if hidden:
-        t["hidden"] = torch.zeros((L + 1, T, cfg.hidden), dtype=torch.float32, device=device)
+        t["hidden"] = torch.zeros((rows, T, cfg.hidden), dtype=torch.float32, device=device)
     if logits:
         t["logits"] = torch.zeros((T, cfg.vocab), dtype=torch.float32, device=device)
     p = Probe(_ptr(t.get("topk_idx")), _ptr(t.get("topk_w")), _ptr(t.get("hidden")),
@@ -439,5 +524,6 @@ def make_probe(L: int, T: int, cfg, topk: bool = True, hidden: bool = True, logi
     return p, t
 
 
-__all__ = ["load", "MoeVerify", "MoeVerifyError", "Probe", "make_probe", "check_config",
+__all__ = ["load", "MoeVerify", "MoeVerifyError", "Probe", "AttnConfig", "AttnWeights",
+           "make_probe", "check_config",
            "device_bytes", "strerror", "weights_to_device", "check_bounded_wait", "EXPORTED"]

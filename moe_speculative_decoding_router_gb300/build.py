@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmoe_verify.so")
-SOURCES = ["route.cu", "gemm.cu", "misc.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["route.cu", "gemm.cu", "misc.cu", "api.cu", "noalloc.cu", "attn.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",

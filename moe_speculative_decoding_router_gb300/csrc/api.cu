@@ -2,6 +2,7 @@
 // library-owned weights and workspace, TMA descriptors and the launch order
 // of one verify step.
 #include <cudaTypedefs.h>
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -53,6 +54,15 @@ struct moe_verify_ctx {
   cudaStream_t capture_stream = nullptr;
   // CTAs of the persistent kernels (expert FFN, lm_head); 0: one per SM
   int grid_ctas = 0;
+  // the stack with attention (moe_verify_init_attn)
+  bool attn = false;
+  int H = 0, hd = 0, max_pos = 0, rows_qkv = 0, cap_pairs = 0, attn_target = 0;
+  __nv_bfloat16 *w_qkv = nullptr, *w_o = nullptr, *kcache = nullptr, *vcache = nullptr,
+                *xa = nullptr, *obuf = nullptr;
+  float *attn_gain = nullptr, *qbuf = nullptr, *part = nullptr;
+  float2* rope = nullptr;
+  int32_t *arrive = nullptr, *plan = nullptr;
+  CUtensorMap map_qkv, map_wo;
   // profiling
   unsigned long long* stamps = nullptr;  // caller-owned [2L + 1][kStampSlots] or nullptr
   bool timing = false;
@@ -699,7 +709,7 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
 int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
                     int32_t B, int32_t K, int32_t* target_ids, const moe_verify_probe* probe,
                     void* cuda_stream) {
-  if (!ctx || !context_ids || !target_ids) return MOE_VERIFY_ERR_ARG;
+  if (!ctx || !context_ids || !target_ids || ctx->attn) return MOE_VERIFY_ERR_ARG;
   if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
   if (K > 0 && !draft_ids) return MOE_VERIFY_ERR_ARG;
   return enqueue_step(ctx, context_ids, draft_ids, B, K, target_ids, probe,
@@ -727,7 +737,7 @@ int moe_verify_accept(moe_verify_ctx* ctx, const int32_t* draft_ids, const int32
 
 int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32_t T, void* h_out,
                      const moe_verify_probe* probe, void* cuda_stream) {
-  if (!ctx || !h_in || !h_out) return MOE_VERIFY_ERR_ARG;
+  if (!ctx || !h_in || !h_out || ctx->attn) return MOE_VERIFY_ERR_ARG;
   if (layer < 0 || layer >= ctx->L || T < 1 || T > ctx->T_max) return MOE_VERIFY_ERR_ARG;
   if (!aligned16(h_in) || !aligned16(h_out)) return MOE_VERIFY_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -805,7 +815,8 @@ cudaGraphExec_t decode_graph(moe_verify_ctx* ctx, int B, int K) {
 int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
                            const int32_t* host_draft_ids, int32_t B, int32_t K,
                            int32_t* host_committed, int32_t* host_accept_len, void* cuda_stream) {
-  if (!ctx || !host_context_ids || !host_committed || !host_accept_len) return MOE_VERIFY_ERR_ARG;
+  if (!ctx || !host_context_ids || !host_committed || !host_accept_len || ctx->attn)
+    return MOE_VERIFY_ERR_ARG;
   if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
   if (K > 0 && !host_draft_ids) return MOE_VERIFY_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -840,7 +851,7 @@ int moe_verify_draft_inputs(moe_verify_ctx* ctx, const int32_t* committed,
 
 int moe_verify_draft(moe_verify_ctx* ctx, const float* h_prev, const int32_t* t_prev, int32_t B,
                      int32_t K, int32_t* drafts, float* hidden_out, void* cuda_stream) {
-  if (!ctx || !h_prev || !t_prev || !drafts) return MOE_VERIFY_ERR_ARG;
+  if (!ctx || !h_prev || !t_prev || !drafts || ctx->attn) return MOE_VERIFY_ERR_ARG;
   if (ctx->L != 1) return MOE_VERIFY_ERR_ARG;
   if (B < 1 || B > ctx->T_max || K < 1 || K > 15) return MOE_VERIFY_ERR_ARG;
   if (!aligned16(h_prev) || (hidden_out && !aligned16(hidden_out))) return MOE_VERIFY_ERR_ARG;
@@ -865,6 +876,238 @@ int moe_verify_draft(moe_verify_ctx* ctx, const float* h_prev, const int32_t* t_
     ids = ctx->io_targets;
   }
   return MOE_VERIFY_OK;
+}
+
+int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weights* weights,
+                         const moe_verify_attn_config* attn,
+                         const moe_verify_attn_weights* aw, void* cuda_stream,
+                         moe_verify_ctx** out) {
+  if (!out) return MOE_VERIFY_ERR_ARG;
+  *out = nullptr;
+  if (!attn || !aw) return MOE_VERIFY_ERR_ARG;
+  int rc = check(config);
+  if (rc != MOE_VERIFY_OK) return rc;
+  const int d = config->hidden, L = config->n_layers;
+  if (attn->n_heads < 1 || d % attn->n_heads != 0) return MOE_VERIFY_ERR_ARG;
+  const int hd = d / attn->n_heads;
+  if (attn->max_pos < 1 || attn->max_pos > 32768) return MOE_VERIFY_ERR_ARG;
+  if (!(attn->rope_theta > 1.f) || !(attn->rope_theta < 1e30f)) return MOE_VERIFY_ERR_ARG;
+  if (!aw->attn_norm || !aw->w_q || !aw->w_k || !aw->w_v || !aw->w_o) return MOE_VERIFY_ERR_ARG;
+  for (int l = 0; l < L; ++l)
+    if (!aw->attn_norm[l] || !aw->w_q[l] || !aw->w_k[l] || !aw->w_v[l] || !aw->w_o[l])
+      return MOE_VERIFY_ERR_ARG;
+  if (hd != 8 && hd != 16 && hd != 32 && hd != 64 && hd != 128) return MOE_VERIFY_ERR_UNSUPPORTED;
+  rc = moe_verify_init(config, weights, cuda_stream, out);
+  if (rc != MOE_VERIFY_OK) return rc;
+  moe_verify_ctx* c = *out;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  auto fail = [&](int code) {
+    moe_verify_destroy(c);
+    *out = nullptr;
+    return code;
+  };
+  c->attn = true;
+  c->H = attn->n_heads;
+  c->hd = hd;
+  c->max_pos = attn->max_pos;
+  c->rows_qkv = round_up(3 * d, 128);
+  const int Bmax = config->max_batch, K1max = config->max_k + 1;
+  c->attn_target = 4 * c->num_sms;
+  // (sequence, split) pairs: at most B + total keys / split width, the width
+  // either >= total keys x H / target or 1024
+  c->cap_pairs = Bmax + (c->attn_target + c->H - 1) / c->H +
+                 Bmax * ((c->max_pos + mv::kAttnMaxSplit - 1) / mv::kAttnMaxSplit) + 1;
+  const uint64_t cache = (uint64_t)L * Bmax * c->max_pos * d * 2;
+  const uint64_t act16 = (uint64_t)round_up(c->T_max, 16) * d * 2;
+  int e = 0;
+  if ((e = dalloc(c, &c->w_qkv, (uint64_t)L * c->rows_qkv * d * 2)) ||
+      (e = dalloc(c, &c->w_o, (uint64_t)L * c->d_pad * d * 2)) ||
+      (e = dalloc(c, &c->attn_gain, (uint64_t)L * d * 4)) ||
+      (e = dalloc(c, &c->rope, (uint64_t)c->max_pos * (hd / 2) * sizeof(float2))) ||
+      (e = dalloc(c, &c->kcache, cache)) || (e = dalloc(c, &c->vcache, cache)) ||
+      (e = dalloc(c, &c->xa, act16)) || (e = dalloc(c, &c->obuf, act16)) ||
+      (e = dalloc(c, &c->qbuf, (uint64_t)c->T_max * d * 4)) ||
+      (e = dalloc(c, &c->part, (uint64_t)c->cap_pairs * c->H * K1max * (hd + 2) * 4)) ||
+      (e = dalloc(c, &c->arrive, (uint64_t)Bmax * c->H * 4)) ||
+      (e = dalloc(c, &c->plan, (uint64_t)(2 + 2 * c->cap_pairs) * 4)))
+    return fail(e);
+#define CKA(x)                                               \
+  do {                                                       \
+    if ((x) != cudaSuccess) return fail(MOE_VERIFY_ERR_CUDA); \
+  } while (0)
+  CKA(cudaMemsetAsync(c->kcache, 0, cache, s));
+  CKA(cudaMemsetAsync(c->vcache, 0, cache, s));
+  CKA(cudaMemsetAsync(c->xa, 0, act16, s));
+  CKA(cudaMemsetAsync(c->obuf, 0, act16, s));
+  CKA(cudaMemsetAsync(c->arrive, 0, (size_t)Bmax * c->H * 4, s));
+  CKA(cudaMemsetAsync(c->plan, 0, (size_t)(2 + 2 * c->cap_pairs) * 4, s));
+  CKA(cudaMemsetAsync(c->w_o, 0, (size_t)L * c->d_pad * d * 2, s));
+  for (int l = 0; l < L; ++l) {
+    CKA(mv::launch_repack_qkv(c->w_qkv + (size_t)l * c->rows_qkv * d,
+                              static_cast<const __nv_bfloat16*>(aw->w_q[l]),
+                              static_cast<const __nv_bfloat16*>(aw->w_k[l]),
+                              static_cast<const __nv_bfloat16*>(aw->w_v[l]), d, hd, c->rows_qkv,
+                              s));
+    CKA(cudaMemcpyAsync(c->w_o + (size_t)l * c->d_pad * d, aw->w_o[l], (size_t)d * d * 2,
+                        cudaMemcpyDeviceToDevice, s));
+    CKA(mv::launch_bf16_to_f32(c->attn_gain + (size_t)l * d,
+                               static_cast<const __nv_bfloat16*>(aw->attn_norm[l]), d, s));
+  }
+  // rotary table: (cos, sin) of pos * theta^(-2i/hd), computed in double
+  {
+    const int half = hd / 2;
+    std::vector<float2> tab((size_t)c->max_pos * half);
+    for (int i = 0; i < half; ++i) {
+      const double f = pow((double)attn->rope_theta, -2.0 * i / (double)hd);
+      for (int pos = 0; pos < c->max_pos; ++pos) {
+        const double a = (double)pos * f;
+        tab[(size_t)pos * half + i] = make_float2((float)cos(a), (float)sin(a));
+      }
+    }
+    CKA(cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                        s));
+    CKA(cudaStreamSynchronize(s));
+  }
+#undef CKA
+  if (encode_map(&c->map_qkv, c->w_qkv, d, (uint64_t)L * c->rows_qkv, 128) ||
+      encode_map(&c->map_wo, c->w_o, d, (uint64_t)L * c->d_pad, 128))
+    return fail(MOE_VERIFY_ERR_CUDA);
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_kv_cache(moe_verify_ctx* ctx, const void** k_cache, const void** v_cache) {
+  if (!ctx || !ctx->attn || !k_cache || !v_cache) return MOE_VERIFY_ERR_ARG;
+  *k_cache = ctx->kcache;
+  *v_cache = ctx->vcache;
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
+                         const int32_t* positions, int32_t B, int32_t K, int32_t* target_ids,
+                         const moe_verify_probe* probe, void* cuda_stream) {
+  if (!ctx || !ctx->attn || !context_ids || !positions || !target_ids) return MOE_VERIFY_ERR_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
+  if (K > 0 && !draft_ids) return MOE_VERIFY_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const int T = B * (K + 1), d = ctx->d, L = ctx->L;
+  StepShape sh;
+  if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
+  // projections: token chunks of <= 256, as even as 16-row granularity allows
+  const int n_chunks = (T + 255) / 256;
+  const int nch = round_up((T + n_chunks - 1) / n_chunks, 16);
+  CUtensorMap map_xa, map_o;
+  if (encode_map(&map_xa, ctx->xa, d, round_up(ctx->T_max, 16), (uint32_t)nch) ||
+      encode_map(&map_o, ctx->obuf, d, round_up(ctx->T_max, 16), (uint32_t)nch))
+    return MOE_VERIFY_ERR_CUDA;
+  int stages = 16;
+  while (stages > 2 && mv::proj_smem_bytes(nch, stages) > 227 * 1024) --stages;
+  mv::ProjParams pb = {};
+  pb.n_chunks = n_chunks;
+  pb.nch = nch;
+  pb.kblocks = d / 64;
+  pb.stages = stages;
+  pb.tmem_cols = pow2_at_least(2 * nch);
+  pb.T = T;
+  pb.d = d;
+  pb.K = K;
+  pb.H = ctx->H;
+  pb.hd = ctx->hd;
+  pb.max_pos = ctx->max_pos;
+  pb.Bmax = ctx->cfg.max_batch;
+  pb.status = ctx->status;
+  pb.positions = positions;
+  pb.rope = ctx->rope;
+  const size_t cache_layer = (size_t)ctx->cfg.max_batch * ctx->max_pos * d;
+  const int attn_grid = ctx->grid_ctas > 0 ? ctx->grid_ctas : ctx->attn_target;
+  // probe->hidden [2L + 1, T, d]: row 2l the residual entering block l's
+  // attention (written by its RMSNorm kernel), row 2l + 1 the residual
+  // entering its MoE part (written by the routing kernel, which indexes the
+  // probe by layer: its pointer is offset so that layer l lands on row 2l + 1)
+  moe_verify_probe route_probe = {};
+  if (probe) route_probe = *probe;
+  const bool pdl = true;
+  for (int l = 0; l < L; ++l) {
+    {
+      Timed tm(ctx, 1, s);
+      mv::AttnNormParams ap = {};
+      ap.T = T;
+      ap.B = B;
+      ap.K = K;
+      ap.d = d;
+      ap.kS = ctx->kS;
+      ap.V = ctx->V;
+      ap.H = ctx->H;
+      ap.max_pos = ctx->max_pos;
+      ap.first = l == 0 ? 1 : 0;
+      ap.eps = ctx->cfg.rms_eps;
+      ap.context_ids = context_ids;
+      ap.draft_ids = draft_ids;
+      ap.positions = positions;
+      ap.embed = ctx->embed;
+      ap.h = ctx->h;
+      ap.y = ctx->y;
+      ap.gain = ctx->attn_gain + (size_t)l * d;
+      ap.xa = ctx->xa;
+      ap.probe_hidden = (probe && probe->hidden) ? probe->hidden + (size_t)(2 * l) * T * d : nullptr;
+      ap.bad = ctx->bad;
+      ap.status = ctx->status;
+      ap.plan = ctx->plan;
+      ap.target_items = ctx->attn_target;
+      ap.cap_pairs = ctx->cap_pairs;
+      CK(mv::launch_attn_norm(ap, s, pdl));
+    }
+    {
+      Timed tm(ctx, 1, s);
+      mv::ProjParams qp = pb;
+      qp.mode = 0;
+      qp.n_items = (ctx->rows_qkv / 128) * n_chunks;
+      qp.a_row0 = l * ctx->rows_qkv;
+      qp.q = ctx->qbuf;
+      qp.kc = ctx->kcache + cache_layer * l;
+      qp.vc = ctx->vcache + cache_layer * l;
+      const int g = persistent_grid(ctx) < qp.n_items ? persistent_grid(ctx) : qp.n_items;
+      CK(mv::launch_proj(ctx->map_qkv, map_xa, qp, g, s, pdl));
+    }
+    {
+      Timed tm(ctx, 1, s);
+      mv::AttnParams at = {};
+      at.B = B;
+      at.K = K;
+      at.H = ctx->H;
+      at.hd = ctx->hd;
+      at.d = d;
+      at.max_pos = ctx->max_pos;
+      at.Bmax = ctx->cfg.max_batch;
+      at.scale_log2 = (float)(1.4426950408889634 / sqrt((double)ctx->hd));
+      at.positions = positions;
+      at.plan = ctx->plan;
+      at.q = ctx->qbuf;
+      at.kc = ctx->kcache + cache_layer * l;
+      at.vc = ctx->vcache + cache_layer * l;
+      at.o = ctx->obuf;
+      at.part = ctx->part;
+      at.arrive = ctx->arrive;
+      at.status = ctx->status;
+      CK(mv::launch_attn(at, attn_grid, s, pdl));
+    }
+    {
+      Timed tm(ctx, 1, s);
+      mv::ProjParams op = pb;
+      op.mode = 1;
+      op.n_items = (ctx->d_pad / 128) * n_chunks;
+      op.a_row0 = l * ctx->d_pad;
+      op.h = ctx->h;
+      const int g = persistent_grid(ctx) < op.n_items ? persistent_grid(ctx) : op.n_items;
+      CK(mv::launch_proj(ctx->map_wo, map_o, op, g, s, pdl));
+    }
+    if (probe && probe->hidden) route_probe.hidden = probe->hidden + (size_t)(l + 1) * T * d;
+    int rc = run_layer(ctx, l, l & 1, mv::kSrcH, sh, context_ids, draft_ids, B, K, nullptr,
+                       probe ? &route_probe : nullptr, l, s, pdl, l == L - 1, false);
+    if (rc != MOE_VERIFY_OK) return rc;
+  }
+  float* ph = (probe && probe->hidden) ? probe->hidden + (size_t)(2 * L) * T * d : nullptr;
+  return enqueue_head(ctx, T, sh, (L - 1) & 1, target_ids, ph, probe ? probe->logits : nullptr, s,
+                      pdl, false);
 }
 
 int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns, void* cuda_stream) {

@@ -1349,6 +1349,229 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   lm_finish(p, *C.abort_flag != 0, &is_last);
 }
 
+// ----------------------------------- attention projections (weight rows on M)
+//
+// [128 rows of one layer's packed q/k/v or W_o] x [a chunk of <= nch tokens],
+// K = d.  Items run tile-major (item i: tile i / n_chunks, chunk i %
+// n_chunks) in a static stride over the grid; the first ring of weight tiles
+// is loaded before the wait for the previous kernel.  Each epilogue thread
+// owns one weight row (one output feature) for all of the chunk's tokens.
+// Mode 0: rows [q | k | v]; in q and k the two dims of a rotary pair sit in
+// neighbouring rows, so the rotation of a token's pair takes one lane
+// exchange; q is stored fp32, the rotated k and v as bf16 in the cache at the
+// token's position.  Mode 1: h[t, row] += acc.
+
+struct ProjItem {
+  int tile, a_row, b_row, n;
+};
+
+__device__ __forceinline__ ProjItem proj_item(const ProjParams& p, int i) {
+  ProjItem it;
+  it.tile = i / p.n_chunks;
+  const int c = i - it.tile * p.n_chunks;
+  it.a_row = p.a_row0 + it.tile * 128;
+  it.b_row = c * p.nch;
+  it.n = min(p.nch, p.T - it.b_row);
+  return it;
+}
+
+// Rows [row0, row0 + 32) of the packed q/k/v block of one warp's epilogue:
+// the rows' part (0 q, 1 k, 2 v, 3 padding; the same for the whole warp since
+// d is a multiple of 64), and this lane's head, head dim and rotary index.
+struct QkvRow {
+  int part, head, dim, freq;
+  bool odd;
+};
+
+__device__ __forceinline__ QkvRow qkv_row(const ProjParams& p, int prow) {
+  QkvRow r;
+  r.part = prow / p.d;
+  const int f = prow - r.part * p.d;
+  r.head = f / p.hd;
+  const int w = f - r.head * p.hd;
+  r.freq = w >> 1;
+  r.odd = (w & 1) != 0;
+  r.dim = r.part < 2 ? r.freq + (r.odd ? (p.hd >> 1) : 0) : w;
+  return r;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    proj_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const ProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int stage_bytes = kStageA + p.nch * 128;
+  uint8_t* stages = smem;
+  const Ctrl C = ctrl_at(smem + (size_t)p.stages * stage_bytes, p.stages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.n_items;
+  const bool has_work = (int)blockIdx.x < n_items;
+
+  if (threadIdx.x == 0) {
+    init_ctrl(C, p.stages, 4, 1);
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (has_work && warp == 1) {
+    tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = has_work ? *C.tmem_slot : 0u;
+
+  if (has_work && warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    const uint32_t tx = (uint32_t)(kStageA + p.nch * 128);
+    int i = blockIdx.x, kb = 0;
+    ProjItem it = proj_item(p, i);
+    int pre = 0;
+    {
+      int pi = i, pk = 0;
+      ProjItem pt = it;
+      while (pre < p.stages && pi < n_items) {
+        mbar_arrive_expect_tx(&C.full[pre], tx);
+        tma_load_2d(stages + (size_t)pre * stage_bytes, &mapA, &C.full[pre], pk * 64, pt.a_row,
+                    pol_w);
+        ++pre;
+        if (++pk == p.kblocks) {
+          pk = 0;
+          pi += gridDim.x;
+          if (pi < n_items) pt = proj_item(p, pi);
+        }
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int s = 0; s < pre; ++s) {
+      tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &mapB, &C.full[s], kb * 64,
+                  it.b_row, pol_x);
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = proj_item(p, i);
+      }
+    }
+    int stage = pre, issued = pre;
+    uint32_t phase = 0;
+    if (stage == p.stages) {
+      stage = 0;
+      phase = 1;
+    }
+    bool ok = true;
+    while (i < n_items) {
+      if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + (size_t)stage * stage_bytes;
+      mbar_arrive_expect_tx(&C.full[stage], tx);
+      tma_load_2d(sa, &mapA, &C.full[stage], kb * 64, it.a_row, pol_w);
+      tma_load_2d(sa + kStageA, &mapB, &C.full[stage], kb * 64, it.b_row, pol_x);
+      ++issued;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += gridDim.x;
+        if (i < n_items) it = proj_item(p, i);
+      }
+    }
+    if (!ok) producer_drain(C, issued, p.stages);
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (has_work && warp == 1 && lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+        const ProjItem it = proj_item(p, i);
+        const int npad = (it.n + 15) & ~15;
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        if (!mma_item(C, stages, stage_bytes, p.stages, stage, phase, p.kblocks,
+                      tmem_base + (uint32_t)(buf * p.nch), umma_idesc_bf16(128, (uint32_t)npad),
+                      p.status))
+          break;
+        umma_commit(&C.tfull[buf]);
+      }
+      mma_drain(C);
+    } else if (has_work && warp >= 2) {
+      // ------------------------------------------------ epilogue warps 2..5
+      const int q = warp & 3;
+      const int K1 = p.K + 1, half = p.hd >> 1;
+      int local = 0;
+      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
+        const ProjItem it = proj_item(p, i);
+        const int npad = (it.n + 15) & ~15;
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.nch);
+        const int prow = it.tile * 128 + q * 32 + lane;  // row within this layer's block
+        const QkvRow r = qkv_row(p, prow);
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tl = c0 + j;
+            const bool valid = tl < it.n;  // the same for every lane
+            const int t = it.b_row + tl;
+            const float x = __uint_as_float(v[j]);
+            if (p.mode == 1) {
+              if (valid && prow < p.d) p.h[(size_t)t * p.d + prow] += x;
+              continue;
+            }
+            if (r.part >= 3) continue;
+            int b = 0, pos = 0;
+            bool seq_ok = false;
+            if (valid) {
+              b = t / K1;
+              const int p0 = __ldg(p.positions + b);
+              seq_ok = p0 >= 0 && p0 <= p.max_pos - K1;
+              pos = seq_ok ? p0 + (t - b * K1) : 0;
+            }
+            const size_t at = (((size_t)b * p.H + r.head) * p.max_pos + pos) * p.hd + r.dim;
+            if (r.part < 2) {
+              // rotary pair (dim i, dim i + hd/2) in lanes (2i, 2i + 1)
+              const float y = __shfl_xor_sync(0xffffffffu, x, 1);
+              const float2 cs = __ldg(p.rope + (size_t)pos * half + r.freq);
+              const float rot = r.odd ? y * cs.y + x * cs.x : x * cs.x - y * cs.y;
+              if (!valid) continue;
+              if (r.part == 0)
+                p.q[(size_t)t * p.d + r.head * p.hd + r.dim] = rot;
+              else if (seq_ok)
+                p.kc[at] = __float2bfloat16_rn(rot);
+            } else if (valid && seq_ok) {
+              p.vc[at] = __float2bfloat16_rn(x);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.tempty[buf]);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (has_work && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+  }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, bool pdl,
                            Args... args) {
@@ -1405,6 +1628,16 @@ cudaError_t launch_ffn_tokm(const CUtensorMap& map_gu256, const CUtensorMap& map
                             const FfnParams& p, int grid, cudaStream_t s, bool pdl) {
   return launch_gemm_ex(ffn_tokm_kernel, grid, ffn_tokm_smem_bytes(p.stages), s, pdl, map_gu256,
                         map_x, map_dn256, map_a, p);
+}
+
+size_t proj_smem_bytes(int nch, int stages) {
+  return 1024 /* alignment slack */ + (size_t)stages * (kStageA + (size_t)nch * 128) + kCtrlBytes;
+}
+
+cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, const ProjParams& p,
+                        int grid, cudaStream_t s, bool pdl) {
+  return launch_gemm_ex(proj_kernel, grid, proj_smem_bytes(p.nch, p.stages), s, pdl, map_w, map_x,
+                        p);
 }
 
 LmLayout lm_layout(int T) {

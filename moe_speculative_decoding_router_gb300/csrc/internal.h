@@ -22,7 +22,9 @@ constexpr uint32_t kErrInternal = 4u;
 // Sources of the residual stream entering a routing kernel.
 // kSrcEmbedAdd: the running state h (written by the previous launch) plus
 // the embedding of each sequence's token (the draft head's step input).
-enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2, kSrcEmbedAdd = 3 };
+// kSrcH: h as it stands (the stack with attention: the attention sub-block
+// has already added its output to h).
+enum RouteSrc : int { kSrcEmbed = 0, kSrcBf16 = 1, kSrcCombine = 2, kSrcEmbedAdd = 3, kSrcH = 4 };
 
 struct RouteParams {
   int T, B, K;          // verify tokens, sequences, drafts per sequence
@@ -131,6 +133,79 @@ struct GemmParams {
   unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
+// ------------------------------------------------ the stack with attention
+//
+// Per block: attn_norm (residual update + attention RMSNorm), the q/k/v
+// projection (RoPE and the key/value cache write in its epilogue), the
+// attention over the cache, the output projection added into h, then the
+// routing (source kSrcH) and the expert FFN as without attention.
+
+// Residual stream entering block l's attention and its normalised bf16 row.
+// Layer 0 also checks the ids and the positions (bad[t] = 1 and the status
+// bit for a token outside [0, V) or a sequence outside [0, max_pos - K)) and
+// lays out the attention's work items for the step.
+struct AttnNormParams {
+  int T, B, K, d, kS, V, H, max_pos;
+  int first;                   // 1: layer 0 (h = embedding of the token), 0: h += combine(y)
+  float eps;
+  const int32_t* context_ids;
+  const int32_t* draft_ids;
+  const int32_t* positions;    // [B]
+  const __nv_bfloat16* embed;  // [V, d]
+  float* h;                    // [T, d]
+  const float* y;              // [T, kS, d] expert outputs of the previous block
+  const float* gain;           // [d]
+  __nv_bfloat16* xa;           // [T, d] bf16(RMSNorm_a(h) * g_a)
+  float* probe_hidden;         // [T, d] or nullptr
+  int32_t* bad;                // [T]
+  uint32_t* status;
+  // work items of the attention (written by layer 0's block 0): plan[0] =
+  // keys per split, plan[1] = (sequence, split) pairs, then the pairs as
+  // plan[2 + 2i] = sequence, plan[3 + 2i] = split
+  int32_t* plan;
+  int target_items;            // wanted (sequence, split, head) items
+  int cap_pairs;               // room in plan for pairs
+};
+
+// Weight-major projection on the tensor cores: items are (128 weight rows,
+// chunk of <= nch tokens); mode 0 is the packed q/k/v projection (rows
+// [q | k | v], q and k rows of a head ordered (0, hd/2, 1, hd/2 + 1, ...) so
+// that each rotary pair sits in neighbouring lanes), mode 1 W_o added into h.
+struct ProjParams {
+  int mode;
+  int n_items, n_chunks, nch;  // weight tiles x token chunks; tokens per chunk
+  int a_row0;                  // first weight row of this layer in the tensor map
+  int kblocks, stages, tmem_cols;
+  int T, d, K, H, hd, max_pos, Bmax;
+  uint32_t* status;
+  const int32_t* positions;    // [B] (mode 0)
+  const float2* rope;          // [max_pos, hd/2] (cos, sin) (mode 0)
+  float* q;                    // [T, d] rotated q (mode 0)
+  __nv_bfloat16* kc;           // this layer's key cache [Bmax, H, max_pos, hd] (mode 0)
+  __nv_bfloat16* vc;           // this layer's value cache (mode 0)
+  float* h;                    // [T, d] (mode 1)
+};
+
+// Causal attention of the step's tokens over their sequences' caches.  Items
+// (sequence, split of <= plan[0] keys, head); a sequence's keys 0 .. pos + K
+// in splits, each split's unnormalised result merged by the last of its
+// sequence's and head's items to finish.
+struct AttnParams {
+  int B, K, H, hd, d, max_pos, Bmax;
+  float scale_log2;            // log2(e) / sqrt(hd)
+  const int32_t* positions;    // [B]
+  const int32_t* plan;
+  const float* q;              // [T, d]
+  const __nv_bfloat16* kc;     // this layer's caches [Bmax, H, max_pos, hd]
+  const __nv_bfloat16* vc;
+  __nv_bfloat16* o;            // [T, d] bf16 attention output
+  float* part;                 // [cap items, K+1, hd + 2] split results (m, l, acc)
+  int32_t* arrive;             // [Bmax, H] finished splits (zero on entry; the merger resets)
+  uint32_t* status;
+};
+constexpr int kAttnMinSplit = 64;    // keys per split: at least
+constexpr int kAttnMaxSplit = 1024;  // and at most
+
 struct AcceptParams {
   int B, K, V;
   const int32_t* drafts;
@@ -182,6 +257,18 @@ cudaError_t launch_draft_inputs(const float* h, const int32_t* committed, const 
 // dst[b * stride + col] = src[b], b < B.
 cudaError_t launch_scatter_column(const int32_t* src, int B, int32_t* dst, int stride, int col,
                                   cudaStream_t s);
+
+// The stack with attention.
+cudaError_t launch_attn_norm(const AttnNormParams& p, cudaStream_t s, bool pdl);
+size_t proj_smem_bytes(int nch, int stages);
+cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, const ProjParams& p,
+                        int grid, cudaStream_t s, bool pdl);
+size_t attn_smem_bytes(int nq, int hd);
+cudaError_t launch_attn(const AttnParams& p, int grid, cudaStream_t s, bool pdl);
+// dst [rows_pad, d] = the packed q/k/v rows of one layer (zero past 3d).
+cudaError_t launch_repack_qkv(__nv_bfloat16* dst, const __nv_bfloat16* wq,
+                              const __nv_bfloat16* wk, const __nv_bfloat16* wv, int d, int hd,
+                              int rows_pad, cudaStream_t s);
 
 // Self-check of the bounded waits (see moe_verify_check_bounded_wait).
 cudaError_t run_bounded_wait_check(uint64_t limit_ns, cudaStream_t s, unsigned long long* host_out,

@@ -132,6 +132,14 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
           }
         }
       }
+    } else if (SRC == kSrcH) {
+      // h as the previous launch (the attention's output projection) left it
+      for (int c = tid; c < nc; c += kRouteThreads) {
+        const float4 v = __ldcg(hg + c);
+        hx[c] = v;
+        if (hp) hp[c] = v;
+        ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
     } else {
       const uint2* src;
       if (SRC == kSrcEmbed || SRC == kSrcEmbedAdd) {
@@ -568,6 +576,7 @@ cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int gr
     case kSrcEmbed: return launch_route_src<kSrcEmbed>(map_wr, p, grid, smem, s, pdl);
     case kSrcBf16: return launch_route_src<kSrcBf16>(map_wr, p, grid, smem, s, pdl);
     case kSrcEmbedAdd: return launch_route_src<kSrcEmbedAdd>(map_wr, p, grid, smem, s, pdl);
+    case kSrcH: return launch_route_src<kSrcH>(map_wr, p, grid, smem, s, pdl);
     default: return launch_route_src<kSrcCombine>(map_wr, p, grid, smem, s, pdl);
   }
 }

@@ -198,3 +198,134 @@ def check_tokens(orc, ids, gpu_targets, probe_idx=None, probe_w=None, probe_hidd
 def record(label, **counts):
     """Adds counts of a test that does not go through check_tokens."""
     RECORD.append(dict(label=label, **counts))
+
+
+# The stack with attention, one block teacher-forced: the attention sub-block
+# adds bf16 roundings of its own (k, v and the attention output), each a
+# last-bit difference at most between the two sides, so a block keeps the
+# tolerance of BLOCK_REL.  A cached key or value is the bf16 rounding of a sum
+# whose inputs (the bf16-normalised row) may already differ by a last bit
+# between the sides, which moves the sum by up to a small fraction of the
+# row's scale (not of the element's: an element near zero has a large
+# relative error); the rounding then adds at most one bf16 step of the
+# element (2^-7 of its magnitude).  So |gpu - oracle| <= KV_STEP |oracle| +
+# rel * max|oracle row|, rel = BLOCK_REL teacher-forced.
+KV_STEP = 2.0 ** -7
+# The attention sub-block alone, teacher-forced, on the same grounds as a MoE
+# block: its sides differ by last-bit flips of bf16 roundings (the normalised
+# row, k, v, the attention output), so it keeps BLOCK_REL.  (Measured at full
+# size: max 2.2e-4, median 7e-7; the MoE part on the GPU's post-attention
+# residual: max 9.3e-4.)
+ATTN_REL = BLOCK_REL
+
+
+def kv_within(g, o, rel):
+    """Cached key/value rows g (GPU) and o (oracle), [..., n] float64: the
+    elements outside the bound above (an empty array when all are inside)."""
+    scale = np.max(np.abs(o), axis=-1, keepdims=True)
+    return np.nonzero(np.abs(g - o) > KV_STEP * np.abs(o) + rel * scale)
+
+
+def _bf16_to_f64(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16 or a.dtype == np.int16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(a, dtype=np.float64)
+
+
+def check_attn_tokens(orc, ids, seq, pos, gpu_targets, probe_idx, probe_w, probe_hidden, kcache,
+                      vcache, sample=None, nthreads=None, label=None):
+    """Teacher-forced check of the stack with attention.
+
+    ids[t], seq[t], pos[t]: token t's id, sequence slot and position;
+    probe_* as for check_tokens, the hidden states [2L + 1, T, d] (entering
+    each block's attention and its MoE part, and after the last block);
+    kcache / vcache: the GPU's caches after the step as bf16 bit patterns [L,
+    slots, heads, max_pos, hd].  For each block the oracle's attention
+    sub-block runs on the GPU's residual and the GPU's cached keys and values
+    of positions < pos (its own key and value of pos are compared with the
+    GPU's) and its output is compared with the GPU's residual entering the MoE
+    part, which the oracle's MoE block then runs on along the GPU's routing;
+    the final argmax is checked on the GPU's final residual.  Returns the
+    counts (also appended to RECORD)."""
+    T = len(ids)
+    sample = list(range(T) if sample is None else sample)
+    nthreads = nthreads or threads()
+    c = orc.cfg
+    L, d = c.n_layers, c.hidden
+
+    def cache_rows(arr, l, b, n):
+        # [heads, n, hd] -> [n, d]
+        x = _bf16_to_f64(arr[l, b, :, :n, :])
+        return np.ascontiguousarray(x.transpose(1, 0, 2).reshape(n, d))
+
+    def one(t):
+        out = {"route_ties": 0, "logit_tie": 0, "kv_steps": 0, "kv_vals": 0,
+               "max_block_rel": 0.0, "max_attn_rel": 0.0, "fail": None}
+        x, b, p = int(ids[t]), int(seq[t]), int(pos[t])
+        H = np.asarray(probe_hidden[:, t, :], dtype=np.float64)
+        e0 = _bf16_to_f64(orc.w["embed"][x])
+        if not np.array_equal(H[0], e0):
+            out["fail"] = f"token {t}: residual stream entering block 0 is not E[{x}]"
+            return out
+        for l in range(L):
+            kc = cache_rows(kcache, l, b, p + 1)
+            vc = cache_rows(vcache, l, b, p + 1)
+            gk, gv = kc[p].copy(), vc[p].copy()
+            h_att, _ = orc.attn_block(l, H[2 * l], p, kc, vc)
+            e = float(rel_err(H[2 * l + 1], h_att))
+            out["max_attn_rel"] = max(out["max_attn_rel"], e)
+            if e > ATTN_REL:
+                out["fail"] = f"token {t} block {l}: teacher-forced attention output rel err {e:.3g}"
+                return out
+            for g, o in ((gk, kc[p]), (gv, vc[p])):
+                out["kv_vals"] += d
+                out["kv_steps"] += int(np.count_nonzero(g != o))
+                bad = kv_within(g, o, BLOCK_REL)[0]
+                if bad.size:
+                    i = int(bad[0])
+                    out["fail"] = (f"token {t} block {l}: cached key/value at position {p} dim {i}"
+                                   f" gpu {g[i]:.6g} oracle {o[i]:.6g} (row scale "
+                                   f"{np.max(np.abs(o)):.3g})")
+                    return out
+            gsel = np.ascontiguousarray(probe_idx[l, t, :])
+            h_new, sel, wts, gap, _ = orc.layer(l, H[2 * l + 1], force_sel=gsel)
+            if not _same_sets(gsel, sel):
+                if gap < TIE:
+                    out["route_ties"] += 1
+                else:
+                    out["fail"] = (f"token {t} (id {x}) block {l}: gpu experts "
+                                   f"{sorted(gsel.tolist())} oracle {sorted(sel.tolist())} "
+                                   f"gap {gap:.3g}")
+                    return out
+            err = np.max(np.abs(probe_w[l, t, :] - wts) / np.maximum(np.abs(wts), 1e-12))
+            if err > BLOCK_REL:
+                out["fail"] = f"token {t} block {l}: routing weights rel err {err:.3g}"
+                return out
+            e = float(rel_err(H[2 * l + 2], h_new))
+            out["max_block_rel"] = max(out["max_block_rel"], e)
+            if e > BLOCK_REL:
+                out["fail"] = f"token {t} block {l}: teacher-forced block output rel err {e:.3g}"
+                return out
+        tgt, lgap, _ = orc.head(H[2 * L])
+        if int(gpu_targets[t]) != tgt:
+            if lgap < TIE:
+                out["logit_tie"] = 1
+            else:
+                out["fail"] = (f"token {t} (id {x}): gpu target {int(gpu_targets[t])} oracle on "
+                               f"the gpu's final residual {tgt}, logit gap {lgap:.3g}")
+        return out
+
+    with fut.ThreadPoolExecutor(max_workers=nthreads) as ex:
+        res = list(ex.map(one, sample))
+    fails = [r["fail"] for r in res if r["fail"]]
+    assert not fails, "\n".join(fails[:10])
+    stats = {"label": label, "tokens": len(res),
+             "route_ties": sum(r["route_ties"] for r in res),
+             "logit_ties": sum(r["logit_tie"] for r in res),
+             "kv_values": sum(r["kv_vals"] for r in res),
+             "kv_values_differing": sum(r["kv_steps"] for r in res),
+             "max_block_rel": max([r["max_block_rel"] for r in res] + [0.0]),
+             "max_attn_rel": max([r["max_attn_rel"] for r in res] + [0.0])}
+    RECORD.append(stats)
+    return stats
