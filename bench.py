@@ -421,6 +421,14 @@ def run_ours(args, rank, world, local):
     ms, got_com, got_alen, clk = timed_plan(ctx, plan, Bq, Kq, args.warmup, args.steps, dev,
                                             dist, clocks)
 
+    if args.profile and args.attn:
+        line = run_attn(w_host, args, dev, peaks, B=Bq, K=Kq)
+        line["clocks"] = clk
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        ctx.close()
+        return
+
     if args.profile and args.draft_head:
         line = run_decode_iteration(args, ctx, cfg, w_host, dev, Bq, Kq, stream)
         line["clocks"] = clk
@@ -493,6 +501,8 @@ def run_ours(args, rank, world, local):
         "single_layer_t4": run_single_layer(ctx, cfg, dev, peaks),
         "zipf_b256_k3_p0.576": run_zipf(w_host, rank, args, dev, peaks),
         "sweep": run_sweep(ctx, cfg, g, rank, dev, peaks),
+        f"attn_b32_k3_pos{ATTN_LO}_{ATTN_HI}": run_attn(w_host, args, dev, peaks,
+                                                         steps=min(args.steps, 20)),
     }
 
     if dist:
@@ -711,6 +721,129 @@ def run_sweep(ctx, cfg, g, rank, dev, peaks, warmup=3, steps=10):
             "check": {"mismatched_rows": mism}}
 
 
+ATTN_LO, ATTN_HI = 512, 4096
+
+
+def run_attn(w_host, args, dev, peaks, B=32, K=3, lo=ATTN_LO, hi=ATTN_HI, steps=None):
+    """The stack with attention (the library's reading of the decoder's
+    unspecified attention: 10 heads of 128, rotary positions, a bf16 key/value
+    cache), B=32 sequences at positions drawn uniformly from [512, 4096), K=3
+    drafts.  Each sequence's cache holds the keys and values of a synthetic
+    prompt, fed through the verify call beforehand (calls of 16 tokens); the
+    timed step re-verifies the prompt's tokens at each sequence's position
+    (the same cache rows are rewritten).  Returns verify tokens/s, the time per
+    step, each kernel's in-graph time per launch, and the attention kernel's
+    roofline: its bytes are every cached key and value of the sequences'
+    positions once, plus q read and the output written."""
+    import torch
+    from moe_speculative_decoding_router_gb300 import binding as BND
+    cfg = S.FULL_ATTN
+    L, d = cfg.n_layers, cfg.hidden
+    steps = steps or args.steps
+    w = dict(w_host)
+    w.update(S.make_attn_weights(cfg))
+    pos = (lo + S.uniform_ids(B, 8, 0, hi - lo - K)).astype(np.int64)
+    n = int(-(-(int(pos.max()) + K + 1) // 16) * 16)
+    ctx = BND.MoeVerify(cfg, BND.weights_to_device(w, device=dev), max_batch=B, max_k=15,
+                        max_pos=n)
+    del w
+    torch.cuda.empty_cache()
+    try:
+        prompts = S.uniform_ids(B * n, 7, 0, cfg.vocab, 123456789).astype(np.int64).reshape(B, n)
+        d_prompts = torch.from_numpy(prompts.astype(np.int32)).to(dev)
+        for p0 in range(0, n, 16):
+            ctx.step_attn(d_prompts[:, p0].contiguous(), d_prompts[:, p0 + 1:p0 + 16].contiguous(),
+                          torch.full((B,), p0, dtype=torch.int32, device=dev))
+        torch.cuda.synchronize()
+        rows = np.arange(B)
+        in_ctx = torch.from_numpy(prompts[rows, pos].astype(np.int32)).to(dev)
+        in_dr = torch.from_numpy(np.stack([prompts[b, pos[b] + 1: pos[b] + 1 + K]
+                                           for b in range(B)]).astype(np.int32)).to(dev)
+        in_pos = torch.from_numpy(pos.astype(np.int32)).to(dev)
+        tg = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        com = torch.empty_like(tg)
+        alen = torch.empty((B,), dtype=torch.int32, device=dev)
+        stamps = torch.zeros((6 * L + 1, 4), dtype=torch.int64, device=dev)
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+
+        def body():
+            ctx.step_attn(in_ctx, in_dr, in_pos, target_ids=tg, stream=s)
+            ctx.accept(in_dr, tg, committed=com, accept_len=alen, stream=s)
+
+        graphs = []
+        for with_stamps in (False, True):
+            with torch.cuda.stream(s):
+                body()
+            s.synchronize()
+            if with_stamps:
+                ctx.set_stamps(stamps)
+            try:
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=s):
+                    body()
+            finally:
+                ctx.set_stamps(None)
+            graphs.append(gr)
+        with torch.cuda.stream(s):
+            for _ in range(args.warmup):
+                graphs[0].replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                graphs[0].replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        # per-launch windows (last CTA end minus the latest return of the wait
+        # for the preceding launch), averaged over replays
+        init = torch.zeros_like(stamps)
+        init[:, 0] = -1
+        wins = []
+        for _ in range(min(steps, 10)):
+            stamps.copy_(init)
+            with torch.cuda.stream(s):
+                graphs[1].replay()
+            s.synchronize()
+            st = stamps.cpu().numpy().view(np.uint64)[:, :3].astype(np.float64)
+            wins.append((st[:, 2] - st[:, 1]) * 1e-6)
+        win = np.mean(np.stack(wins), axis=0)  # ms per launch slot
+        status = ctx.sync_status()
+    finally:
+        ctx.close()
+    T = B * (K + 1)
+    keys = float(np.sum(pos + K + 1))
+    attn_bytes = keys * d * 2 * 2 + T * d * 4 + T * d * 2
+    attn_ms = float(np.mean(win[2:6 * L:6]))
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    rows_qkv = -(-3 * d // 128) * 128
+    qkv_bytes = rows_qkv * d * 2 + T * d * 2 + T * d * 4 + 2 * T * d * 2
+    o_bytes = d * d * 2 + T * d * 2 + 2 * T * d * 4
+    qkv_ms, o_ms = float(np.mean(win[1:6 * L:6])), float(np.mean(win[3:6 * L:6]))
+    kib = {"attn_rmsnorm": win[0:6 * L:6], "qkv_projection": win[1:6 * L:6],
+           "attention": win[2:6 * L:6], "o_projection": win[3:6 * L:6],
+           "routing": win[4:6 * L:6], "expert_ffn": win[5:6 * L:6]}
+    return {"batch": B, "drafts": K, "positions": f"uniform in [{lo}, {hi})",
+            "mean_position": round(float(pos.mean()), 1), "steps": steps,
+            "value": round(T / (ms * 1e-3), 1), "unit": "verify tokens/s",
+            "ms_per_step": round(ms, 4),
+            "in_graph_ms_per_launch": {k: round(float(np.mean(v)), 5) for k, v in kib.items()},
+            "in_graph_ms_lm_head": round(float(win[6 * L]), 5),
+            "roofline": {"kernel": "attention over the key/value cache", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": peaks[0], "unit": "GB/s",
+                         "frac": round(achieved / peaks[0], 4), "peak_source": peaks[3],
+                         "alg_bytes_per_launch": round(attn_bytes),
+                         "alg_bytes": "each sequence's cached keys and values of positions "
+                                      "0 .. pos + K once, q read, output written",
+                         "launch_ms": round(attn_ms, 5),
+                         "launch_ms_source": "in-graph launch timestamps"},
+            "projections": {"qkv_gbs": round(qkv_bytes / (qkv_ms * 1e-3) / 1e9, 1),
+                            "o_gbs": round(o_bytes / (o_ms * 1e-3) / 1e9, 1),
+                            "alg_bytes": "weights once, activations in and out"},
+            "cache_fill": f"{n} prompt tokens per sequence through the verify call (16 per call)",
+            "check": {"status": status}}
+
+
 def whole_job(ms, e_s, tokens, e_tokens, device):
     """Whole-job figures over the ranks of the default process group: the
     slowest rank's device and end-to-end times, every rank's committed tokens."""
@@ -902,13 +1035,17 @@ def main():
                     help="profiling only: the stack with the Zipf(s=1.2) router bias")
     ap.add_argument("--draft-head", action="store_true",
                     help="profiling only: time whole decode iterations with the FastMTP draft head")
+    ap.add_argument("--attn", action="store_true",
+                    help="profiling only: the stack with attention at positions in [512, 4096)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if (args.layers or args.batch or args.drafts is not None or args.draft_head
-            or args.zipf) and not args.profile:
-        ap.error("--layers, --batch, --drafts, --zipf and --draft-head are for profiling runs "
-                 "only (--profile)")
+            or args.zipf or args.attn) and not args.profile:
+        ap.error("--layers, --batch, --drafts, --zipf, --draft-head and --attn are for "
+                 "profiling runs only (--profile)")
+    if args.attn and (args.layers or args.zipf or args.draft_head):
+        ap.error("--attn runs the full stack without the Zipf bias or the draft head")
     if args.draft_head and (args.layers or (args.drafts is not None and args.drafts < 1)):
         ap.error("--draft-head needs the full stack and at least one draft")
     if args.drafts is not None and not 0 <= args.drafts <= 15:

@@ -247,7 +247,7 @@ MOE_VERIFY_API int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elap
  * * max_pos + pos) * hd + i.
  * -------------------------------------------------------------------- */
 typedef struct {
-  int32_t n_heads;  /* >= 1, hd = d / n_heads one of 8, 16, 32, 64, 128 */
+  int32_t n_heads;  /* >= 1, hd = d / n_heads one of 16, 32, 64, 128 */
   int32_t max_pos;  /* positions held per sequence slot: 1..32768 */
   float rope_theta; /* > 1 (10000) */
 } moe_verify_attn_config;
@@ -266,7 +266,7 @@ typedef struct {                  /* HOST arrays of n_layers device pointers, bf
  * of max_batch sequence slots x max_pos positions x n_layers (bf16, 2 x L x
  * max_batch x max_pos x d x 2 bytes, zeroed) and a rotary table (max_pos x
  * hd/2 x 8 bytes).  Returns MOE_VERIFY_ERR_UNSUPPORTED for a head width other
- * than 8, 16, 32, 64 or 128.  The context then runs moe_verify_step_attn
+ * than 16, 32, 64 or 128, or for L x max_batch x n_heads x max_pos >= 2^31.  The context then runs moe_verify_step_attn
  * (moe_verify_step, moe_verify_layer, moe_verify_decode_host and
  * moe_verify_draft refuse it with MOE_VERIFY_ERR_ARG); moe_verify_accept,
  * moe_verify_sync_status, the timing calls, moe_verify_set_grid and
@@ -354,16 +354,19 @@ MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] h
  * once shows that no CTA waits for one that has not started (every expert-FFN
  * work item is claimed in order by a running CTA).  With attention it also
  * sets the CTAs of the projections (at most one per work item) and of the
- * attention (default 4 per SM).  Host-buffer decode graphs
+ * attention (default one per SM).  Host-buffer decode graphs
  * already captured keep the grid they were captured with. */
 MOE_VERIFY_API int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas);
 
 /* Profiling (no counterpart in the method): launch timestamps inside later
- * moe_verify_step calls, for timing kernels in a graph-replayed step without
- * breaking the overlap of consecutive launches.  stamps is a device array of
- * (2 L + 1) x 4 uint64 (8-byte aligned, caller-owned), or NULL to stop.
- * Launch j of a step (routing of layer l: j = 2l; expert FFN of layer l:
- * j = 2l + 1; lm_head: j = 2L) updates stamps[4j + 0] = min over its CTAs of
+ * moe_verify_step (moe_verify_step_attn) calls, for timing kernels in a
+ * graph-replayed step without breaking the overlap of consecutive launches.
+ * stamps is a device array of (2 L + 1) x 4 uint64 ((6 L + 1) x 4 for a context
+ * with attention; 8-byte aligned, caller-owned), or NULL to stop.  Launch j of
+ * a step (routing of layer l: j = 2l; expert FFN of layer l: j = 2l + 1;
+ * lm_head: j = 2L; with attention: attention RMSNorm 6l, q/k/v projection
+ * 6l + 1, attention 6l + 2, output projection 6l + 3, routing 6l + 4, expert
+ * FFN 6l + 5, lm_head 6L) updates stamps[4j + 0] = min over its CTAs of
  * the start time, stamps[4j + 1] = max of the time its wait for the
  * preceding launch returned, stamps[4j + 2] = max of the end time (global
  * timer, ns); stamps[4j + 3] is unused.  The caller sets stamps[4j] to

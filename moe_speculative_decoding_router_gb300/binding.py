@@ -441,11 +441,12 @@ class MoeVerify:
             raise MoeVerifyError(rc, "moe_verify_set_grid")
 
     def set_stamps(self, stamps):
-        """moe_verify_set_stamps: a device int64 tensor [2L + 1, 4] (viewed as
-        uint64 by the library), or None to stop."""
+        """moe_verify_set_stamps: a device int64 tensor [2L + 1, 4] ([6L + 1, 4]
+        with attention; viewed as uint64 by the library), or None to stop."""
         import torch
         if stamps is not None:
-            _check_dev(stamps, torch.int64, "stamps", (2 * self.cfg.n_layers + 1, 4))
+            per = 6 if self.attn else 2
+            _check_dev(stamps, torch.int64, "stamps", (per * self.cfg.n_layers + 1, 4))
         rc = self.lib.moe_verify_set_stamps(self.handle, _ptr(stamps) if stamps is not None else None)
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_set_stamps")

@@ -61,8 +61,8 @@ struct moe_verify_ctx {
                 *xa = nullptr, *obuf = nullptr;
   float *attn_gain = nullptr, *qbuf = nullptr, *part = nullptr;
   float2* rope = nullptr;
-  int32_t *arrive = nullptr, *plan = nullptr;
-  CUtensorMap map_qkv, map_wo;
+  int32_t *arrive = nullptr, *plan = nullptr, *attn_ctr = nullptr;
+  CUtensorMap map_qkv, map_wo, map_kc, map_vc;
   // profiling
   unsigned long long* stamps = nullptr;  // caller-owned [2L + 1][kStampSlots] or nullptr
   bool timing = false;
@@ -214,6 +214,27 @@ int encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
   return r == CUDA_SUCCESS ? MOE_VERIFY_OK : MOE_VERIFY_ERR_CUDA;
 }
 
+// 2-D bf16 tensor [rows, inner] read in boxes of box_inner x box_rows with
+// the swizzle that matches the box's row bytes (128, 64 or 32).
+int encode_map_box(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                   uint32_t box_inner, uint32_t box_rows) {
+  auto fn = get_encode();
+  if (!fn) return MOE_VERIFY_ERR_CUDA;
+  const uint32_t rb = box_inner * 2;
+  const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
+  if (rb != 128 && rb != 64 && rb != 32) return MOE_VERIFY_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_VERIFY_OK : MOE_VERIFY_ERR_CUDA;
+}
+
 void free_all(moe_verify_ctx* c) {
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
@@ -329,8 +350,10 @@ int32_t* item_counter(moe_verify_ctx* c, int parity) {
 int persistent_grid(const moe_verify_ctx* c) { return c->grid_ctas > 0 ? c->grid_ctas : c->num_sms; }
 
 // Timer slots of launch `slot` of a step (routing of layer l: 2l, expert FFN
-// of layer l: 2l + 1, lm_head: 2L), or nullptr when stamps are off or the
-// launch is not part of a step (slot < 0).
+// of layer l: 2l + 1, lm_head: 2L; with attention: attention RMSNorm 6l,
+// q/k/v projection 6l + 1, attention 6l + 2, output projection 6l + 3,
+// routing 6l + 4, expert FFN 6l + 5, lm_head 6L), or nullptr when stamps are
+// off or the launch is not part of a step (slot < 0).
 unsigned long long* stamp_slot(const moe_verify_ctx* c, int slot) {
   return (c->stamps && slot >= 0) ? c->stamps + (size_t)slot * mv::kStampSlots : nullptr;
 }
@@ -340,7 +363,7 @@ unsigned long long* stamp_slot(const moe_verify_ctx* c, int slot) {
 int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh,
               const int32_t* context_ids, const int32_t* draft_ids, int B, int K,
               const void* h_in, const moe_verify_probe* probe, int probe_layer, cudaStream_t s,
-              bool pdl, bool next_head, bool stamped = false) {
+              bool pdl, bool next_head, int stamp_base = -1) {
   const int T = sh.T;
   mv::RouteParams rp = {};
   rp.T = T;
@@ -381,7 +404,7 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   rp.perm_token = c->perm_token;
   rp.perm_slot = c->perm_slot;
   rp.perm_w = c->perm_w;
-  rp.stamps = stamp_slot(c, stamped ? 2 * l : -1);
+  rp.stamps = stamp_slot(c, stamp_base);
   {
     Timed tm(c, 3, s);
     CK(mv::launch_route(c->map_wr, rp, sh.grid_route, sh.route_smem, s, pdl));
@@ -442,7 +465,7 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.pf_limit = pull_routed ? c->nE * c->mt_gu
                               : c->S * ((T + sh.nch - 1) / sh.nch) * c->mt_gu;
   }
-  fp.stamps = stamp_slot(c, stamped ? 2 * l + 1 : -1);
+  fp.stamps = stamp_slot(c, stamp_base >= 0 ? stamp_base + 1 : -1);
   if (sh.tokm) {
     fp.spec = 0;
     fp.pf_limit = 0;
@@ -643,7 +666,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
 // (parity `last_parity`).  probe_hidden [T, d] and logits [T, V] may be NULL.
 static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int last_parity,
                         int32_t* target_ids, float* probe_hidden, float* logits, cudaStream_t s,
-                        bool pdl, bool stamped = false) {
+                        bool pdl, int stamp_slot_lm = -1) {
   mv::FinalParams fp = {};
   fp.T = T;
   fp.d = ctx->d;
@@ -680,7 +703,7 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   gp.bad = ctx->bad;
   gp.done = ctx->done_lm;
   gp.aborted = ctx->done_lm + 1;
-  gp.stamps = stamp_slot(ctx, stamped ? 2 * ctx->L : -1);
+  gp.stamps = stamp_slot(ctx, stamp_slot_lm);
   {
     Timed tm(ctx, 2, s);
     CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, persistent_grid(ctx), s,
@@ -698,12 +721,12 @@ static int enqueue_step(moe_verify_ctx* ctx, const int32_t* context_ids, const i
   const bool pdl = true;
   for (int l = 0; l < ctx->L; ++l) {
     int rc = run_layer(ctx, l, l & 1, l == 0 ? mv::kSrcEmbed : mv::kSrcCombine, sh, context_ids,
-                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1, true);
+                       draft_ids, B, K, nullptr, probe, l, s, pdl, l == ctx->L - 1, 2 * l);
     if (rc != MOE_VERIFY_OK) return rc;
   }
   float* ph = (probe && probe->hidden) ? probe->hidden + (size_t)ctx->L * T * ctx->d : nullptr;
   return enqueue_head(ctx, T, sh, (ctx->L - 1) & 1, target_ids, ph, probe ? probe->logits : nullptr,
-                      s, pdl, true);
+                      s, pdl, 2 * ctx->L);
 }
 
 int moe_verify_step(moe_verify_ctx* ctx, const int32_t* context_ids, const int32_t* draft_ids,
@@ -896,7 +919,11 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
   for (int l = 0; l < L; ++l)
     if (!aw->attn_norm[l] || !aw->w_q[l] || !aw->w_k[l] || !aw->w_v[l] || !aw->w_o[l])
       return MOE_VERIFY_ERR_ARG;
-  if (hd != 8 && hd != 16 && hd != 32 && hd != 64 && hd != 128) return MOE_VERIFY_ERR_UNSUPPORTED;
+  if (hd != 16 && hd != 32 && hd != 64 && hd != 128) return MOE_VERIFY_ERR_UNSUPPORTED;
+  // cache rows (layers x slots x heads x positions) are addressed with 32-bit
+  // tensor-map coordinates
+  if ((uint64_t)L * config->max_batch * attn->n_heads * attn->max_pos >= (1ull << 31))
+    return MOE_VERIFY_ERR_UNSUPPORTED;
   rc = moe_verify_init(config, weights, cuda_stream, out);
   if (rc != MOE_VERIFY_OK) return rc;
   moe_verify_ctx* c = *out;
@@ -912,7 +939,7 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
   c->max_pos = attn->max_pos;
   c->rows_qkv = round_up(3 * d, 128);
   const int Bmax = config->max_batch, K1max = config->max_k + 1;
-  c->attn_target = 4 * c->num_sms;
+  c->attn_target = 8 * c->num_sms;
   // (sequence, split) pairs: at most B + total keys / split width, the width
   // either >= total keys x H / target or 1024
   c->cap_pairs = Bmax + (c->attn_target + c->H - 1) / c->H +
@@ -929,7 +956,8 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
       (e = dalloc(c, &c->qbuf, (uint64_t)c->T_max * d * 4)) ||
       (e = dalloc(c, &c->part, (uint64_t)c->cap_pairs * c->H * K1max * (hd + 2) * 4)) ||
       (e = dalloc(c, &c->arrive, (uint64_t)Bmax * c->H * 4)) ||
-      (e = dalloc(c, &c->plan, (uint64_t)(2 + 2 * c->cap_pairs) * 4)))
+      (e = dalloc(c, &c->plan, (uint64_t)(2 + 2 * c->cap_pairs) * 4)) ||
+      (e = dalloc(c, &c->attn_ctr, (uint64_t)L * 4)))
     return fail(e);
 #define CKA(x)                                               \
   do {                                                       \
@@ -941,6 +969,7 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
   CKA(cudaMemsetAsync(c->obuf, 0, act16, s));
   CKA(cudaMemsetAsync(c->arrive, 0, (size_t)Bmax * c->H * 4, s));
   CKA(cudaMemsetAsync(c->plan, 0, (size_t)(2 + 2 * c->cap_pairs) * 4, s));
+  CKA(cudaMemsetAsync(c->attn_ctr, 0, (size_t)L * 4, s));
   CKA(cudaMemsetAsync(c->w_o, 0, (size_t)L * c->d_pad * d * 2, s));
   for (int l = 0; l < L; ++l) {
     CKA(mv::launch_repack_qkv(c->w_qkv + (size_t)l * c->rows_qkv * d,
@@ -969,8 +998,12 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
     CKA(cudaStreamSynchronize(s));
   }
 #undef CKA
+  const uint64_t cache_rows = (uint64_t)L * Bmax * c->H * c->max_pos;
+  const uint32_t bw = hd < 64 ? (uint32_t)hd : 64u;
   if (encode_map(&c->map_qkv, c->w_qkv, d, (uint64_t)L * c->rows_qkv, 128) ||
-      encode_map(&c->map_wo, c->w_o, d, (uint64_t)L * c->d_pad, 128))
+      encode_map(&c->map_wo, c->w_o, d, (uint64_t)L * c->d_pad, 128) ||
+      encode_map_box(&c->map_kc, c->kcache, hd, cache_rows, bw, mv::attn_max_split(hd)) ||
+      encode_map_box(&c->map_vc, c->vcache, hd, cache_rows, bw, mv::attn_max_split(hd)))
     return fail(MOE_VERIFY_ERR_CUDA);
   return MOE_VERIFY_OK;
 }
@@ -992,21 +1025,26 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
   const int T = B * (K + 1), d = ctx->d, L = ctx->L;
   StepShape sh;
   if (shape_for(ctx, T, &sh) != MOE_VERIFY_OK) return MOE_VERIFY_ERR_CUDA;
-  // projections: token chunks of <= 256, as even as 16-row granularity allows
-  const int n_chunks = (T + 255) / 256;
-  const int nch = round_up((T + n_chunks - 1) / n_chunks, 16);
-  CUtensorMap map_xa, map_o;
-  if (encode_map(&map_xa, ctx->xa, d, round_up(ctx->T_max, 16), (uint32_t)nch) ||
-      encode_map(&map_o, ctx->obuf, d, round_up(ctx->T_max, 16), (uint32_t)nch))
-    return MOE_VERIFY_ERR_CUDA;
-  int stages = 16;
-  while (stages > 2 && mv::proj_smem_bytes(nch, stages) > 227 * 1024) --stages;
+  // projections: token chunks of <= 256 rows, as many as it takes for the
+  // (weight tile, chunk) items to cover the SMs (the chunks of one tile run
+  // side by side and share its weights through L2)
+  auto proj_shape = [&](int tiles, mv::ProjParams* pp, CUtensorMap* map, void* act) {
+    int chunks = (ctx->num_sms + tiles - 1) / tiles;
+    const int most = (T + 15) / 16;
+    if (chunks > most) chunks = most;
+    if (chunks < (T + 255) / 256) chunks = (T + 255) / 256;
+    const int nch = round_up((T + chunks - 1) / chunks, 16);
+    pp->nch = nch;
+    pp->n_chunks = (T + nch - 1) / nch;
+    pp->n_items = tiles * pp->n_chunks;
+    int stages = 16;
+    while (stages > 2 && mv::proj_smem_bytes(nch, stages) > 227 * 1024) --stages;
+    pp->stages = stages;
+    pp->tmem_cols = pow2_at_least(2 * nch);
+    return encode_map(map, act, d, round_up(ctx->T_max, 16), (uint32_t)nch);
+  };
   mv::ProjParams pb = {};
-  pb.n_chunks = n_chunks;
-  pb.nch = nch;
   pb.kblocks = d / 64;
-  pb.stages = stages;
-  pb.tmem_cols = pow2_at_least(2 * nch);
   pb.T = T;
   pb.d = d;
   pb.K = K;
@@ -1017,8 +1055,13 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
   pb.status = ctx->status;
   pb.positions = positions;
   pb.rope = ctx->rope;
+  mv::ProjParams pq = pb, po = pb;
+  CUtensorMap map_xa, map_o;
+  if (proj_shape(ctx->rows_qkv / 128, &pq, &map_xa, ctx->xa) ||
+      proj_shape(ctx->d_pad / 128, &po, &map_o, ctx->obuf))
+    return MOE_VERIFY_ERR_CUDA;
   const size_t cache_layer = (size_t)ctx->cfg.max_batch * ctx->max_pos * d;
-  const int attn_grid = ctx->grid_ctas > 0 ? ctx->grid_ctas : ctx->attn_target;
+  const int attn_grid = ctx->grid_ctas > 0 ? ctx->grid_ctas : ctx->num_sms;
   // probe->hidden [2L + 1, T, d]: row 2l the residual entering block l's
   // attention (written by its RMSNorm kernel), row 2l + 1 the residual
   // entering its MoE part (written by the routing kernel, which indexes the
@@ -1053,18 +1096,22 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
       ap.status = ctx->status;
       ap.plan = ctx->plan;
       ap.target_items = ctx->attn_target;
+      ap.max_split = mv::attn_max_split(ctx->hd);
+      ap.item_ctr = ctx->attn_ctr;
+      ap.n_item_ctr = L;
       ap.cap_pairs = ctx->cap_pairs;
+      ap.stamps = stamp_slot(ctx, 6 * l);
       CK(mv::launch_attn_norm(ap, s, pdl));
     }
     {
       Timed tm(ctx, 1, s);
-      mv::ProjParams qp = pb;
+      mv::ProjParams qp = pq;
       qp.mode = 0;
-      qp.n_items = (ctx->rows_qkv / 128) * n_chunks;
       qp.a_row0 = l * ctx->rows_qkv;
       qp.q = ctx->qbuf;
       qp.kc = ctx->kcache + cache_layer * l;
       qp.vc = ctx->vcache + cache_layer * l;
+      qp.stamps = stamp_slot(ctx, 6 * l + 1);
       const int g = persistent_grid(ctx) < qp.n_items ? persistent_grid(ctx) : qp.n_items;
       CK(mv::launch_proj(ctx->map_qkv, map_xa, qp, g, s, pdl));
     }
@@ -1078,6 +1125,9 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
       at.d = d;
       at.max_pos = ctx->max_pos;
       at.Bmax = ctx->cfg.max_batch;
+      at.max_split = mv::attn_max_split(ctx->hd);
+      at.row0 = l * ctx->cfg.max_batch * ctx->H * ctx->max_pos;
+      at.item_ctr = ctx->attn_ctr + l;
       at.scale_log2 = (float)(1.4426950408889634 / sqrt((double)ctx->hd));
       at.positions = positions;
       at.plan = ctx->plan;
@@ -1088,26 +1138,27 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
       at.part = ctx->part;
       at.arrive = ctx->arrive;
       at.status = ctx->status;
-      CK(mv::launch_attn(at, attn_grid, s, pdl));
+      at.stamps = stamp_slot(ctx, 6 * l + 2);
+      CK(mv::launch_attn(ctx->map_kc, ctx->map_vc, at, attn_grid, s, pdl));
     }
     {
       Timed tm(ctx, 1, s);
-      mv::ProjParams op = pb;
+      mv::ProjParams op = po;
       op.mode = 1;
-      op.n_items = (ctx->d_pad / 128) * n_chunks;
       op.a_row0 = l * ctx->d_pad;
       op.h = ctx->h;
+      op.stamps = stamp_slot(ctx, 6 * l + 3);
       const int g = persistent_grid(ctx) < op.n_items ? persistent_grid(ctx) : op.n_items;
       CK(mv::launch_proj(ctx->map_wo, map_o, op, g, s, pdl));
     }
     if (probe && probe->hidden) route_probe.hidden = probe->hidden + (size_t)(l + 1) * T * d;
     int rc = run_layer(ctx, l, l & 1, mv::kSrcH, sh, context_ids, draft_ids, B, K, nullptr,
-                       probe ? &route_probe : nullptr, l, s, pdl, l == L - 1, false);
+                       probe ? &route_probe : nullptr, l, s, pdl, l == L - 1, 6 * l + 4);
     if (rc != MOE_VERIFY_OK) return rc;
   }
   float* ph = (probe && probe->hidden) ? probe->hidden + (size_t)(2 * L) * T * d : nullptr;
   return enqueue_head(ctx, T, sh, (L - 1) & 1, target_ids, ph, probe ? probe->logits : nullptr, s,
-                      pdl, false);
+                      pdl, 6 * L);
 }
 
 int moe_verify_check_bounded_wait(int64_t limit_ns, int64_t* elapsed_ns, void* cuda_stream) {

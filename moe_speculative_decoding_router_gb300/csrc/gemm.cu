@@ -1408,6 +1408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool has_work = (int)blockIdx.x < n_items;
 
   if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
     init_ctrl(C, p.stages, 4, 1);
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
@@ -1446,6 +1447,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (p.stamps) stamp_max(p.stamps + 1);
     for (int s = 0; s < pre; ++s) {
       tma_load_2d(stages + (size_t)s * stage_bytes + kStageA, &mapB, &C.full[s], kb * 64,
                   it.b_row, pol_x);
@@ -1486,6 +1488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
     if (has_work && warp == 1 && lane == 0) {
       // ------------------------------------------------ MMA issuer
       int stage = 0, local = 0;
@@ -1523,39 +1526,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t v[16];
           tmem_ld16(tb + (uint32_t)c0, v);
           tmem_ld_wait();
+          // the 16 columns' global loads are issued before their stores
+          if (p.mode == 1) {
+            if (prow < p.d) {
+              float hv[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                hv[j] = c0 + j < it.n ? p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < it.n)
+                  p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] = hv[j] + __uint_as_float(v[j]);
+            }
+            continue;
+          }
+          if (r.part >= 3) continue;
+          // each column's sequence and position (the same for every lane)
+          int bq[16], pos[16];
+          bool ok[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int tl = c0 + j;
-            const bool valid = tl < it.n;  // the same for every lane
-            const int t = it.b_row + tl;
-            const float x = __uint_as_float(v[j]);
-            if (p.mode == 1) {
-              if (valid && prow < p.d) p.h[(size_t)t * p.d + prow] += x;
-              continue;
-            }
-            if (r.part >= 3) continue;
-            int b = 0, pos = 0;
-            bool seq_ok = false;
-            if (valid) {
-              b = t / K1;
-              const int p0 = __ldg(p.positions + b);
-              seq_ok = p0 >= 0 && p0 <= p.max_pos - K1;
-              pos = seq_ok ? p0 + (t - b * K1) : 0;
-            }
-            const size_t at = (((size_t)b * p.H + r.head) * p.max_pos + pos) * p.hd + r.dim;
-            if (r.part < 2) {
+            const int t = it.b_row + c0 + j;
+            const bool valid = c0 + j < it.n;
+            bq[j] = valid ? t / K1 : 0;
+            const int p0 = valid ? __ldg(p.positions + bq[j]) : 0;
+            ok[j] = valid && p0 >= 0 && p0 <= p.max_pos - K1;
+            pos[j] = ok[j] ? p0 + (t - bq[j] * K1) : 0;
+          }
+          if (r.part < 2) {
+            float2 cs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cs[j] = __ldg(p.rope + (size_t)pos[j] * half + r.freq);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
               // rotary pair (dim i, dim i + hd/2) in lanes (2i, 2i + 1)
+              const float x = __uint_as_float(v[j]);
               const float y = __shfl_xor_sync(0xffffffffu, x, 1);
-              const float2 cs = __ldg(p.rope + (size_t)pos * half + r.freq);
-              const float rot = r.odd ? y * cs.y + x * cs.x : x * cs.x - y * cs.y;
-              if (!valid) continue;
+              const float rot = r.odd ? y * cs[j].y + x * cs[j].x : x * cs[j].x - y * cs[j].y;
+              if (c0 + j >= it.n) continue;
+              const int t = it.b_row + c0 + j;
               if (r.part == 0)
                 p.q[(size_t)t * p.d + r.head * p.hd + r.dim] = rot;
-              else if (seq_ok)
-                p.kc[at] = __float2bfloat16_rn(rot);
-            } else if (valid && seq_ok) {
-              p.vc[at] = __float2bfloat16_rn(x);
+              else if (ok[j])
+                p.kc[(((size_t)bq[j] * p.H + r.head) * p.max_pos + pos[j]) * p.hd + r.dim] =
+                    __float2bfloat16_rn(rot);
             }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (ok[j])
+                p.vc[(((size_t)bq[j] * p.H + r.head) * p.max_pos + pos[j]) * p.hd + r.dim] =
+                    __float2bfloat16_rn(__uint_as_float(v[j]));
           }
         }
         tc_fence_before();
@@ -1570,6 +1591,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
+  if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
 }
 
 template <typename Kern, typename... Args>

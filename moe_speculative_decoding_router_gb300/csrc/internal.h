@@ -164,7 +164,11 @@ struct AttnNormParams {
   // plan[2 + 2i] = sequence, plan[3 + 2i] = split
   int32_t* plan;
   int target_items;            // wanted (sequence, split, head) items
+  int max_split;               // attn_max_split(hd): keys per chunk
   int cap_pairs;               // room in plan for pairs
+  int32_t* item_ctr;           // [n_item_ctr] the attention's item counters (one per layer), cleared
+  int n_item_ctr;
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
 // Weight-major projection on the tensor cores: items are (128 weight rows,
@@ -184,6 +188,7 @@ struct ProjParams {
   __nv_bfloat16* kc;           // this layer's key cache [Bmax, H, max_pos, hd] (mode 0)
   __nv_bfloat16* vc;           // this layer's value cache (mode 0)
   float* h;                    // [T, d] (mode 1)
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 
 // Causal attention of the step's tokens over their sequences' caches.  Items
@@ -192,6 +197,8 @@ struct ProjParams {
 // sequence's and head's items to finish.
 struct AttnParams {
   int B, K, H, hd, d, max_pos, Bmax;
+  int row0;                    // this layer's first row in the cache tensor maps
+  int max_split;               // attn_max_split(hd): keys per chunk (shared-memory buffer)
   float scale_log2;            // log2(e) / sqrt(hd)
   const int32_t* positions;    // [B]
   const int32_t* plan;
@@ -201,10 +208,20 @@ struct AttnParams {
   __nv_bfloat16* o;            // [T, d] bf16 attention output
   float* part;                 // [cap items, K+1, hd + 2] split results (m, l, acc)
   int32_t* arrive;             // [Bmax, H] finished splits (zero on entry; the merger resets)
+  int32_t* item_ctr;           // items claimed so far (zero on entry: cleared by layer 0's attn_norm)
   uint32_t* status;
+  unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };
 constexpr int kAttnMinSplit = 64;    // keys per split: at least
 constexpr int kAttnMaxSplit = 1024;  // and at most
+constexpr int kAttnMaxSplits = 64;   // splits of one sequence: at most (32,768 / 64 <= 1,024)
+// keys per chunk (the attention kernel's shared-memory buffer holds at most
+// 16,384 key elements, 32 KB of keys and as much of values, in TMA boxes of
+// at most 256 rows): 128 keys of 128 dims, 256 keys of 64 or fewer
+__host__ __device__ inline int attn_max_split(int hd) {
+  const int c = 16384 / hd;
+  return c > 256 ? 256 : c;
+}
 
 struct AcceptParams {
   int B, K, V;
@@ -263,8 +280,12 @@ cudaError_t launch_attn_norm(const AttnNormParams& p, cudaStream_t s, bool pdl);
 size_t proj_smem_bytes(int nch, int stages);
 cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, const ProjParams& p,
                         int grid, cudaStream_t s, bool pdl);
-size_t attn_smem_bytes(int nq, int hd);
-cudaError_t launch_attn(const AttnParams& p, int grid, cudaStream_t s, bool pdl);
+size_t attn_smem_bytes(int hd, int nq);
+// map_k, map_v: the key and value caches as 2-D bf16 tensors [L * Bmax * H *
+// max_pos rows, hd], boxes of min(hd, 64) x attn_max_split(hd) with the swizzle
+// of the box's row bytes (128, 64 or 32).  hd is 16, 32, 64 or 128.
+cudaError_t launch_attn(const CUtensorMap& map_k, const CUtensorMap& map_v, const AttnParams& p,
+                        int grid, cudaStream_t s, bool pdl);
 // dst [rows_pad, d] = the packed q/k/v rows of one layer (zero past 3d).
 cudaError_t launch_repack_qkv(__nv_bfloat16* dst, const __nv_bfloat16* wq,
                               const __nv_bfloat16* wk, const __nv_bfloat16* wv, int d, int hd,

@@ -131,6 +131,23 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* row_ad
                : "r"(smem_u32(row_addr)));
 }
 
+// The same with each 8x8 matrix transposed on the way: lane l receives the
+// elements (row 2 (l % 4) + {0, 1}, column l / 4) of matrix i in register i.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row_addr)));
+}
+
+// Transpose of an 8x8 b16 matrix held as a warp fragment (lane l holds row
+// l / 4, columns 2 (l % 4) and 2 (l % 4) + 1): lane l receives the same
+// positions of the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 // D += A B for one 16x8x16 tile (A row-major 16x16 bf16, B column-major
 // 16x8 bf16, D fp32), warp-wide.
 __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,

@@ -237,13 +237,23 @@ def make_weights(cfg: ModelConfig, seed: int = SEED_WEIGHTS, with_embed: bool = 
     if rb is not None:
         w["router_bias"] = rb
     if cfg.n_heads > 0:
-        w["attn_norm"] = np.full((L, d), one, dtype=np.uint16)
-        for name in _ATTN_TENSORS:
-            arr = np.empty((L, d, d), dtype=np.uint16)
-            for l in range(L):
-                lib().synth_normal_bf16(arr[l].ctypes.data, arr[l].size, seed, tid_attn(L, l, name),
-                                        0, float(sg), _threads(nthreads))
-            w[name] = arr
+        w.update(make_attn_weights(cfg, seed, nthreads))
+    return w
+
+
+def make_attn_weights(cfg: ModelConfig, seed: int = SEED_WEIGHTS,
+                      nthreads: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """The attention tensors alone (the entries that make_weights adds for a
+    shape record with n_heads > 0): unit attn_norm gains and W_q, W_k, W_v,
+    W_o [L, d, d]."""
+    L, d = cfg.n_layers, cfg.hidden
+    w: Dict[str, np.ndarray] = {"attn_norm": np.full((L, d), np.uint16(0x3F80), dtype=np.uint16)}
+    for name in _ATTN_TENSORS:
+        arr = np.empty((L, d, d), dtype=np.uint16)
+        for l in range(L):
+            lib().synth_normal_bf16(arr[l].ctypes.data, arr[l].size, seed, tid_attn(L, l, name),
+                                    0, float(cfg.sigma), _threads(nthreads))
+        w[name] = arr
     return w
 
 
