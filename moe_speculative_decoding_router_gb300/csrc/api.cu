@@ -939,7 +939,10 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
   c->max_pos = attn->max_pos;
   c->rows_qkv = round_up(3 * d, 128);
   const int Bmax = config->max_batch, K1max = config->max_k + 1;
-  c->attn_target = 8 * c->num_sms;
+  // about four items per SM: measured at 32 sequences of ~1,900 positions,
+  // 8 per SM gave 88 us per attention launch and 2 or 4 per SM 72 us (fewer,
+  // longer items: fewer item ends and split merges)
+  c->attn_target = 4 * c->num_sms;
   // (sequence, split) pairs: at most B + total keys / split width, the width
   // either >= total keys x H / target or 1024
   c->cap_pairs = Bmax + (c->attn_target + c->H - 1) / c->H +
@@ -956,7 +959,7 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
       (e = dalloc(c, &c->qbuf, (uint64_t)c->T_max * d * 4)) ||
       (e = dalloc(c, &c->part, (uint64_t)c->cap_pairs * c->H * K1max * (hd + 2) * 4)) ||
       (e = dalloc(c, &c->arrive, (uint64_t)Bmax * c->H * 4)) ||
-      (e = dalloc(c, &c->plan, (uint64_t)(2 + 2 * c->cap_pairs) * 4)) ||
+      (e = dalloc(c, &c->plan, (uint64_t)(2 + 2 * c->cap_pairs + Bmax) * 4)) ||
       (e = dalloc(c, &c->attn_ctr, (uint64_t)L * 4)))
     return fail(e);
 #define CKA(x)                                               \
@@ -968,7 +971,7 @@ int moe_verify_init_attn(const moe_verify_config* config, const moe_verify_weigh
   CKA(cudaMemsetAsync(c->xa, 0, act16, s));
   CKA(cudaMemsetAsync(c->obuf, 0, act16, s));
   CKA(cudaMemsetAsync(c->arrive, 0, (size_t)Bmax * c->H * 4, s));
-  CKA(cudaMemsetAsync(c->plan, 0, (size_t)(2 + 2 * c->cap_pairs) * 4, s));
+  CKA(cudaMemsetAsync(c->plan, 0, (size_t)(2 + 2 * c->cap_pairs + Bmax) * 4, s));
   CKA(cudaMemsetAsync(c->attn_ctr, 0, (size_t)L * 4, s));
   CKA(cudaMemsetAsync(c->w_o, 0, (size_t)L * c->d_pad * d * 2, s));
   for (int l = 0; l < L; ++l) {
@@ -1128,6 +1131,7 @@ int moe_verify_step_attn(moe_verify_ctx* ctx, const int32_t* context_ids, const 
       at.max_split = mv::attn_max_split(ctx->hd);
       at.row0 = l * ctx->cfg.max_batch * ctx->H * ctx->max_pos;
       at.item_ctr = ctx->attn_ctr + l;
+      at.cap_pairs = ctx->cap_pairs;
       at.scale_log2 = (float)(1.4426950408889634 / sqrt((double)ctx->hd));
       at.positions = positions;
       at.plan = ctx->plan;

@@ -31,7 +31,7 @@ namespace mv {
 namespace {
 
 constexpr int kNormThreads = 256;
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 256;  // compute threads of the attention kernel (plus a loading warp)
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnStages = 3;  // chunk buffers of the attention kernel's ring
 
@@ -47,26 +47,40 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
-__device__ __forceinline__ void bf16x8_to_f(const uint4& u, float (&f)[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(b[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-
 __device__ __forceinline__ bool seq_in_range(int p0, int K, int max_pos) {
   return p0 >= 0 && p0 <= max_pos - 1 - K;
+}
+
+// Exclusive scan over the block of one value per thread; returns the
+// thread's prefix and sets *total.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_scan, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();  // s_scan is free
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  int base = 0, all = 0;
+  for (int w = 0; w < kNormThreads / 32; ++w) {
+    if (w < warp) base += s_scan[w];
+    all += s_scan[w];
+  }
+  *total = all;
+  return base + incl - v;
 }
 
 // Layer 0, block 0: the attention's (sequence, split) pairs for this step.
 // keys_b = pos_b + K + 1 (0 for a sequence out of range); the split width is
 // the larger of the total keys x heads over the wanted items and the longest
 // sequence over kAttnMaxSplits, rounded up to a whole number of chunks
-// (max_split keys, or 64 below one chunk) and kept in [64, 1024]; a
-// sequence's pairs are consecutive, in split order.
+// (max_split keys, or 64 below one chunk) and kept in [64, 1024].  The pairs
+// are laid out longest first (by chunks, then sequence and split), so that
+// the CTAs that claim them in order end together; seqbase[b] (the splits of
+// the sequences before b) places each split's partial result.
 __device__ void build_plan(const AttnNormParams& p) {
   __shared__ long long s_tot[kNormThreads / 32];
   __shared__ int s_max[kNormThreads / 32];
@@ -109,41 +123,54 @@ __device__ void build_plan(const AttnNormParams& p) {
     s_width = (int)c;
   }
   __syncthreads();
-  const int C = s_width;
-  // contiguous runs of sequences per thread, then an exclusive scan of the
-  // runs' pair counts over the block
+  const int C = s_width, Cm = p.max_split;
+  const int maxc = (C + Cm - 1) / Cm;  // chunks of a full split
+  // contiguous runs of sequences per thread
   const int per = (p.B + kNormThreads - 1) / kNormThreads;
   const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-  int mine = 0;
-  for (int b = b0; b < b1; ++b) {
+  auto splits = [&](int b, int* last_chunks) {
     const int p0 = p.positions[b];
-    if (seq_in_range(p0, p.K, p.max_pos)) mine += (p0 + p.K + 1 + C - 1) / C;
-  }
-  int incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) s_scan[warp] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int w = 0; w < warp; ++w) base += s_scan[w];
-  int at = base + incl - mine;
+    if (!seq_in_range(p0, p.K, p.max_pos)) return 0;
+    const int keys = p0 + p.K + 1, n = (keys + C - 1) / C;
+    *last_chunks = (keys - (n - 1) * C + Cm - 1) / Cm;
+    return n;
+  };
+  int* seqbase = p.plan + 2 + 2 * p.cap_pairs;
+  int mine = 0, total = 0, lc = 0;
+  for (int b = b0; b < b1; ++b) mine += splits(b, &lc);
+  int at = block_excl_scan(mine, s_scan, &total);
   for (int b = b0; b < b1; ++b) {
-    const int p0 = p.positions[b];
-    if (!seq_in_range(p0, p.K, p.max_pos)) continue;
-    const int n = (p0 + p.K + 1 + C - 1) / C;
-    for (int s = 0; s < n; ++s, ++at) {
-      if (at < p.cap_pairs) {
-        p.plan[2 + 2 * at] = b;
-        p.plan[3 + 2 * at] = s;
+    seqbase[b] = at;
+    at += splits(b, &lc);
+  }
+  // the pairs, by chunks from maxc down to 1
+  int placed = 0;
+  for (int nb = maxc; nb >= 1; --nb) {
+    int cnt = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int n = splits(b, &lc);
+      if (n == 0) continue;
+      cnt += (nb == maxc ? n - 1 : 0) + (lc == nb ? 1 : 0);
+    }
+    int bucket = 0;
+    int w = placed + block_excl_scan(cnt, s_scan, &bucket);
+    for (int b = b0; b < b1; ++b) {
+      const int n = splits(b, &lc);
+      if (n == 0) continue;
+      for (int s = 0; s < n; ++s) {
+        const int ch = s + 1 < n ? maxc : lc;
+        if (ch != nb) continue;
+        if (w < p.cap_pairs) {
+          p.plan[2 + 2 * w] = b;
+          p.plan[3 + 2 * w] = s;
+        }
+        ++w;
       }
     }
+    placed += bucket;
   }
   for (int l = tid; l < p.n_item_ctr; l += kNormThreads) p.item_ctr[l] = 0;
-  if (tid == kNormThreads - 1) {
-    const int total = base + incl;
+  if (tid == 0) {
     if (total > p.cap_pairs) atomicOr(p.status, kErrInternal);  // not reachable by the sizing
     p.plan[0] = C;
     p.plan[1] = min(total, p.cap_pairs);
@@ -246,21 +273,25 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
   lo = pack_bf16(x - hf.x, y - hf.y);
 }
 
+// An item: split s (keys k0 .. k0 + n - 1, `chunks` chunks) of sequence b,
+// head hh; its partial result's slot among the step's splits, and the slot of
+// its sequence's split 0 (the splits of a sequence have consecutive slots).
 struct AttnItem {
-  int b, s, hh, k0, n, keys, nsplit, pair, chunks;
+  int b, s, hh, k0, n, keys, nsplit, chunks, slot0;
 };
 
 __device__ __forceinline__ AttnItem attn_item(const AttnParams& p, int C, int item) {
   AttnItem it;
-  it.pair = item / p.H;
-  it.hh = item - it.pair * p.H;
-  it.b = p.plan[2 + 2 * it.pair];
-  it.s = p.plan[3 + 2 * it.pair];
+  const int pair = item / p.H;
+  it.hh = item - pair * p.H;
+  it.b = p.plan[2 + 2 * pair];
+  it.s = p.plan[3 + 2 * pair];
   it.keys = p.positions[it.b] + p.K + 1;
   it.k0 = it.s * C;
   it.n = min(it.keys, it.k0 + C) - it.k0;
   it.nsplit = (it.keys + C - 1) / C;
   it.chunks = (it.n + p.max_split - 1) / p.max_split;
+  it.slot0 = p.plan[2 + 2 * p.cap_pairs + it.b];
   return it;
 }
 
@@ -284,15 +315,19 @@ __device__ __forceinline__ void attn_issue(const CUtensorMap* map_k, const CUten
   }
 }
 
-// Persistent, one CTA per SM, 8 warps.  Items (sequence, split, head) are
-// claimed in order from a per-layer counter, one item ahead of use, so CTAs
-// that stream faster take more of them.  An item's keys and values stream
-// through a ring of kAttnStages shared-memory buffers in chunks of max_split
-// keys (2-D TMA boxes with the hardware swizzle), one thread keeping the next
-// chunks in flight while the CTA works on the current one.  Each warp takes its
-// share of a chunk's keys, 16 at a time, on the tensor cores (mma.sync
-// m16n8k16) with the keys and the head's dims on the 16-row side and the
-// item's queries (8 per tile, NQT tiles) as the columns:
+// Persistent, one CTA per SM: 8 compute warps and one loading warp.  The
+// loading warp claims items (sequence, split, head) in order from a per-layer
+// counter, one item ahead, so CTAs that stream faster take more of them, and
+// streams each item's keys and values through a ring of kAttnStages
+// shared-memory buffers in chunks of max_split keys (2-D TMA boxes with the
+// hardware swizzle), tagging each buffer with its (item, chunk); a buffer is
+// refilled once the eight compute warps have released it.  It also publishes
+// each claimed item's (sequence, head) one item ahead, so that the compute
+// warps copy the next item's queries into shared memory while they work on
+// the current one.  Each compute warp
+// takes its share of a chunk's keys, 16 at a time, on the tensor cores
+// (mma.sync m16n8k16) with the keys and the head's dims on the 16-row side and
+// the item's queries (8 per tile, NQT tiles) as the columns:
 //   S^T = K Q^T     K bf16 (exact), Q fp32 as the sum of two bf16 parts
 //   online softmax per query column in the log2 domain (running max and sum)
 //   O^T += V^T P^T  V bf16 (exact), P fp32 as two bf16 parts, moved from the
@@ -300,39 +335,43 @@ __device__ __forceinline__ void attn_issue(const CUtensorMap* map_k, const CUten
 //                   transpose in registers
 // so the products are those of fp32 operands to ~2^-16, accumulated in fp32.
 // At the end of an item the warps' (max, sum, O) are merged in warp order
-// (their O staged in the buffer of the item's last chunk, free until the ring
-// comes round to it); a split's result is merged with its sequence's other
-// splits by the last of them to finish, in split order.
+// (their O staged in the buffer of the item's last chunk, released only
+// afterwards); a split's result is merged with its sequence's other splits by
+// the last of them to finish, in split order.
 template <int HD, int NQT>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads + 32, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const AttnParams p) {
   constexpr int KS = HD / 16;                 // k-steps of K Q^T, m-tiles of V^T P^T
   constexpr int NQ = 8 * NQT;                 // query columns
   constexpr int BW = HD < 64 ? HD : 64;       // box width (elements)
   constexpr uint32_t RB = BW * 2;             // box row bytes
-  constexpr int kRing = kAttnStages + 1;      // items between claim and use
   extern __shared__ uint8_t attn_raw[];
   __shared__ int s_last;
   __shared__ int s_abort;
-  __shared__ int s_item[kRing];
+  __shared__ int2 s_tag[kAttnStages];         // (item, chunk) of each buffer; item < 0: end
+  constexpr int kClaims = 8;
+  __shared__ AttnItem s_claim[kClaims];       // claimed item k (b < 0: none)
   uint8_t* kv = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_raw) + 1023) &
                                            ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
   const int K1 = p.K + 1, Cm = p.max_split;
   const uint32_t box = (uint32_t)Cm * RB, tile = (HD / BW) * box;
-  float* qs = reinterpret_cast<float*>(kv + 2 * kAttnStages * (size_t)tile);  // [NQ][HD]
-  float* mst = qs + NQ * HD;                                     // [8][NQ]
+  float* qs = reinterpret_cast<float*>(kv + 2 * kAttnStages * (size_t)tile);  // [2][NQ][HD]
+  float* mst = qs + 2 * NQ * HD;                                 // [8][NQ]
   float* lst = mst + kAttnWarps * NQ;                            // [8][NQ]
   float* wst = lst + kAttnWarps * NQ;                            // [8][NQ] warp weights
   float* wsp = wst + kAttnWarps * NQ;                            // [16][kAttnMaxSplits]
   float* tot = wsp + 16 * kAttnMaxSplits;                        // [16]
-  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 16);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 16);        // [kAttnStages]
+  uint64_t* empty = full + kAttnStages;                          // [kAttnStages]
   if (tid == 0) {
     stamp_min(p.stamps);
     s_abort = 0;
-    for (int b = 0; b < kAttnStages; ++b) mbar_init(&full[b], 1);
+    for (int b = 0; b < kAttnStages; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kAttnWarps);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
@@ -342,91 +381,127 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   pdl_launch_dependents();
   if (tid == 0 && p.stamps) stamp_max(p.stamps + 1);
   const int C = p.plan[0], n_items = p.plan[1] * p.H;
-  const int kpw = Cm / kAttnWarps;  // keys per warp and chunk (a multiple of 16)
-  const uint64_t pol = policy_evict_first();
-  // thread 0: the item whose chunks are being loaded (< 0: none left), its
-  // next chunk, the items claimed and the loads issued so far, and the buffers
-  // with a load not yet waited for (bit b)
-  int nx_item = -1, nx_chunk = 0, claimed = 0, issued = 0;
-  uint32_t pending = 0;
-  AttnItem nx;
-  auto claim = [&]() {
-    const int it = atomicAdd(p.item_ctr, 1);
-    nx_item = it < n_items ? it : -1;
-    s_item[claimed % kRing] = nx_item;
-    ++claimed;
-    if (nx_item >= 0) nx = attn_item(p, C, nx_item);
-    nx_chunk = 0;
-  };
-  auto issue_next = [&]() {
-    attn_issue<HD>(&map_k, &map_v, p, kv, full, nx, nx_chunk, issued % kAttnStages, pol);
-    pending |= 1u << (issued % kAttnStages);
-    ++issued;
-    if (++nx_chunk == nx.chunks) claim();
-  };
-  if (tid == 0) {
-    claim();
-    for (int k = 0; k < kAttnStages - 1 && nx_item >= 0; ++k) issue_next();
-  }
-  __syncthreads();
-  int u = 0;  // chunks consumed so far by this CTA
-  bool aborted = false;
-  for (int m = 0; !aborted; ++m) {
-    const int item = s_item[m % kRing];
-    if (item < 0) break;
-    const AttnItem it = attn_item(p, C, item);
-    const int p0 = it.keys - K1;
-    // Q of the item's queries into shared memory (rows >= K + 1 zero), then
-    // as B fragments (pre-scaled to the log2 domain), hi and lo bf16 parts
-    {
-      const float* qb = p.q + (size_t)(it.b * K1) * p.d + it.hh * HD;
-      for (int i = tid; i < NQ * HD / 4; i += kAttnThreads) {
-        const int row = i / (HD / 4), c4 = i - row * (HD / 4);
-        reinterpret_cast<float4*>(qs)[i] =
-            row < K1 ? __ldcg(reinterpret_cast<const float4*>(qb + (size_t)row * p.d) + c4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    __syncthreads();
-    uint32_t qh[NQT][KS][2], ql[NQT][KS][2];
-#pragma unroll
-    for (int nq = 0; nq < NQT; ++nq)
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float2 v =
-              *reinterpret_cast<const float2*>(qs + (nq * 8 + g) * HD + ks * 16 + r * 8 + 2 * t4);
-          split_bf16(v.x * p.scale_log2, v.y * p.scale_log2, qh[nq][ks][r], ql[nq][ks][r]);
-        }
-    // O^T [dims x queries] fragments; per query column of this lane (2 t4 + e
-    // of each query tile) the running max and this lane's part of the sum
-    float O[KS][NQT][4];
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-      for (int nq = 0; nq < NQT; ++nq) O[mt][nq][0] = O[mt][nq][1] = O[mt][nq][2] = O[mt][nq][3] = 0.f;
-    float mq[NQT][2], lq[NQT][2];
-#pragma unroll
-    for (int nq = 0; nq < NQT; ++nq) {
-      mq[nq][0] = mq[nq][1] = -INFINITY;
-      lq[nq][0] = lq[nq][1] = 0.f;
-    }
 
-    int last_buf = 0;
-    for (int c = 0; c < it.chunks; ++c, ++u) {
-      const int buf = u % kAttnStages;
-      last_buf = buf;
-      // the buffer of chunk u - 1 (finished by every thread) takes the next load
-      if (tid == 0 && nx_item >= 0) issue_next();
-      // a wait that gives up raises s_abort; the barrier makes the CTA leave together
-      mbar_wait(&full[buf], (uint32_t)((u / kAttnStages) & 1), &s_abort, p.status);
-      __syncthreads();
-      if (s_abort) {
-        aborted = true;
-        break;
+  if (warp == kAttnWarps) {
+    // ------------------------------------------------ loading warp
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = 0, k = 0;
+      bool ok = true;
+      // the claimed item and the one claimed after it (published before the
+      // first one's chunks are loaded)
+      int cur = atomicAdd(p.item_ctr, 1);
+      int nxt = cur < n_items ? atomicAdd(p.item_ctr, 1) : n_items;
+      AttnItem it = {};
+      if (cur < n_items) it = attn_item(p, C, cur);
+      if (cur >= n_items) it.b = -1;
+      s_claim[0] = it;
+      while (ok && cur < n_items) {
+        AttnItem itn = {};
+        itn.b = -1;
+        if (nxt < n_items) itn = attn_item(p, C, nxt);
+        ++k;
+        s_claim[k % kClaims] = itn;
+        for (int c = 0; c < it.chunks; ++c, ++issued) {
+          const int b = issued % kAttnStages;
+          if (!mbar_wait(&empty[b], (uint32_t)(((issued / kAttnStages) & 1) ^ 1), &s_abort,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          s_tag[b] = make_int2(cur, c);
+          attn_issue<HD>(&map_k, &map_v, p, kv, full, it, c, b, pol);
+        }
+        cur = nxt;
+        it = itn;
+        if (cur < n_items) nxt = atomicAdd(p.item_ctr, 1);
       }
-      if (tid == 0) pending &= ~(1u << buf);
+      if (ok) {
+        // the end: a buffer tagged with no item, completed by a plain arrival
+        const int b = issued % kAttnStages;
+        if (mbar_wait(&empty[b], (uint32_t)(((issued / kAttnStages) & 1) ^ 1), &s_abort,
+                      p.status)) {
+          s_tag[b] = make_int2(-1, 0);
+          mbar_arrive(&full[b]);
+        }
+      } else {
+        // let the loads already issued land before the CTA exits
+        for (int v = issued - kAttnStages; v < issued; ++v) {
+          if (v < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[v % kAttnStages], (uint32_t)((v / kAttnStages) & 1)) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ compute warps 0..7
+    const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    const int kpw = Cm / kAttnWarps;  // keys per warp and chunk (a multiple of 16)
+    auto bar = [] { named_bar_sync(1, kAttnThreads); };
+    uint32_t qh[NQT][KS][2], ql[NQT][KS][2];
+    float O[KS][NQT][4];
+    float mq[NQT][2], lq[NQT][2];
+    AttnItem it = {};
+    int item = -1, p0 = 0, m = -1;
+    // rows K + 1 .. NQ - 1 of both query buffers stay zero
+    for (int i = tid; i < 2 * NQ * HD; i += kAttnThreads) qs[i] = 0.f;
+    // the queries of an item (sequence b, head hh) into query buffer qb, one
+    // 16-byte copy per thread and pass
+    auto fetch_q = [&](int b, int hh, float* qb) {
+      const float* src = p.q + (size_t)(b * K1) * p.d + hh * HD;
+      for (int i = tid; i < K1 * HD / 4; i += kAttnThreads) {
+        const int row = i / (HD / 4), c4 = i - row * (HD / 4);
+        cp_async16(qb + row * HD + 4 * c4, src + (size_t)row * p.d + 4 * c4);
+      }
+      cp_async_commit();
+    };
+    for (int u = 0;; ++u) {
+      const int buf = u % kAttnStages;
+      // a wait that gives up raises s_abort; the barrier makes the warps leave together
+      mbar_wait(&full[buf], (uint32_t)((u / kAttnStages) & 1), &s_abort, p.status);
+      bar();
+      if (s_abort) break;
+      const int2 tag = s_tag[buf];
+      if (tag.x < 0) break;
+      const int c = tag.y;
+      if (c == 0) {
+        // a new item (the CTA's m-th): its queries are in query buffer m % 2
+        // (copied while the previous item ran; the first item's now), and
+        // the next item's are copied into the other buffer meanwhile; then as
+        // B fragments (pre-scaled to the log2 domain), hi and lo bf16 parts
+        item = tag.x;
+        ++m;
+        it = s_claim[m % kClaims];  // published before the item's first chunk
+        p0 = it.keys - K1;
+        float* qcur = qs + (m & 1) * NQ * HD;
+        if (m == 0) fetch_q(it.b, it.hh, qcur);
+        cp_async_wait_all();
+        bar();
+        const AttnItem& nx = s_claim[(m + 1) % kClaims];
+        if (nx.b >= 0) fetch_q(nx.b, nx.hh, qs + ((m + 1) & 1) * NQ * HD);
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float2 v = *reinterpret_cast<const float2*>(qcur + (nq * 8 + g) * HD + ks * 16 +
+                                                                r * 8 + 2 * t4);
+              split_bf16(v.x * p.scale_log2, v.y * p.scale_log2, qh[nq][ks][r], ql[nq][ks][r]);
+            }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq)
+            O[mt][nq][0] = O[mt][nq][1] = O[mt][nq][2] = O[mt][nq][3] = 0.f;
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq) {
+          mq[nq][0] = mq[nq][1] = -INFINITY;
+          lq[nq][0] = lq[nq][1] = 0.f;
+        }
+      }
       const uint8_t* Kt = kv + (size_t)buf * 2 * tile;
       const uint8_t* Vt = Kt + tile;
       const int n = min(Cm, it.n - c * Cm);  // keys of this chunk
@@ -516,131 +591,126 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
-      __syncthreads();  // the buffer is reloaded kAttnStages - 1 chunks on
-    }
-    if (aborted) break;
-
-    // ---- the warps' states, then merged in warp order; O^T goes to the
-    // buffer of the item's last chunk (the next load into it is issued at the
-    // start of the next chunk, after this item) as [8][NQ][HD]
-    float* ost = reinterpret_cast<float*>(kv + (size_t)last_buf * 2 * tile);
-#pragma unroll
-    for (int nq = 0; nq < NQT; ++nq)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 4);
-        lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 8);
-        lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 16);
-        if (g == 0) {
-          mst[warp * NQ + nq * 8 + 2 * t4 + h] = mq[nq][h];
-          lst[warp * NQ + nq * 8 + 2 * t4 + h] = lq[nq][h];
-        }
+      if (c + 1 < it.chunks) {
+        // release the buffer to the loading warp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[buf]);
+        continue;
       }
-    float* ow = ost + (size_t)warp * NQ * HD;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
+
+      // ---- end of the item: the warps' states, then merged in warp order;
+      // O^T goes to this (last) chunk's buffer as [8][NQ][HD], released after
+      float* ost = reinterpret_cast<float*>(kv + (size_t)buf * 2 * tile);
 #pragma unroll
       for (int nq = 0; nq < NQT; ++nq)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          ow[(nq * 8 + 2 * t4 + (e & 1)) * HD + mt * 16 + g + ((e & 2) ? 8 : 0)] = O[mt][nq][e];
-    __syncthreads();
-    if (tid < NQ) {
-      // per query: the merged max and sum, and each warp's weight
-      float M = -INFINITY;
-      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mst[w * NQ + tid]);
-      float L = 0.f;
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float mw = mst[w * NQ + tid];
-        const float ww = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        wst[w * NQ + tid] = ww;
-        L = fmaf(lst[w * NQ + tid], ww, L);
-      }
-      mst[tid] = M;  // warp 0's slots now hold the merged values
-      lst[tid] = L;
-    }
-    __syncthreads();
-    const int outs = K1 * HD;
-    if (it.nsplit == 1) {
-      for (int i = tid; i < outs; i += kAttnThreads) {
-        const int j = i / HD, dim = i - j * HD;
-        float a = 0.f;
-        for (int w = 0; w < kAttnWarps; ++w)
-          a = fmaf(ost[((size_t)w * NQ + j) * HD + dim], wst[w * NQ + j], a);
-        p.o[(size_t)(it.b * K1 + j) * p.d + it.hh * HD + dim] = __float2bfloat16_rn(a / lst[j]);
-      }
-    } else {
-      // this split's (max, sum, unnormalised output) per query
-      const int pitch = HD + 2;
-      float* mine = p.part + (size_t)item * K1 * pitch;
-      for (int i = tid; i < outs; i += kAttnThreads) {
-        const int j = i / HD, dim = i - j * HD;
-        float a = 0.f;
-        for (int w = 0; w < kAttnWarps; ++w)
-          a = fmaf(ost[((size_t)w * NQ + j) * HD + dim], wst[w * NQ + j], a);
-        mine[j * pitch + 2 + dim] = a;
-      }
-      for (int j = tid; j < K1; j += kAttnThreads) {
-        mine[j * pitch] = mst[j];
-        mine[j * pitch + 1] = lst[j];
-      }
-      // the CTA's writes, ordered by the barrier, released by one fence
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(p.arrive + it.b * p.H + it.hh, 1) == it.nsplit - 1;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        // merge the splits in order: item of split s' = (pair - s + s') * H + hh
-        const int first = (it.pair - it.s) * p.H + it.hh;
-        for (int j = warp; j < K1; j += kAttnWarps) {
-          float M = -INFINITY;
-          for (int q = lane; q < it.nsplit; q += 32) {
-            const float* pq = p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch;
-            if (__ldcg(pq + 1) > 0.f) M = fmaxf(M, __ldcg(pq));
+        for (int h = 0; h < 2; ++h) {
+          lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 4);
+          lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 8);
+          lq[nq][h] += __shfl_xor_sync(0xffffffffu, lq[nq][h], 16);
+          if (g == 0) {
+            mst[warp * NQ + nq * 8 + 2 * t4 + h] = mq[nq][h];
+            lst[warp * NQ + nq * 8 + 2 * t4 + h] = lq[nq][h];
           }
-          M = warp_max_f(M);
-          float Ls = 0.f;
-          for (int q = lane; q < it.nsplit; q += 32) {
-            const float* pq = p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch;
-            const float lsp = __ldcg(pq + 1);
-            const float wq = lsp > 0.f ? exp2f(__ldcg(pq) - M) : 0.f;
-            wsp[j * kAttnMaxSplits + q] = wq;
-            Ls = fmaf(lsp, wq, Ls);
-          }
-          Ls = warp_sum_f(Ls);
-          if (lane == 0) tot[j] = Ls;
         }
-        __syncthreads();
+      bar();  // every warp is done with the buffer's keys and values
+      float* ow = ost + (size_t)warp * NQ * HD;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ow[(nq * 8 + 2 * t4 + (e & 1)) * HD + mt * 16 + g + ((e & 2) ? 8 : 0)] = O[mt][nq][e];
+      bar();
+      if (tid < NQ) {
+        // per query: the merged max and sum, and each warp's weight
+        float M = -INFINITY;
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mst[w * NQ + tid]);
+        float L = 0.f;
+        for (int w = 0; w < kAttnWarps; ++w) {
+          const float mw = mst[w * NQ + tid];
+          const float ww = mw == -INFINITY ? 0.f : exp2f(mw - M);
+          wst[w * NQ + tid] = ww;
+          L = fmaf(lst[w * NQ + tid], ww, L);
+        }
+        mst[tid] = M;  // warp 0's slots now hold the merged values
+        lst[tid] = L;
+      }
+      bar();
+      const int outs = K1 * HD;
+      if (it.nsplit == 1) {
         for (int i = tid; i < outs; i += kAttnThreads) {
           const int j = i / HD, dim = i - j * HD;
-          float A = 0.f;
-#pragma unroll 4
-          for (int q = 0; q < it.nsplit; ++q)
-            A = fmaf(__ldcg(p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch + 2 + dim),
-                     wsp[j * kAttnMaxSplits + q], A);
-          p.o[(size_t)(it.b * K1 + j) * p.d + it.hh * HD + dim] = __float2bfloat16_rn(A / tot[j]);
+          float a = 0.f;
+          for (int w = 0; w < kAttnWarps; ++w)
+            a = fmaf(ost[((size_t)w * NQ + j) * HD + dim], wst[w * NQ + j], a);
+          p.o[(size_t)(it.b * K1 + j) * p.d + it.hh * HD + dim] = __float2bfloat16_rn(a / lst[j]);
         }
-        if (tid == 0) p.arrive[it.b * p.H + it.hh] = 0;
+      } else {
+        // this split's (max, sum, unnormalised output) per query
+        const int pitch = HD + 2;
+        float* mine = p.part + ((size_t)(it.slot0 + it.s) * p.H + it.hh) * K1 * pitch;
+        for (int i = tid; i < outs; i += kAttnThreads) {
+          const int j = i / HD, dim = i - j * HD;
+          float a = 0.f;
+          for (int w = 0; w < kAttnWarps; ++w)
+            a = fmaf(ost[((size_t)w * NQ + j) * HD + dim], wst[w * NQ + j], a);
+          mine[j * pitch + 2 + dim] = a;
+        }
+        for (int j = tid; j < K1; j += kAttnThreads) {
+          mine[j * pitch] = mst[j];
+          mine[j * pitch + 1] = lst[j];
+        }
+        // the warps' writes, ordered by the barrier, released by one fence
+        bar();
+        if (tid == 0) {
+          __threadfence();
+          s_last = atomicAdd(p.arrive + it.b * p.H + it.hh, 1) == it.nsplit - 1;
+        }
+        bar();
+        if (s_last) {
+          __threadfence();
+          // merge the splits in order: split s' in slot (slot0 + s') * H + hh
+          const int first = it.slot0 * p.H + it.hh;
+          for (int j = warp; j < K1; j += kAttnWarps) {
+            float M = -INFINITY;
+            for (int q = lane; q < it.nsplit; q += 32) {
+              const float* pq = p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch;
+              if (__ldcg(pq + 1) > 0.f) M = fmaxf(M, __ldcg(pq));
+            }
+            M = warp_max_f(M);
+            float Ls = 0.f;
+            for (int q = lane; q < it.nsplit; q += 32) {
+              const float* pq = p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch;
+              const float lsp = __ldcg(pq + 1);
+              const float wq = lsp > 0.f ? exp2f(__ldcg(pq) - M) : 0.f;
+              wsp[j * kAttnMaxSplits + q] = wq;
+              Ls = fmaf(lsp, wq, Ls);
+            }
+            Ls = warp_sum_f(Ls);
+            if (lane == 0) tot[j] = Ls;
+          }
+          bar();
+          for (int i = tid; i < outs; i += kAttnThreads) {
+            const int j = i / HD, dim = i - j * HD;
+            float A = 0.f;
+#pragma unroll 4
+            for (int q = 0; q < it.nsplit; ++q)
+              A = fmaf(
+                  __ldcg(p.part + (size_t)(first + q * p.H) * K1 * pitch + j * pitch + 2 + dim),
+                  wsp[j * kAttnMaxSplits + q], A);
+            p.o[(size_t)(it.b * K1 + j) * p.d + it.hh * HD + dim] =
+                __float2bfloat16_rn(A / tot[j]);
+          }
+          if (tid == 0) p.arrive[it.b * p.H + it.hh] = 0;
+        }
       }
-    }
-    __syncthreads();  // the warps' states, Q and the merge scratch are reused
-  }
-  // a wait that gave up: let the loads already issued land before the CTA
-  // exits (chunk v went to buffer v % kAttnStages; the loads of chunks u ..
-  // issued - 1 were not waited for)
-  if (tid == 0) {
-    for (int v = u; v < issued; ++v) {
-      const int b = v % kAttnStages;
-      if (!(pending & (1u << b))) continue;
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&full[b], (uint32_t)((v / kAttnStages) & 1)) &&
-             globaltimer_ns() - t0 < kWaitLimitNs) {
-      }
+      bar();  // the warps' states, Q and the merge scratch are reused
+      if (lane == 0) mbar_arrive(&empty[buf]);
     }
   }
+  __syncthreads();
   if (tid == 0 && p.stamps) stamp_max(p.stamps + 2);
 }
 
@@ -692,7 +762,7 @@ cudaError_t launch_attn_t(const CUtensorMap& map_k, const CUtensorMap& map_v, co
   auto kern = attn_kernel<HD, NQT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), smem, s, pdl, map_k, map_v, p);
+  return launch_pdl(kern, dim3(grid), dim3(kAttnThreads + 32), smem, s, pdl, map_k, map_v, p);
 }
 
 template <int HD>
@@ -707,8 +777,8 @@ cudaError_t launch_attn_hd(const CUtensorMap& map_k, const CUtensorMap& map_v, c
 size_t attn_smem_bytes(int hd, int nq) {
   const size_t cm = (size_t)attn_max_split(hd);
   return 1024 /* alignment */ + 2 * kAttnStages * cm * hd * 2 +
-         ((size_t)nq * hd + 3 * kAttnWarps * nq + 16 * kAttnMaxSplits + 16) * sizeof(float) +
-         kAttnStages * sizeof(uint64_t);
+         ((size_t)2 * nq * hd + 3 * kAttnWarps * nq + 16 * kAttnMaxSplits + 16) * sizeof(float) +
+         2 * kAttnStages * sizeof(uint64_t);
 }
 
 cudaError_t launch_attn_norm(const AttnNormParams& p, cudaStream_t s, bool pdl) {

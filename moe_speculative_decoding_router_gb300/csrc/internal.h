@@ -160,8 +160,9 @@ struct AttnNormParams {
   int32_t* bad;                // [T]
   uint32_t* status;
   // work items of the attention (written by layer 0's block 0): plan[0] =
-  // keys per split, plan[1] = (sequence, split) pairs, then the pairs as
-  // plan[2 + 2i] = sequence, plan[3 + 2i] = split
+  // keys per split, plan[1] = (sequence, split) pairs, then the pairs in claim
+  // order as plan[2 + 2i] = sequence, plan[3 + 2i] = split, then from plan[2 +
+  // 2 cap_pairs] each sequence's first split slot (the splits before it)
   int32_t* plan;
   int target_items;            // wanted (sequence, split, head) items
   int max_split;               // attn_max_split(hd): keys per chunk
@@ -209,6 +210,7 @@ struct AttnParams {
   float* part;                 // [cap items, K+1, hd + 2] split results (m, l, acc)
   int32_t* arrive;             // [Bmax, H] finished splits (zero on entry; the merger resets)
   int32_t* item_ctr;           // items claimed so far (zero on entry: cleared by layer 0's attn_norm)
+  int cap_pairs;               // room in plan for pairs (the per-sequence slots follow them)
   uint32_t* status;
   unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
 };

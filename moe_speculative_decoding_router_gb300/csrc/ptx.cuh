@@ -179,6 +179,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Asynchronous 16-byte copy global -> shared by one thread (L1 bypassed);
+// cp_async_wait_all waits for the calling thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Bulk prefetch of [src, src + bytes) into L2 (no completion tracking).
 // Address 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
