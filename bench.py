@@ -422,7 +422,7 @@ def run_ours(args, rank, world, local):
                                             dist, clocks)
 
     if args.profile and args.attn:
-        line = run_attn(w_host, args, dev, peaks, B=Bq, K=Kq)
+        line = run_attn(w_host, args, dev, peaks, B=Bq, K=Kq, layers=args.layers)
         line["clocks"] = clk
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -724,7 +724,7 @@ def run_sweep(ctx, cfg, g, rank, dev, peaks, warmup=3, steps=10):
 ATTN_LO, ATTN_HI = 512, 4096
 
 
-def run_attn(w_host, args, dev, peaks, B=32, K=3, lo=ATTN_LO, hi=ATTN_HI, steps=None):
+def run_attn(w_host, args, dev, peaks, B=32, K=3, lo=ATTN_LO, hi=ATTN_HI, steps=None, layers=0):
     """The stack with attention (the library's reading of the decoder's
     unspecified attention: 10 heads of 128, rotary positions, a bf16 key/value
     cache), B=32 sequences at positions drawn uniformly from [512, 4096), K=3
@@ -735,9 +735,10 @@ def run_attn(w_host, args, dev, peaks, B=32, K=3, lo=ATTN_LO, hi=ATTN_HI, steps=
     step, each kernel's in-graph time per launch, and the attention kernel's
     roofline: its bytes are every cached key and value of the sequences'
     positions once, plus q read and the output written."""
+    import dataclasses
     import torch
     from moe_speculative_decoding_router_gb300 import binding as BND
-    cfg = S.FULL_ATTN
+    cfg = S.FULL_ATTN if not layers else dataclasses.replace(S.FULL_ATTN, n_layers=layers)
     L, d = cfg.n_layers, cfg.hidden
     steps = steps or args.steps
     w = dict(w_host)
@@ -1044,8 +1045,8 @@ def main():
             or args.zipf or args.attn) and not args.profile:
         ap.error("--layers, --batch, --drafts, --zipf, --draft-head and --attn are for "
                  "profiling runs only (--profile)")
-    if args.attn and (args.layers or args.zipf or args.draft_head):
-        ap.error("--attn runs the full stack without the Zipf bias or the draft head")
+    if args.attn and (args.zipf or args.draft_head):
+        ap.error("--attn runs the stack without the Zipf bias or the draft head")
     if args.draft_head and (args.layers or (args.drafts is not None and args.drafts < 1)):
         ap.error("--draft-head needs the full stack and at least one draft")
     if args.drafts is not None and not 0 <= args.drafts <= 15:
