@@ -416,3 +416,72 @@ def test_full_attn_graph_capture(full_attn):
         torch.cuda.synchronize()
         assert torch.equal(out, direct)
     assert ctx.sync_status() == 0
+
+
+# ------------------------------------------------------------- other shapes
+
+@pytest.mark.parametrize("n_heads", [1, 2])
+def test_tiny_attn_other_head_widths(n_heads):
+    """Head widths 64 (one 128-byte swizzled box per key row) and 32 (the
+    64-byte swizzle): prompts of 48 in calls of 4, every target and the cache
+    against the oracle."""
+    import dataclasses
+    B_ = _B()
+    cfg = dataclasses.replace(S.TINY_ATTN, n_heads=n_heads, name=f"tiny_attn_h{n_heads}")
+    w = S.make_weights(cfg)
+    ctx = B_.MoeVerify(cfg, B_.weights_to_device(w), max_batch=3, max_k=3, max_pos=64)
+    try:
+        orc = O.Oracle(cfg, w)
+        n = 48
+        seqs = _prompts(3, n, cfg.vocab, first=11000 + n_heads)
+        tg, _ = _feed(ctx, seqs, 3)
+        refs = _oracle_seqs(orc, seqs, caches=True)
+        _compare_free(tg, refs, 0, f"attn tiny hd={cfg.hidden // n_heads} prompts")
+        kc, vc = _cache_np(ctx)
+        L, d = cfg.n_layers, cfg.hidden
+        for b, r in enumerate(refs):
+            for name, gpu, ref in (("key", kc, r["kcache"]), ("value", vc, r["vcache"])):
+                g = parity._bf16_to_f64(gpu[:, b, :, :n, :]).transpose(0, 2, 1, 3).reshape(L, n, d)
+                bad = parity.kv_within(g, ref, REL)
+                assert bad[0].size == 0, f"{name} cache, sequence {b}"
+    finally:
+        ctx.close()
+
+
+@pytest.fixture(scope="module")
+def full_attn_long():
+    B_ = _B()
+    cfg = S.FULL_ATTN
+    w = S.make_weights(cfg)
+    ctx = B_.MoeVerify(cfg, B_.weights_to_device(w), max_batch=4, max_k=15, max_pos=2304)
+    torch.cuda.empty_cache()
+    yield ctx, O.Oracle(cfg, w)
+    ctx.close()
+
+
+def test_full_attn_long_context_teacher_forced(full_attn_long):
+    """Full size at ~2,000 positions: four prompts of 2,048 tokens fed in calls
+    of 16, then one call per sequence at a different position; with 4
+    sequences the split width is 256 keys, so each sequence's keys span ~8
+    splits merged by the last to finish.  Every token of the last call is
+    checked teacher-forced (attention part, MoE part, routing, target) on the
+    GPU's residual stream and cache."""
+    ctx, orc = full_attn_long
+    B_ = _B()
+    Bn, K, n = 4, 15, 2048
+    seqs = _prompts(Bn, n, orc.cfg.vocab, first=12 * 10 ** 6)
+    _feed(ctx, seqs, K)
+    pos0 = np.array([n - 16, n - 16 - 333, n - 16 - 1000, 700])
+    new = _prompts(Bn, K + 1, orc.cfg.vocab, first=13 * 10 ** 6)
+    probe, pt = B_.make_probe(orc.cfg.n_layers, Bn * (K + 1), orc.cfg)
+    tg = ctx.step_attn(_i32(new[:, 0]), _i32(new[:, 1:]), _i32(pos0), probe=probe)
+    assert ctx.sync_status() == 0
+    kc, vc = _cache_np(ctx)
+    ids = new.reshape(-1)
+    seq = np.repeat(np.arange(Bn), K + 1)
+    pos = np.repeat(pos0, K + 1) + np.tile(np.arange(K + 1), Bn)
+    sample = sorted(set(range(0, Bn * (K + 1), 5)) | {K, 2 * K + 1, Bn * (K + 1) - 1})
+    check_attn_tokens(orc, ids, seq, pos, tg.cpu().numpy().reshape(-1),
+                      pt["topk_idx"].cpu().numpy(), pt["topk_w"].cpu().numpy(),
+                      pt["hidden"].cpu().numpy(), kc, vc, sample=sample,
+                      label="attn full long context (~2,000 positions) teacher-forced")
