@@ -1395,6 +1395,7 @@ __device__ __forceinline__ QkvRow qkv_row(const ProjParams& p, int prow) {
   return r;
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const ProjParams p) {
@@ -1511,73 +1512,91 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ------------------------------------------------ epilogue warps 2..5
       const int q = warp & 3;
       const int K1 = p.K + 1, half = p.hd >> 1;
+      // The global inputs of 16 token columns, loaded ahead of use (the
+      // item's first 16 while its MMAs run, the next 16 while the current
+      // ones are stored).  MODE 0: each column's cache row (slot * H * max_pos
+      // + position; -1 for a column past the chunk or a sequence out of range)
+      // and this row's rotary (cos, sin); MODE 1: h[t, row].
+      struct Cols {
+        int crow[MODE == 0 ? 16 : 1];
+        float2 cs[MODE == 0 ? 16 : 1];
+        float hv[MODE == 1 ? 16 : 1];
+      };
+      auto fetch = [&](const ProjItem& it, const QkvRow& r, int prow, int c0, Cols& f) {
+        if constexpr (MODE == 1) {
+          if (prow < p.d) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              f.hv[j] = c0 + j < it.n ? p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] : 0.f;
+          }
+        } else {
+          if (r.part >= 3) return;
+          int pos[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = it.b_row + c0 + j;
+            const bool valid = c0 + j < it.n;
+            const int b = valid ? t / K1 : 0;
+            const int p0 = valid ? __ldg(p.positions + b) : 0;
+            const bool ok = valid && p0 >= 0 && p0 <= p.max_pos - K1;
+            pos[j] = ok ? p0 + (t - b * K1) : 0;
+            f.crow[j] = ok ? b * p.H * p.max_pos + pos[j] : -1;
+          }
+          if (r.part < 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f.cs[j] = __ldg(p.rope + (size_t)pos[j] * half + r.freq);
+          }
+        }
+      };
       int local = 0;
       for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++local) {
         const ProjItem it = proj_item(p, i);
         const int npad = (it.n + 15) & ~15;
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
+        const int prow = it.tile * 128 + q * 32 + lane;  // row within this layer's block
+        const QkvRow r = qkv_row(p, prow);
+        Cols cur, nxt;
+        fetch(it, r, prow, 0, cur);
         if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.nch);
-        const int prow = it.tile * 128 + q * 32 + lane;  // row within this layer's block
-        const QkvRow r = qkv_row(p, prow);
         for (int c0 = 0; c0 < npad; c0 += 16) {
+          if (c0 + 16 < npad) fetch(it, r, prow, c0 + 16, nxt);
           uint32_t v[16];
           tmem_ld16(tb + (uint32_t)c0, v);
           tmem_ld_wait();
-          // the 16 columns' global loads are issued before their stores
-          if (p.mode == 1) {
+          if constexpr (MODE == 1) {
             if (prow < p.d) {
-              float hv[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                hv[j] = c0 + j < it.n ? p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] : 0.f;
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < it.n)
-                  p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] = hv[j] + __uint_as_float(v[j]);
+                  p.h[(size_t)(it.b_row + c0 + j) * p.d + prow] = cur.hv[j] + __uint_as_float(v[j]);
             }
-            continue;
-          }
-          if (r.part >= 3) continue;
-          // each column's sequence and position (the same for every lane)
-          int bq[16], pos[16];
-          bool ok[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = it.b_row + c0 + j;
-            const bool valid = c0 + j < it.n;
-            bq[j] = valid ? t / K1 : 0;
-            const int p0 = valid ? __ldg(p.positions + bq[j]) : 0;
-            ok[j] = valid && p0 >= 0 && p0 <= p.max_pos - K1;
-            pos[j] = ok[j] ? p0 + (t - bq[j] * K1) : 0;
-          }
-          if (r.part < 2) {
-            float2 cs[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) cs[j] = __ldg(p.rope + (size_t)pos[j] * half + r.freq);
+          } else if (r.part < 2) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               // rotary pair (dim i, dim i + hd/2) in lanes (2i, 2i + 1)
               const float x = __uint_as_float(v[j]);
               const float y = __shfl_xor_sync(0xffffffffu, x, 1);
-              const float rot = r.odd ? y * cs[j].y + x * cs[j].x : x * cs[j].x - y * cs[j].y;
+              const float2 cs = cur.cs[j];
+              const float rot = r.odd ? y * cs.y + x * cs.x : x * cs.x - y * cs.y;
               if (c0 + j >= it.n) continue;
               const int t = it.b_row + c0 + j;
               if (r.part == 0)
                 p.q[(size_t)t * p.d + r.head * p.hd + r.dim] = rot;
-              else if (ok[j])
-                p.kc[(((size_t)bq[j] * p.H + r.head) * p.max_pos + pos[j]) * p.hd + r.dim] =
+              else if (cur.crow[j] >= 0)
+                p.kc[((size_t)cur.crow[j] + (size_t)r.head * p.max_pos) * p.hd + r.dim] =
                     __float2bfloat16_rn(rot);
             }
-          } else {
+          } else if (r.part == 2) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (ok[j])
-                p.vc[(((size_t)bq[j] * p.H + r.head) * p.max_pos + pos[j]) * p.hd + r.dim] =
+              if (cur.crow[j] >= 0)
+                p.vc[((size_t)cur.crow[j] + (size_t)r.head * p.max_pos) * p.hd + r.dim] =
                     __float2bfloat16_rn(__uint_as_float(v[j]));
           }
+          cur = nxt;
         }
         tc_fence_before();
         __syncwarp();
@@ -1658,8 +1677,11 @@ size_t proj_smem_bytes(int nch, int stages) {
 
 cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, const ProjParams& p,
                         int grid, cudaStream_t s, bool pdl) {
-  return launch_gemm_ex(proj_kernel, grid, proj_smem_bytes(p.nch, p.stages), s, pdl, map_w, map_x,
-                        p);
+  if (p.mode == 1)
+    return launch_gemm_ex(proj_kernel<1>, grid, proj_smem_bytes(p.nch, p.stages), s, pdl, map_w,
+                          map_x, p);
+  return launch_gemm_ex(proj_kernel<0>, grid, proj_smem_bytes(p.nch, p.stages), s, pdl, map_w,
+                        map_x, p);
 }
 
 LmLayout lm_layout(int T) {
