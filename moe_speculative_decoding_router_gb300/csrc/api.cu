@@ -54,6 +54,7 @@ struct moe_verify_ctx {
   cudaStream_t capture_stream = nullptr;
   // CTAs of the persistent kernels (expert FFN, lm_head); 0: one per SM
   int grid_ctas = 0;
+  int lm_pair_max = 0;  // lm_head CTA pairs that fit on the GPU at once
   // the stack with attention (moe_verify_init_attn)
   bool attn = false;
   int H = 0, hd = 0, max_pos = 0, rows_qkv = 0, cap_pairs = 0, attn_target = 0;
@@ -300,7 +301,12 @@ struct StepShape {
   // as wide as the item's chunk of rows (rows past the buffers read as zeros;
   // rows past an item's own are loaded but never used)
   CUtensorMap map_x, map_a, map_f;
+  CUtensorMap map_f128;  // the final rows with 128-row boxes (the lm_head on CTA pairs)
 };
+
+// CTA pairs of the lm_head at large T: as many as fit at once (measured once
+// per context), at most half the persistent grid.
+int lm_pairs(const moe_verify_ctx* c);
 
 int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
   StepShape& s = *out;
@@ -331,6 +337,23 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
       encode_map(&s.map_a, c->abuf, c->I_pad, c->rows_max, (uint32_t)s.nch) ||
       encode_map(&s.map_f, c->xf, c->d, round_up(c->T_max, 16), (uint32_t)s.nch_lm))
     return MOE_VERIFY_ERR_CUDA;
+  if (s.lm.pair) {
+    // the pair form needs at least one pair that fits; else the single-CTA form
+    const int pairs = lm_pairs(c);
+    if (pairs < 1) {
+      s.lm.pair = false;
+      s.lm.n_chunks = (T + 255) / 256;
+      s.lm.nch = round_up((T + s.lm.n_chunks - 1) / s.lm.n_chunks, 16);
+      s.lm.tmem_cols = pow2_at_least(2 * s.lm.nch);
+      s.lm.stages = mv::gemm_max_stages(s.lm.nch);
+      s.n_chunks_lm = s.lm.n_chunks;
+      s.nch_lm = s.lm.nch;
+      if (encode_map(&s.map_f, c->xf, c->d, round_up(c->T_max, 16), (uint32_t)s.nch_lm))
+        return MOE_VERIFY_ERR_CUDA;
+    } else if (encode_map(&s.map_f128, c->xf, c->d, round_up(c->T_max, 16), 128)) {
+      return MOE_VERIFY_ERR_CUDA;
+    }
+  }
   return MOE_VERIFY_OK;
 }
 
@@ -348,6 +371,11 @@ int32_t* item_counter(moe_verify_ctx* c, int parity) {
 }
 
 int persistent_grid(const moe_verify_ctx* c) { return c->grid_ctas > 0 ? c->grid_ctas : c->num_sms; }
+
+int lm_pairs(const moe_verify_ctx* c) {
+  const int want = persistent_grid(c) / 2;
+  return want < c->lm_pair_max ? want : c->lm_pair_max;
+}
 
 // Timer slots of launch `slot` of a step (routing of layer l: 2l, expert FFN
 // of layer l: 2l + 1, lm_head: 2L; with attention: attention RMSNorm 6l,
@@ -458,6 +486,10 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.pf_base = 0;
     fp.pf_div = sh.n_chunks_lm;
     fp.pf_limit = (c->V_pad / 128) * sh.n_chunks_lm;
+    if (sh.lm.pair) {
+      fp.pf_pair = 1;
+      fp.pf_limit = 2 * lm_pairs(c);
+    }
   } else if (l + 1 < c->L && src != mv::kSrcBf16 && fp.spec > 0) {
     fp.pf_items = 1;
     fp.pf_base = (l + 1) * c->nE * c->mt_gu * 128;
@@ -650,6 +682,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   int e1 = encode_map(&c->map_gu, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 128);
   int e2 = encode_map(&c->map_dn, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 128);
   int e3 = encode_map(&c->map_lm, c->w_lm, d, c->V_pad, 128);
+  c->lm_pair_max = mv::lmhead_pair_max_clusters(mv::lm_layout(mv::kLmPairMinT + 1).stages);
   int e5 = encode_map(&c->map_gu256, c->w_gu, d, (uint64_t)L * c->nE * c->mt_gu * 128, 256);
   int e6 = encode_map(&c->map_dn256, c->w_dn, c->I_pad, (uint64_t)L * c->nE * c->mt_dn * 128, 256);
   // router weights of all layers: boxes of 64 columns x E rows
@@ -687,7 +720,8 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
     CK(mv::launch_final(fp, s, pdl));
   }
   mv::GemmParams gp = {};
-  gp.n_items_static = (ctx->V_pad / 128) * sh.n_chunks_lm;
+  gp.n_items_static = sh.lm.pair ? ((ctx->V_pad + 255) / 256) * sh.n_chunks_lm
+                                 : (ctx->V_pad / 128) * sh.n_chunks_lm;
   gp.kblocks = ctx->d / 64;
   gp.nch = sh.nch_lm;
   gp.stages = sh.lm.stages;
@@ -706,8 +740,11 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   gp.stamps = stamp_slot(ctx, stamp_slot_lm);
   {
     Timed tm(ctx, 2, s);
-    CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, persistent_grid(ctx), s,
-                         pdl));
+    if (sh.lm.pair)
+      CK(mv::launch_lmhead_pair(ctx->map_lm, sh.map_f128, gp, lm_pairs(ctx), s, pdl));
+    else
+      CK(mv::launch_lmhead(ctx->map_lm, sh.map_f, gp, sh.lm.tokens_on_m, persistent_grid(ctx), s,
+                           pdl));
   }
   return MOE_VERIFY_OK;
 }

@@ -503,7 +503,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // weight item numbered like this CTA (the first items of the next
         // kernel's CTAs together), while HBM has room (the last items of
         // other CTAs and the routing in between)
-        int row = p.pf_base + (int)(blockIdx.x / p.pf_div) * 128, row0 = 0;
+        // (the lm_head on CTA pairs: CTA c's first rows are half c % 2 of
+        // the 256-row tile of item c / 2)
+        const int c = (int)blockIdx.x;
+        int row = p.pf_base + (p.pf_pair ? ((c >> 1) / p.pf_div) * 256 + (c & 1) * 128
+                                         : (c / p.pf_div) * 128),
+            row0 = 0;
         const bool known = !p.pf_items || guess_gu_item(p, (int)blockIdx.x, p.pf_base, true, &row,
                                                         &row0);
         if (known)
@@ -1349,6 +1354,254 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   lm_finish(p, *C.abort_flag != 0, &is_last);
 }
 
+// ------------------------------------------- lm_head on CTA pairs (T > 256)
+//
+// Items (a chunk of <= 256 tokens, 256 vocabulary rows), vocabulary-major
+// (item i: vocabulary tile i / n_chunks, chunk i % n_chunks), in a static
+// stride over the pairs (clusters of 2 CTAs), so that the pairs working at
+// once share each vocabulary tile through L2.  The even CTA holds each stage's
+// tokens 0..127 and vocabulary rows 0..127, the odd CTA tokens 128..255 and
+// rows 128..255; one thread of the even CTA issues M = 256 (tokens), N = 256
+// (vocabulary rows) MMAs (cta_group::2) over both CTAs' shared memory, and each
+// CTA's TMEM receives its 128 tokens x the tile's 256 rows.  So each SM
+// receives 32 KB per stage for its 128 x 256 x 64 share of the product,
+// against 48 KB with one CTA per item: at large T the single-CTA form is bound
+// by its SM's TMA ingest.  Each epilogue thread owns one token (one TMEM lane)
+// and takes the argmax over the item's 256 rows in registers: one atomic per
+// token and item, no exchange between lanes or warps.
+// Handshakes: each CTA loads its halves into its own ring, and every load
+// completes on the even CTA's full barrier (which expects both CTAs' bytes);
+// the even CTA's commits release the stage in both CTAs (empty) and hand each
+// accumulator to both CTAs' epilogues (tfull), which release it on the even
+// CTA's tempty (eight arrivals).  A stage is refilled only after the commit of
+// its previous use, so one use's bytes never reach the barrier's previous
+// phase.  Each CTA reduces its own 128 rows per token.
+
+struct PairItem {
+  int tok_row, voc_row, v0;
+};
+
+__device__ __forceinline__ PairItem pair_item(const GemmParams& p, int i, uint32_t rank) {
+  PairItem it;
+  const int vt = i / p.n_chunks, c = i - vt * p.n_chunks;
+  it.tok_row = c * 256 + (int)rank * 128;  // this CTA's tokens
+  it.v0 = vt * 256;                        // the tile's first vocabulary row
+  it.voc_row = it.v0 + (int)rank * 128;    // this CTA's half of the tile
+  return it;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_pair_kernel(const __grid_constant__ CUtensorMap mapA,
+                       const __grid_constant__ CUtensorMap mapB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  constexpr int stage_bytes = 2 * 128 * 128;  // 128 tokens + 128 vocabulary rows, x 64 bf16
+  uint8_t* stages = smem;
+  uint8_t* ctrl_base = smem + (size_t)p.stages * stage_bytes;
+  const Ctrl C = ctrl_at(ctrl_base, p.stages);
+  __shared__ int is_last;
+  const uint32_t rank = cluster_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int n_items = p.n_items_static;
+  const bool has_work = pair < n_items;  // the same for both CTAs of a pair
+
+  if (threadIdx.x == 0) {
+    stamp_min(p.stamps);
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&C.tfull[b], 1);
+      mbar_init(&C.tempty[b], 8);  // both CTAs' four epilogue warps
+    }
+    mbar_init(C.drain, 1);
+    *C.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (has_work && warp == 1) {
+    tmem_alloc_pair(C.tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any arrival on them
+  tc_fence_after();
+  const uint32_t tmem_base = has_work ? *C.tmem_slot : 0u;
+
+  if (has_work && warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    // every load completes on the even CTA's barrier, which the even CTA's
+    // producer arms with both CTAs' bytes
+    const uint32_t full0 = mbar_cluster_addr(&C.full[0], 0);
+    auto full_at = [&](int st) { return full0 + (uint32_t)(st * sizeof(uint64_t)); };
+    // the first ring of vocabulary tiles (B, from offset 16 KB of each stage)
+    // does not depend on earlier kernels
+    int i = pair, kb = 0;
+    PairItem it = pair_item(p, i, rank);
+    int pre = 0;
+    {
+      int pi = i, pk = 0;
+      PairItem pt = it;
+      while (pre < p.stages && pi < n_items) {
+        if (rank == 0) mbar_arrive_expect_tx(&C.full[pre], (uint32_t)(2 * stage_bytes));
+        tma_load_2d_pair(stages + (size_t)pre * stage_bytes + kStageA, &mapA, full_at(pre),
+                         pk * 64, pt.voc_row, pol_w);
+        ++pre;
+        if (++pk == p.kblocks) {
+          pk = 0;
+          pi += n_pairs;
+          if (pi < n_items) pt = pair_item(p, pi, rank);
+        }
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (p.stamps) stamp_max(p.stamps + 1);
+    for (int s = 0; s < pre; ++s) {
+      tma_load_2d_pair(stages + (size_t)s * stage_bytes, &mapB, full_at(s), kb * 64,
+                       it.tok_row, pol_x);
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += n_pairs;
+        if (i < n_items) it = pair_item(p, i, rank);
+      }
+    }
+    int stage = pre, issued = pre;
+    uint32_t phase = 0;
+    if (stage == p.stages) {
+      stage = 0;
+      phase = 1;
+    }
+    bool ok = true;
+    while (i < n_items) {
+      if (!mbar_wait(&C.empty[stage], phase ^ 1u, C.abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + (size_t)stage * stage_bytes;
+      if (rank == 0) mbar_arrive_expect_tx(&C.full[stage], (uint32_t)(2 * stage_bytes));
+      tma_load_2d_pair(sa + kStageA, &mapA, full_at(stage), kb * 64, it.voc_row, pol_w);
+      tma_load_2d_pair(sa, &mapB, full_at(stage), kb * 64, it.tok_row, pol_x);
+      ++issued;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++kb == p.kblocks) {
+        kb = 0;
+        i += n_pairs;
+        if (i < n_items) it = pair_item(p, i, rank);
+      }
+    }
+    // (the even CTA's barriers see both CTAs' loads: it alone can wait for the
+    // loads in flight; the odd CTA's are covered by the even CTA's drain and
+    // the cluster barrier before either exits)
+    if (!ok && rank == 0) producer_drain(C, issued, p.stages);
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
+    if (has_work && warp == 1 && lane == 0 && rank == 0) {
+      // ------------------------------------------------ even CTA: MMA issuer
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      const uint32_t idesc = umma_idesc_bf16(256, 256);
+      bool ok = true;
+      for (int i = pair; i < n_items && ok; i += n_pairs, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tempty[buf], (use & 1u) ^ 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * 256);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(&C.full[stage], phase, C.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + (size_t)stage * stage_bytes);
+          const uint32_t sb = sa + kStageA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_pair(tmem_d, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sb + kk * 32),
+                           idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit_pair(&C.empty[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(&C.tfull[buf]);
+      }
+      // every MMA issued completes before TMEM is released
+      umma_commit_pair(C.drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(C.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    } else if (has_work && warp >= 2) {
+      // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
+      const int q = warp & 3;
+      int local = 0;
+      for (int i = pair; i < n_items; i += n_pairs, ++local) {
+        const PairItem it = pair_item(p, i, rank);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
+        // this thread's token: the greedy argmax over the tile's 256 rows
+        // (ascending ids, so a strictly larger key keeps the lowest id on ties)
+        const int tok = it.tok_row + q * 32 + lane;
+        uint32_t best = 0u;  // orderable image of the best logit so far
+        int best_id = -1;
+        const int nv = min(256, p.V - it.v0);
+        for (int c0 = 0; c0 < 256; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float lv = __uint_as_float(v[j]);
+            const uint32_t key = orderable(lv);
+            if (c0 + j < nv && (key > best || best_id < 0)) {
+              best = key;
+              best_id = it.v0 + c0 + j;
+            }
+            if (p.logits && tok < p.T && c0 + j < nv)
+              p.logits[(size_t)tok * p.V + it.v0 + c0 + j] = lv;
+          }
+        }
+        // the key of argmax_key(): larger logit first, then lower id
+        if (tok < p.T && best_id >= 0)
+          atomicMax(p.keys + tok, ((unsigned long long)best << 32) |
+                                      (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_id));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&C.tempty[buf]);
+          else
+            mbar_arrive_remote(&C.tempty[buf], 0);
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();  // the pair's MMAs, epilogues and remote arrivals are done
+  if (has_work && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+  }
+  lm_finish(p, *C.abort_flag != 0, &is_last);
+}
+
 // ----------------------------------- attention projections (weight rows on M)
 //
 // [128 rows of one layer's packed q/k/v or W_o] x [a chunk of <= nch tokens],
@@ -1687,6 +1940,16 @@ cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, cons
 LmLayout lm_layout(int T) {
   LmLayout l;
   l.tokens_on_m = T > 64 && T <= 128;
+  l.pair = T > kLmPairMinT;
+  if (l.pair) {
+    // chunks of 256 tokens, each CTA of a pair loading 128 of them
+    l.n_chunks = (T + 255) / 256;
+    l.nch = 128;
+    l.tmem_cols = 512;  // two accumulators of 256 token columns
+    l.stages = gemm_max_stages(l.nch);
+    if (l.stages > 16) l.stages = 16;
+    return l;
+  }
   if (l.tokens_on_m) {
     l.n_chunks = 1;
     l.nch = (T + 15) / 16 * 16;
@@ -1699,6 +1962,53 @@ LmLayout lm_layout(int T) {
   }
   l.stages = gemm_max_stages(l.nch);
   return l;
+}
+
+int lmhead_pair_max_clusters(int stages) {
+  const size_t smem = gemm_smem_bytes(128, stages);
+  if (cudaFuncSetAttribute(lmhead_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, lmhead_pair_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_lmhead_pair(const CUtensorMap& map_w, const CUtensorMap& map_x128,
+                               const GemmParams& p, int pairs, cudaStream_t s, bool pdl) {
+  const size_t smem = gemm_smem_bytes(128, p.stages);
+  cudaError_t e = cudaFuncSetAttribute(lmhead_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_pair_kernel, map_w, map_x128, p);
 }
 
 cudaError_t launch_lmhead(const CUtensorMap& map_w, const CUtensorMap& map_x, const GemmParams& p,

@@ -92,6 +92,7 @@ struct FfnParams {
   // item c as guessed for the first items (pf_base = that layer's first
   // gate/up row); pf_items = 0, rows pf_base + (c / pf_div) * 128
   int pf_base, pf_div, pf_limit, pf_kb, pf_items;
+  int pf_pair;                 // 1: the next kernel is the lm_head on CTA pairs (rows per pair item)
   // Items run shared experts first, so the first items' weights are known
   // before the routing for the shared experts always, and for the routed
   // experts when each holds one chunk: spec = 2 guesses both, 1 the shared
@@ -258,12 +259,20 @@ cudaError_t launch_ffn_tokm(const CUtensorMap& map_gu256, const CUtensorMap& map
                             const CUtensorMap& map_dn256, const CUtensorMap& map_a,
                             const FfnParams& p, int grid, cudaStream_t s, bool pdl);
 // The lm_head launch for T tokens: tokens on the MMA's M side for 65..128
-// tokens (one chunk), else vocabulary rows on M with chunks of <= 256 tokens.
+// tokens (one chunk); above kLmPairMinT tokens on CTA pairs (256 vocabulary
+// rows x chunks of 256 tokens, each CTA loading half of each); else
+// vocabulary rows on M with chunks of <= 256 tokens.
+constexpr int kLmPairMinT = 256;
 struct LmLayout {
-  bool tokens_on_m;
+  bool tokens_on_m, pair;
   int nch, n_chunks, tmem_cols, stages;
 };
 LmLayout lm_layout(int T);
+// CTA pairs of the lm_head that fit on the GPU at once (0: none).
+int lmhead_pair_max_clusters(int stages);
+// map_x128: the final normalised rows with 128-row boxes; grid = 2 * pairs.
+cudaError_t launch_lmhead_pair(const CUtensorMap& map_w, const CUtensorMap& map_x128,
+                               const GemmParams& p, int pairs, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const CUtensorMap& map_w, const CUtensorMap& map_x, const GemmParams& p,
                           bool tokens_on_m, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);

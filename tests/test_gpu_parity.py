@@ -79,7 +79,7 @@ def test_tiny_every_id_matches_oracle(tiny):
 
 # T = 68 and 96 reach the tokens-on-M lm_head with ragged chunks (65..128 tokens)
 @pytest.mark.parametrize("Bn,K", [(1, 0), (1, 3), (3, 1), (4, 3), (17, 3), (24, 3), (128, 0),
-                                  (77, 2)])
+                                  (77, 2), (100, 3), (128, 3)])  # T = 400, 512: lm_head on CTA pairs
 def test_tiny_batch_shapes(tiny, Bn, K):
     ctx, orc = tiny
     ids = S.uniform_ids(Bn * (K + 1), 41 + Bn, K, 512).reshape(Bn, K + 1)
@@ -88,7 +88,8 @@ def test_tiny_batch_shapes(tiny, Bn, K):
     check_tokens(orc, ids.reshape(-1), got, label=f"tiny B={Bn} K={K}")
 
 
-@pytest.mark.parametrize("Bn", [1, 20])  # T = 4: vocabulary rows on M; T = 80: tokens on M
+# T = 4: vocabulary rows on M; T = 80: tokens on M; T = 280, 512: CTA pairs
+@pytest.mark.parametrize("Bn", [1, 20, 70, 128])
 def test_tiny_logits_probe(tiny, Bn):
     ctx, orc = tiny
     B = _B()
