@@ -450,6 +450,14 @@ def run_ours(args, rank, world, local):
                                   "ffn_per_layer": [round(x, 2) for x in win[:, 1:2 * L:2].mean(0)],
                                   "routing_per_layer": [round(x, 2)
                                                         for x in win[:, 0:2 * L:2].mean(0)],
+                                  # from the previous launch's end to the routing's end
+                                  # (all of the routing's blocks, every wave)
+                                  "routing_span_per_layer": [
+                                      round(x, 2) for x in
+                                      ((st[:, 2:2 * L:2, 2] - st[:, 1:2 * L - 1:2, 2]) * 1e-3)
+                                      .mean(0)],
+                                  "layer_period": round(float(np.mean(np.diff(
+                                      st[:, 1:2 * L:2, 2], axis=1))) * 1e-3, 2),
                                   "lm_head": round(float(win[:, 2 * L].mean()), 2),
                                   "step_span": round(float(st[:, 2 * L, 2].mean()) * 1e-3, 2)},
                               "clocks": clk}), flush=True)
