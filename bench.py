@@ -399,6 +399,7 @@ def run_ours(args, rank, world, local):
     w_dev = BND.weights_to_device(w_host, device=dev)
     ctx = BND.MoeVerify(cfg, w_dev, max_batch=Bq if args.profile else 1024,
                         max_k=Kq if args.profile else K_DRAFT)
+    ctx.set_layer_kernel(args.layer_kernel)
     del w_dev
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
@@ -1046,6 +1047,9 @@ def main():
                     help="profiling only: time whole decode iterations with the FastMTP draft head")
     ap.add_argument("--attn", action="store_true",
                     help="profiling only: the stack with attention at positions in [512, 4096)")
+    ap.add_argument("--layer-kernel", type=int, default=0,
+                    help="profiling only: steps of at most this many verify tokens route inside "
+                         "the expert-FFN kernel (0..8; 0, the default: a routing launch per layer)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1053,6 +1057,10 @@ def main():
             or args.zipf or args.attn) and not args.profile:
         ap.error("--layers, --batch, --drafts, --zipf, --draft-head and --attn are for "
                  "profiling runs only (--profile)")
+    if args.layer_kernel and not args.profile:
+        ap.error("--layer-kernel is for profiling runs only (--profile)")
+    if not 0 <= args.layer_kernel <= 8:
+        ap.error("--layer-kernel must be in 0..8")
     if args.attn and (args.zipf or args.draft_head):
         ap.error("--attn runs the stack without the Zipf bias or the draft head")
     if args.draft_head and (args.layers or (args.drafts is not None and args.drafts < 1)):

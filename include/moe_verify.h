@@ -341,7 +341,8 @@ MOE_VERIFY_API uint64_t moe_verify_device_bytes(const moe_verify_config* config)
  *   ms[1], n[1]: attention sub-block (attention RMSNorm, q/k/v and output
  *                projections, attention; contexts with attention only)
  *   ms[2], n[2]: lm_head + argmax        ms[3], n[3]: routing + final RMSNorm
- * reset != 0 clears the sums afterwards. */
+ * (a step run by the single-kernel layer counts its layers' routing with the
+ * expert FFN).  reset != 0 clears the sums afterwards. */
 MOE_VERIFY_API int moe_verify_set_timing(moe_verify_ctx* ctx, int32_t enable);
 MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] host*/, int64_t* n /*[4] host*/,
                           int32_t reset);
@@ -357,6 +358,25 @@ MOE_VERIFY_API int moe_verify_get_timing(moe_verify_ctx* ctx, double* ms /*[4] h
  * attention (default one per SM).  Host-buffer decode graphs
  * already captured keep the grid they were captured with. */
 MOE_VERIFY_API int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas);
+
+/* The single-kernel layer for the batch-1 operating point (FastMTP paragraph
+ * of "Jina AI Releases jina-ocr-v1, a 3.4B MoE Document Parser With Built-In
+ * Speculative Decoding": at batch 1 the step is bound by launch overhead).
+ * moe_verify_step and moe_verify_decode_host calls of at most max_tokens
+ * verify tokens (B x (K + 1)) run each layer as one launch of the persistent
+ * expert-FFN kernel: its first work items route one token each (the routing
+ * kernel's arithmetic in the same order, so results are the same bit for bit)
+ * while the other CTAs stream their first weight tiles; every CTA then takes
+ * expert items.  Each wait in it is for a lower work item, claimed by a
+ * running CTA, and gives up after 2 s like the others (timeout status).
+ * 0 <= max_tokens <= 8; 0, the initial value, turns it off (a routing
+ * launch and an expert-FFN launch per layer): on one GB300 the two launches
+ * are faster (0.545 against 0.61 ms for the 12-layer step at B = 1, K = 3).  It applies where the router
+ * weights (E x d bf16) fit in the kernel's shared-memory ring and d <= 2048;
+ * moe_verify_layer, moe_verify_draft and moe_verify_step_attn always run the
+ * two launches.  Host-buffer decode graphs already captured keep the setting
+ * they were captured with.  MOE_VERIFY_ERR_ARG for max_tokens outside 0..8. */
+MOE_VERIFY_API int moe_verify_set_layer_kernel(moe_verify_ctx* ctx, int32_t max_tokens);
 
 /* Profiling (no counterpart in the method): launch timestamps inside later
  * moe_verify_step (moe_verify_step_attn) calls, for timing kernels in a

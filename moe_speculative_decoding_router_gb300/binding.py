@@ -31,8 +31,8 @@ EXPORTED = ("moe_verify_init", "moe_verify_step", "moe_verify_accept", "moe_veri
             "moe_verify_strerror", "moe_verify_check_config", "moe_verify_device_bytes",
             "moe_verify_set_timing", "moe_verify_get_timing", "moe_verify_greedy_head_noalloc",
             "moe_verify_check_bounded_wait", "moe_verify_draft", "moe_verify_draft_inputs",
-            "moe_verify_set_grid", "moe_verify_set_stamps", "moe_verify_init_attn",
-            "moe_verify_step_attn", "moe_verify_kv_cache")
+            "moe_verify_set_grid", "moe_verify_set_layer_kernel", "moe_verify_set_stamps",
+            "moe_verify_init_attn", "moe_verify_step_attn", "moe_verify_kv_cache")
 
 
 class Config(ctypes.Structure):
@@ -112,6 +112,8 @@ def load(build_if_missing: bool = True):
     L.moe_verify_check_bounded_wait.argtypes = [ctypes.c_int64, _P, _P]
     L.moe_verify_set_grid.restype = _i32
     L.moe_verify_set_grid.argtypes = [_P, _i32]
+    L.moe_verify_set_layer_kernel.restype = _i32
+    L.moe_verify_set_layer_kernel.argtypes = [_P, _i32]
     L.moe_verify_set_stamps.restype = _i32
     L.moe_verify_set_stamps.argtypes = [_P, _P]
     L.moe_verify_init_attn.restype = _i32
@@ -439,6 +441,13 @@ class MoeVerify:
         rc = self.lib.moe_verify_set_grid(self.handle, int(ctas))
         if rc != OK:
             raise MoeVerifyError(rc, "moe_verify_set_grid")
+
+    def set_layer_kernel(self, max_tokens: int):
+        """moe_verify_set_layer_kernel: steps of at most max_tokens verify
+        tokens run one launch per layer (0: off)."""
+        rc = self.lib.moe_verify_set_layer_kernel(self.handle, int(max_tokens))
+        if rc != OK:
+            raise MoeVerifyError(rc, "moe_verify_set_layer_kernel")
 
     def set_stamps(self, stamps):
         """moe_verify_set_stamps: a device int64 tensor [2L + 1, 4] ([6L + 1, 4]

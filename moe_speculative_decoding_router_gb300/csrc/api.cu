@@ -37,6 +37,8 @@ struct moe_verify_ctx {
           *dep = nullptr;
   float* perm_w = nullptr;
   unsigned int *done_ffn = nullptr, *done_lm = nullptr;
+  // the single-kernel layer: routed tokens [2] and finished CTAs [2] by parity
+  int32_t* route_ctr = nullptr;
   unsigned long long* keys = nullptr;
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
@@ -54,6 +56,13 @@ struct moe_verify_ctx {
   cudaStream_t capture_stream = nullptr;
   // CTAs of the persistent kernels (expert FFN, lm_head); 0: one per SM
   int grid_ctas = 0;
+  // steps of at most this many verify tokens route inside the expert-FFN
+  // kernel (one launch per layer); 0: off.  Off by default: measured on the
+  // 12-layer step at B = 1, K = 3, 0.61 ms per step against 0.545 ms with a
+  // routing launch per layer (the routing's stages run ~1.7x slower in the
+  // expert FFN's 6-warp CTAs than in the 16-warp routing blocks, more than
+  // the launch handoff it saves)
+  int fuse_max_T = 0;
   int lm_pair_max = 0;  // lm_head CTA pairs that fit on the GPU at once
   // the stack with attention (moe_verify_init_attn)
   bool attn = false;
@@ -294,6 +303,7 @@ constexpr int kTokmMinT = 320;
 struct StepShape {
   int T, tpb, grid_route, nch, stages, tmem_cols, nch_lm, n_chunks_lm;
   bool tokm;
+  bool fused;  // the verify step's layers route inside the expert-FFN kernel
   mv::LmLayout lm;
   bool wr_smem;
   size_t route_smem;
@@ -331,6 +341,8 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
   s.n_chunks_lm = s.lm.n_chunks;
   s.nch_lm = s.lm.nch;
   s.tmem_cols = s.tokm ? 512 : pow2_at_least(2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm));
+  s.fused = T <= c->fuse_max_T && !s.tokm &&
+            mv::ffn_route_fits(s.nch, s.stages, c->d, c->E, c->k, c->S);
   s.wr_smem = mv::route_wr_fits(s.tpb, c->d, c->E, c->k, c->S);
   s.route_smem = mv::route_smem_bytes(s.tpb, c->d, c->E, c->k, c->S, s.wr_smem);
   if (encode_map(&s.map_x, c->xperm, c->d, c->rows_max, (uint32_t)s.nch) ||
@@ -433,7 +445,9 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
   rp.perm_slot = c->perm_slot;
   rp.perm_w = c->perm_w;
   rp.stamps = stamp_slot(c, stamp_base);
-  {
+  // the verify step's few-token layers: the routing inside the expert FFN
+  const bool fused = sh.fused && (src == mv::kSrcEmbed || src == mv::kSrcCombine);
+  if (!fused) {
     Timed tm(c, 3, s);
     CK(mv::launch_route(c->map_wr, rp, sh.grid_route, sh.route_smem, s, pdl));
   }
@@ -498,6 +512,13 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
                               : c->S * ((T + sh.nch - 1) / sh.nch) * c->mt_gu;
   }
   fp.stamps = stamp_slot(c, stamp_base >= 0 ? stamp_base + 1 : -1);
+  if (fused) {
+    fp.n_route = T;
+    fp.rt = rp;
+    fp.route_done = c->route_ctr + parity;
+    fp.route_done_clear = c->route_ctr + (1 - parity);
+    fp.exit_ctr = c->route_ctr + 2 + parity;
+  }
   if (sh.tokm) {
     fp.spec = 0;
     fp.pf_limit = 0;
@@ -506,8 +527,8 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
                            s, pdl));
   } else {
     Timed tm(c, 0, s);
-    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, fp, persistent_grid(c), s,
-                      pdl));
+    CK(mv::launch_ffn(c->map_gu, sh.map_x, c->map_dn, sh.map_a, *map_pf, c->map_wr, fp,
+                      persistent_grid(c), s, pdl));
   }
   return MOE_VERIFY_OK;
 }
@@ -628,6 +649,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   AL(c->dep, z.dep);
   AL(c->done_ffn, 16);
   AL(c->done_lm, 16);
+  AL(c->route_ctr, 16);
   AL(c->keys, z.keys);
   AL(c->status, 16);
   AL(c->io_ctx, z.io);
@@ -645,6 +667,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   CKF(cudaMemsetAsync(c->dep, 0, z.dep, s));
   CKF(cudaMemsetAsync(c->done_ffn, 0, 16, s));
   CKF(cudaMemsetAsync(c->done_lm, 0, 16, s));
+  CKF(cudaMemsetAsync(c->route_ctr, 0, 16, s));
   CKF(cudaMemsetAsync(c->status, 0, 16, s));
   CKF(cudaMemsetAsync(c->bias, 0, z.bias, s));
 
@@ -715,6 +738,7 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   fp.cnt_clear = ctx->cnt + (size_t)last_parity * ctx->E;
   fp.n_cnt_clear = ctx->E;
   fp.item_clear = item_counter(ctx, last_parity);
+  fp.route_done_clear = ctx->route_ctr + last_parity;
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, pdl));
@@ -1240,6 +1264,12 @@ void moe_verify_destroy(moe_verify_ctx* ctx) {
 int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas) {
   if (!ctx || ctas < 0 || ctas > 8 * ctx->num_sms) return MOE_VERIFY_ERR_ARG;
   ctx->grid_ctas = ctas;
+  return MOE_VERIFY_OK;
+}
+
+int moe_verify_set_layer_kernel(moe_verify_ctx* ctx, int32_t max_tokens) {
+  if (!ctx || max_tokens < 0 || max_tokens > mv::kFuseMaxT) return MOE_VERIFY_ERR_ARG;
+  ctx->fuse_max_T = max_tokens;
   return MOE_VERIFY_OK;
 }
 

@@ -41,6 +41,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_stages.cuh"
 
 namespace mv {
 
@@ -92,6 +93,8 @@ struct Ctrl {
   int* q_item;        // [kQueue]
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  uint64_t* rbar;     // single-kernel layer: router weights and gain staged
+  int* ticket;        // single-kernel layer: the CTA's current ticket
 };
 
 __device__ __forceinline__ Ctrl ctrl_at(uint8_t* base, int stages) {
@@ -110,6 +113,9 @@ __device__ __forceinline__ Ctrl ctrl_at(uint8_t* base, int stages) {
   c.q_item = reinterpret_cast<int*>(c.q_empty + kQueue);
   c.tmem_slot = reinterpret_cast<uint32_t*>(c.q_item + kQueue);
   c.abort_flag = reinterpret_cast<volatile int*>(c.tmem_slot + 1);
+  c.rbar = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(c.abort_flag + 2) + 7) & ~uintptr_t(7));
+  c.ticket = reinterpret_cast<int*>(c.rbar + 1);
   return c;
 }
 
@@ -333,10 +339,104 @@ __device__ __forceinline__ bool guess_gu_item(const FfnParams& p, int c, int bas
   return true;
 }
 
+// Shared memory of a routing task of the single-kernel layer, in the ring:
+// [router weights: d / 64 swizzled panels] [gain d fp32] [normalised row
+// d + 8 bf16] [partial logits] [logits E] [reduction 64] [rows k + S].
+__host__ __device__ inline size_t route_task_bytes(int d, int E, int k, int S) {
+  const int n_mt = (E + 15) / 16;
+  return (size_t)(d / 64) * rs::route_wr_panel(E) + (size_t)d * 4 + ((size_t)d + 8) * 2 +
+         ((size_t)rs::route_ksplit(E) * n_mt * 16 * 8 + E + 64) * 4 + (size_t)(k + S) * 4;
+}
+
+// Routing tasks of the single-kernel layer, all threads of the CTA.  Ticket
+// j < n_route routes token j with the routing kernel's stages (the same bits
+// as there): residual stream and RMSNorm, router logits on the tensor cores
+// from the router weights staged in this CTA's ring (rbar), softmax and top-k
+// with the row claims, and the token's normalised row copied into its expert
+// rows.  Ticket 0 clears, after the wait, what kernels complete by then used:
+// the dependency counters, the other parity's expert counters and routed-token
+// counter.  Each task then publishes its token (rows, row metadata and claims
+// made visible to other CTAs' loads, TMA included, then route_done) and
+// claims the next ticket.  `first` is this CTA's ticket - n_route (< 0);
+// returns its first expert item.
+template <int SRC>
+__device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring, int first) {
+  constexpr int NW = kGemmThreads / 32;
+  const RouteParams& rt = p.rt;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int d = rt.d, E = rt.E, k = rt.k, S = rt.S;
+  const int n_mt = (E + 15) / 16, ksplit = rs::route_ksplit(E);
+  const int pitch = d + 8, cpr = d / 8;
+  uint8_t* wr_s = ring;
+  float* gs = reinterpret_cast<float*>(ring + (size_t)(d / 64) * rs::route_wr_panel(E));
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(gs + d);
+  float* part = reinterpret_cast<float*>(xb + pitch);
+  float* zs = part + ksplit * n_mt * 16 * 8;
+  float* red = zs + E;
+  int* rows = reinterpret_cast<int*>(red + 64);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid == 0 && rt.stamps) stamp_max(rt.stamps + 1);
+  if (first == -p.n_route) {
+    for (int i = tid; i < rt.n_dep_clear; i += kGemmThreads) rt.dep_clear[i] = 0;
+    for (int e = tid; e < E; e += kGemmThreads) rt.cnt_other[e] = 0;
+    if (tid == 0) *p.route_done_clear = 0;
+  }
+  mbar_wait(C.rbar, 0, C.abort_flag, rt.status);
+  __syncthreads();
+  const bool ok = !*C.abort_flag;  // the same for every thread (barriers below)
+  while (first < 0) {
+    const int t = first + p.n_route;
+    for (int i = tid; i < k + S; i += kGemmThreads) rows[i] = -1;
+    if (ok) rs::norm_token<SRC, NW, 16>(rt, t, gs, xb, red);  // d <= 2048
+    __syncthreads();
+    if (ok)
+      for (int i = tid; i < S * cpr; i += kGemmThreads) {
+        const int sx = i / cpr, c = i - sx * cpr;
+        reinterpret_cast<uint4*>(rt.xperm + ((size_t)(E + sx) * rt.T + t) * d)[c] =
+            reinterpret_cast<const uint4*>(xb)[c];
+      }
+    rs::router_logits<1, true>(rt, wr_s, xb, pitch, part, zs, 1, NW, ok);
+    if (warp == 0 && ok) {
+      if (E <= 64)
+        rs::select_experts<2>(rt, zs, t, rows);
+      else
+        rs::select_experts<8>(rt, zs, t, rows);
+    }
+    __syncthreads();
+    if (ok)
+      for (int i = tid; i < k * cpr; i += kGemmThreads) {
+        const int q = i / cpr, c = i - q * cpr;
+        const int row = rows[q];
+        if (row >= 0)
+          reinterpret_cast<uint4*>(rt.xperm + (size_t)row * d)[c] =
+              reinterpret_cast<const uint4*>(xb)[c];
+      }
+    __threadfence();
+    fence_proxy_async_global();
+    __syncthreads();
+    if (tid == 0) {
+      if (rt.stamps) stamp_max(rt.stamps + 2);
+      atomicAdd(p.route_done, 1);
+      *C.ticket = atomicAdd(p.next_item, 1) - p.n_route;
+    }
+    __syncthreads();
+    first = *C.ticket;
+  }
+  // the ring goes to this CTA's TMA loads: its ordinary accesses come first
+  fence_proxy_async_shared();
+  __syncthreads();
+  return first;
+}
+
+// kRoute: the single-kernel layer (FfnParams::n_route tokens routed here
+// first, with the router map map_wr); otherwise map_wr is not read.
+template <bool kRoute>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
                const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
-               const __grid_constant__ CUtensorMap map_pf, const FfnParams p) {
+               const __grid_constant__ CUtensorMap map_pf, const __grid_constant__ CUtensorMap map_wr,
+               const FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stage_bytes = kStageA + p.nch * 128;
@@ -367,18 +467,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // The host guesses routed items only when every routed expert expects
   // several rows (else most of those guesses would miss and their loads
   // would only take bandwidth); shared items are always right.
+  // The single-kernel layer: tickets below n_route are routing tasks, and
+  // expert item i is ticket n_route + i, so every wait (an expert item's for
+  // the routing, a down item's for gate/up items) is for lower tickets.
   int first = 0, guess_row = 0, guess_row0 = 0, pre = 0;
   if (threadIdx.x == 0) {
     stamp_min(p.stamps);
     first = atomicAdd(p.next_item, 1);
-    if (p.spec > 0 && guess_gu_item(p, first, p.a_base_gu, p.spec > 1, &guess_row, &guess_row0))
+    if (kRoute) first -= p.n_route;
+    if (first >= 0 && p.spec > 0 &&
+        guess_gu_item(p, first, p.a_base_gu, p.spec > 1, &guess_row, &guess_row0))
       pre = min(p.stages, p.kb_gu);
     init_ctrl(C, p.stages, 2, 2);
+    if (kRoute) {
+      mbar_init(C.rbar, 1);
+      fence_mbar_init();
+      *C.ticket = first;
+    }
     tma_prefetch_desc(&map_gu);
     tma_prefetch_desc(&map_x);
     tma_prefetch_desc(&map_dn);
     tma_prefetch_desc(&map_a);
     if (p.pf_limit > 0) tma_prefetch_desc(&map_pf);
+    if (kRoute && first < 0) {
+      // a routing task: the router weights and the gain (static) into the ring
+      if (p.rt.stamps) stamp_min(p.rt.stamps);
+      tma_prefetch_desc(&map_wr);
+      const int d = p.rt.d, E = p.rt.E;
+      const size_t panel = rs::route_wr_panel(E);
+      const uint64_t pol = policy_evict_last();
+      mbar_arrive_expect_tx(C.rbar, (uint32_t)((size_t)E * d * 2 + (size_t)d * 4));
+      for (int pn = 0; pn < d / 64; ++pn)
+        tma_load_2d(stages + (size_t)pn * panel, &map_wr, C.rbar, pn * 64, p.rt.wr_row, pol);
+      bulk_load(stages + (size_t)(d / 64) * panel, p.rt.gain, (uint32_t)(d * 4), C.rbar);
+    }
     if (pre > 0) {
       const uint64_t pol_w = policy_evict_first();
       mbar_arrive_expect_tx(C.spec, (uint32_t)(pre * kStageA));
@@ -390,10 +512,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(C.tmem_slot, (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
-  // The routing kernel (the predecessor) must be complete before the counts
-  // and rows are read; dependents may start once this grid is past its wait.
+  if constexpr (kRoute) {
+    __syncthreads();
+    first = *C.ticket;
+    if (first < 0) {
+      if (p.rt.src == kSrcEmbed)
+        first = ffn_route_tasks<kSrcEmbed>(p, C, stages, first);
+      else
+        first = ffn_route_tasks<kSrcCombine>(p, C, stages, first);
+    }
+  }
+  // The routing (the predecessor kernel, or this kernel's routing tasks) must
+  // be complete before the counts and rows are read; dependents may start
+  // once this grid is past its wait.
   pdl_wait();
   pdl_launch_dependents();
+  if constexpr (kRoute) {
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      uint32_t n = 0;
+      // (polled with a pause: every CTA waits here while the routing tasks'
+      // own loads are in flight)
+      while (ld_acquire(p.route_done) < p.n_route) {
+        __nanosleep(128);
+        if ((++n & 15u) == 0 && (*C.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+          if (!*C.abort_flag) {
+            *C.abort_flag = 1;
+            atomicOr(p.status, kErrTimeout);
+          }
+          break;
+        }
+      }
+      fence_proxy_async_global();
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 1);
   if (threadIdx.x == 0 && pre > 0) {
     // the speculated first item's activation rows load while the item lists
@@ -427,7 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!queue_push(C, nq++, item, p.status)) return false;
         if (item >= 0) {
           it = decode(p, L, nE, n_gu, item);
-          next_raw = atomicAdd(p.next_item, 1);
+          next_raw = atomicAdd(p.next_item, 1) - (kRoute ? p.n_route : 0);
         }
         return true;
       };
@@ -609,9 +762,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const int n = c0 + j;
               if (n < it.n) {
                 const int r = it.row0 + n;
-                const int tok = __ldg(p.perm_token + r);
-                const int slot = __ldg(p.perm_slot + r);
-                const float w = __ldg(p.perm_w + r);
+                // (written in this launch by its routing tasks: through L2)
+                const int tok = kRoute ? __ldcg(p.perm_token + r) : __ldg(p.perm_token + r);
+                const int slot = kRoute ? __ldcg(p.perm_slot + r) : __ldg(p.perm_slot + r);
+                const float w = kRoute ? __ldcg(p.perm_w + r) : __ldg(p.perm_w + r);
                 p.y[((size_t)tok * p.kS + slot) * p.d + m] = w * __uint_as_float(v[j]);
               }
             }
@@ -632,6 +786,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
   // the counters this launch used are cleared by the next routing kernel
+  // (the single-kernel layer: its ticket counter by its last CTA to finish;
+  // the next launch claiming on it starts after this one is complete)
+  if (kRoute && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1) {
+      *p.next_item = 0;
+      *p.exit_ctr = 0;
+    }
+  }
 }
 
 // End of an lm_head launch: the last CTA to finish turns the argmax keys into
@@ -1900,10 +2063,17 @@ int gemm_max_stages(int nch) {
 
 cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_dn, const CUtensorMap& map_a,
-                       const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
-                       bool pdl) {
-  return launch_gemm_ex(ffn_kernel, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu, map_x,
-                        map_dn, map_a, map_pf, p);
+                       const CUtensorMap& map_pf, const CUtensorMap& map_wr, const FfnParams& p,
+                       int grid, cudaStream_t s, bool pdl) {
+  if (p.n_route > 0)
+    return launch_gemm_ex(ffn_kernel<true>, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl,
+                          map_gu, map_x, map_dn, map_a, map_pf, map_wr, p);
+  return launch_gemm_ex(ffn_kernel<false>, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu,
+                        map_x, map_dn, map_a, map_pf, map_wr, p);
+}
+
+bool ffn_route_fits(int nch, int stages, int d, int E, int k, int S) {
+  return d <= 2048 && route_task_bytes(d, E, k, S) <= (size_t)stages * (kStageA + (size_t)nch * 128);
 }
 
 size_t ffn_tokm_smem_bytes(int stages) {

@@ -99,6 +99,17 @@ struct FfnParams {
   // experts' items only, 0 none.
   int spec;
   unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
+  // The single-kernel layer (a few verify tokens): n_route > 0 makes the
+  // first n_route tickets route one token each (rt, with rt.stamps the
+  // routing's timer slots) before any expert item runs; route_done counts the
+  // tokens routed (zero on entry; the first routing task clears
+  // route_done_clear, the other parity's), exit_ctr the CTAs that have
+  // finished (the last one resets it and next_item).
+  int n_route;
+  RouteParams rt;
+  int32_t* route_done;
+  int32_t* route_done_clear;
+  int32_t* exit_ctr;
 };
 
 struct FinalParams {
@@ -114,6 +125,7 @@ struct FinalParams {
   int32_t* cnt_clear;          // [n_cnt_clear] expert counters of the last layer, cleared
   int n_cnt_clear;
   int32_t* item_clear;         // item counter of the last layer's expert FFN, cleared
+  int32_t* route_done_clear;   // routed-token counter of the last layer, cleared (or nullptr)
 };
 
 // The lm_head GEMM with its argmax epilogue.
@@ -246,10 +258,20 @@ bool route_wr_fits(int tpb, int d, int E, int k, int S);
 // Launchers (enqueue only).  `pdl` requests programmatic dependent launch.
 cudaError_t launch_route(const CUtensorMap& map_wr, const RouteParams& p, int grid, size_t smem,
                          cudaStream_t s, bool pdl);
+// Steps of at most this many verify tokens may route inside the expert-FFN
+// kernel (the single-kernel layer; off unless the caller sets it).
+constexpr int kFuseMaxT = 8;
+
+// p.n_route > 0: the single-kernel layer, routing with the router map map_wr
+// (64-column boxes of E rows, 128-byte swizzle) in the shared memory of the
+// ring (ffn_route_fits).
 cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_dn, const CUtensorMap& map_a,
-                       const CUtensorMap& map_pf, const FfnParams& p, int grid, cudaStream_t s,
-                       bool pdl);
+                       const CUtensorMap& map_pf, const CUtensorMap& map_wr, const FfnParams& p,
+                       int grid, cudaStream_t s, bool pdl);
+// Whether a routing task of the single-kernel layer (router weights, gain,
+// one normalised row, logits) fits in the ring of `stages` stages of nch rows.
+bool ffn_route_fits(int nch, int stages, int d, int E, int k, int S);
 // The token-major form of the layer's expert FFN (large T): 128 of an
 // expert's rows on the MMA's M side, 256 weight rows on N.  map_gu256 and
 // map_dn256 are the weight maps with 256-row boxes, map_x and map_a the

@@ -207,6 +207,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The same for shared memory of this CTA (a buffer read by ordinary loads,
+// then filled by TMA).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both

@@ -24,31 +24,23 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_stages.cuh"
 
 namespace mv {
+
+using rs::bf16x4_to_f4;
+using rs::norm_pack;
+using rs::norm_scale;
+using rs::route_ksplit;
+using rs::route_wr_panel;
+using rs::sum_slots;
+using rs::sumsq4;
+using rs::warp_sum;
 
 namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-  float2 a = __bfloat1622float2(b[0]), c = __bfloat1622float2(b[1]);
-  return make_float4(a.x, a.y, c.x, c.y);
-}
 
 // Bulk copy of `bytes` (16-byte aligned, multiple of 16) into shared memory,
 // completing on `bar`, in pieces of at most 16 KB.
@@ -59,42 +51,16 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, size_t byt
   }
 }
 
-// acc[j] = y[0][c_j] + y[1][c_j] + ... + y[kS-1][c_j] (fp32, slot order) for
-// NC float4 chunks of one token's expert outputs y [kS, nc] (chunks c_j >= nc
-// are skipped).  Slots go in
-// fixed groups of 8 whose loads are all issued before the first add, so a
-// token costs one memory round trip per 8 slots.
-template <int NC>
-__device__ __forceinline__ void sum_slots(const float4* __restrict__ yr, int nc, int kS,
-                                          const int (&c)[NC], float4 (&acc)[NC]) {
-  for (int s0 = 0; s0 < kS; s0 += 8) {
-    float4 u[8][NC];
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-#pragma unroll
-      for (int j = 0; j < NC; ++j)
-        u[q][j] = (s0 + q < kS && c[j] < nc) ? __ldcg(yr + (size_t)(s0 + q) * nc + c[j])
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-#pragma unroll
-      for (int j = 0; j < NC; ++j) {
-        if (s0 + q == 0) {
-          acc[j] = u[q][j];
-        } else if (s0 + q < kS) {
-          acc[j].x += u[q][j].x; acc[j].y += u[q][j].y;
-          acc[j].z += u[q][j].z; acc[j].w += u[q][j].w;
-        }
-      }
-  }
-}
-
-// Stage 1 for the block's tokens t0 .. t0+ntok-1, all threads: build the
-// residual stream h entering the block (and write it back), RMSNorm, and the
-// normalised bf16 row xb [TPB, d] (row pitch xpitch elements).  For the combine source xs [TPB, d] already
-// holds the tokens' h rows and gs [d] the gain (bulk copies issued before the
-// wait); the expert outputs of the previous block are summed in slot order
-// (routed slots in selection order, then the shared experts) and added to h.
+// Stage 1 for the block's tokens t0 .. t0+ntok-1 (TPB > 1; rows of at most
+// 2,048, so that each thread holds at most one chunk of a row and the sum of
+// squares is reduced in the order of the one-token path: per warp over its 32
+// chunks, then over the warps in order), all threads: build the residual
+// stream h entering the block (and write it back), RMSNorm, and the
+// normalised bf16 row xb [TPB, d] (row pitch xpitch elements).  For the
+// combine source xs [TPB, d] already holds the tokens' h rows and gs [d] the
+// gain (bulk copies issued before the wait); the expert outputs of the
+// previous block are summed in slot order (routed slots in selection order,
+// then the shared experts) and added to h.
 template <int SRC, int TPB>
 __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, const float* gs,
                            __nv_bfloat16* xb, int xpitch, float* red) {
@@ -113,12 +79,15 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
     float4* hp = p.probe_hidden ? reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d) : nullptr;
     if (SRC == kSrcCombine) {
       const float4* yr = reinterpret_cast<const float4*>(p.y + (size_t)t * kS * d);
+      const float4* yrs[kPass];
+#pragma unroll
+      for (int j = 0; j < kPass; ++j) yrs[j] = yr;
       for (int c0 = tid; c0 < nc; c0 += kPass * kRouteThreads) {
         float4 acc[kPass];
         int cj[kPass];
 #pragma unroll
         for (int j = 0; j < kPass; ++j) cj[j] = c0 + j * kRouteThreads;
-        sum_slots<kPass>(yr, nc, kS, cj, acc);
+        sum_slots<kPass>(yrs, nc, kS, cj, acc);
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
           const int c = c0 + j * kRouteThreads;
@@ -128,7 +97,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
             hx[c] = v;
             hg[c] = v;
             if (hp) hp[c] = v;
-            ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            ss[tt] += sumsq4(v);
           }
         }
       }
@@ -138,7 +107,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
         const float4 v = __ldcg(hg + c);
         hx[c] = v;
         if (hp) hp[c] = v;
-        ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        ss[tt] += sumsq4(v);
       }
     } else {
       const uint2* src;
@@ -164,7 +133,7 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
         hx[c] = v;
         hg[c] = v;
         if (hp) hp[c] = v;
-        ss[tt] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        ss[tt] += sumsq4(v);
       }
     }
   }
@@ -181,94 +150,12 @@ __device__ void block_norm(const RouteParams& p, int t0, int ntok, float* xs, co
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kRouteWarps; ++w) tot += red[w * 8 + tt];
-    const float r = rsqrtf(tot / (float)d + p.eps);
+    const float r = norm_scale(tot, d, p.eps);
     for (int c = tid; c < nc; c += kRouteThreads) {
       const float4 v = reinterpret_cast<const float4*>(xs + tt * d)[c];
       const float4 g = reinterpret_cast<const float4*>(gs)[c];
-      __nv_bfloat162 lo = __halves2bfloat162(__float2bfloat16_rn(v.x * r * g.x),
-                                             __float2bfloat16_rn(v.y * r * g.y));
-      __nv_bfloat162 hi = __halves2bfloat162(__float2bfloat16_rn(v.z * r * g.z),
-                                             __float2bfloat16_rn(v.w * r * g.w));
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(xb + tt * xpitch)[c] = packed;
+      reinterpret_cast<uint2*>(xb + tt * xpitch)[c] = norm_pack(v, r, g);
     }
-  }
-}
-
-// Router-logit partition over the warps: 16-expert tiles x K splits.
-__host__ __device__ inline int route_ksplit(int E) {
-  const int n_mt = (E + 15) / 16;
-  return n_mt >= kRouteWarps ? 1 : kRouteWarps / n_mt;
-}
-
-// Shared-memory bytes of the staged router weights: d/64 panels of E rows x
-// 128 bytes (64 bf16), 128-byte swizzled, each panel 1024-byte aligned.
-__host__ __device__ inline size_t route_wr_panel(int E) { return (size_t)((E + 7) / 8) * 1024; }
-
-// Softmax over the E router logits z of token t and its top-k selection, one
-// warp; lane l holds experts l, l + 32, ... (PER of them, E <= 32 * PER).
-// Writes the token's k routed expert rows into rows[] and the row metadata
-// of all k + S.
-template <int PER>
-__device__ __forceinline__ void select_experts(const RouteParams& p, const float* z, int t,
-                                               int* rows) {
-  const int lane = threadIdx.x & 31, E = p.E, k = p.k, S = p.S;
-  float ze[PER];
-  int rank[PER];
-  float m = -FLT_MAX;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = lane + 32 * j;
-    ze[j] = e < E ? z[e] : -FLT_MAX;
-    m = fmaxf(m, ze[j]);
-    rank[j] = 0;
-  }
-  m = warp_max(m);
-  float sum = 0.f;
-#pragma unroll
-  for (int j = 0; j < PER; ++j)
-    if (lane + 32 * j < E) sum += __expf(ze[j] - m);
-  sum = warp_sum(sum);
-#pragma unroll 4
-  for (int f = 0; f < E; ++f) {
-    const float zf = z[f];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane + 32 * j;
-      rank[j] += (zf > ze[j] || (zf == ze[j] && f < e)) ? 1 : 0;
-    }
-  }
-  int slot[PER];
-#pragma unroll
-  for (int j = 0; j < PER; ++j)
-    slot[j] = (lane + 32 * j < E && rank[j] < k) ? atomicAdd(p.cnt + lane + 32 * j, 1) : 0;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = lane + 32 * j;
-    if (e < E && rank[j] < k) {
-      const float w = __expf(ze[j] - m) / sum;
-      int sl = slot[j];
-      if (sl >= p.T) {  // only reachable if the counters were not cleared
-        atomicOr(p.status, kErrInternal);
-        sl = p.T - 1;
-      }
-      const int row = e * p.T + sl;
-      rows[rank[j]] = row;
-      p.perm_token[row] = t;
-      p.perm_slot[row] = rank[j];
-      p.perm_w[row] = w;
-      if (p.probe_idx) p.probe_idx[(size_t)t * k + rank[j]] = e;
-      if (p.probe_w) p.probe_w[(size_t)t * k + rank[j]] = w;
-    }
-  }
-  // shared experts: their rows were copied right after the RMSNorm
-  for (int s = lane; s < S; s += 32) {
-    const int row = (E + s) * p.T + t;
-    p.perm_token[row] = t;
-    p.perm_slot[row] = k + s;
-    p.perm_w[row] = 1.0f;
   }
 }
 
@@ -288,15 +175,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   // normalised bf16 rows are padded by 16 bytes so that the B-fragment loads
   // of the 8 token rows fall in distinct shared-memory banks
   const int pitch = d + 8;
-  // shared memory: [router weights, when staged] [gain d fp32] [xs TPB x d fp32]
-  // [xb TPB x pitch bf16] [partial logits ksplit x 16n_mt x 8] [zs TPB x E]
-  // [red 64] [rows TPB x (k+S)]
+  // shared memory: [router weights, when staged] [gain d fp32] [xs TPB x d
+  // fp32, several tokens per block only] [xb TPB x pitch bf16] [partial
+  // logits ksplit x 16n_mt x 8] [zs TPB x E] [red 128] [rows TPB x (k+S)]
   const size_t panel = route_wr_panel(E);
   const size_t wr_bytes = WR ? (size_t)(d / 64) * panel : 0;
   uint8_t* wr_s = rsm;
   float* gs = reinterpret_cast<float*>(rsm + wr_bytes);
   float* xs = gs + d;
-  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + TPB * d);
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + (TPB > 1 ? TPB * d : 0));
   float* part = reinterpret_cast<float*>(xb + TPB * pitch);
   float* zs = part + ksplit * n_mt * 16 * 8;
   float* red = zs + TPB * E;
@@ -305,16 +192,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __shared__ int abort_flag;
 
   // Before waiting for the previous kernel: the gain and the router weights
-  // (static), and for the combine source the tokens' h rows, which the
-  // routing kernel two launches back wrote (a kernel lets its dependents start
-  // only after its own wait, so that kernel is complete here).
+  // (static), and for the combine source with several tokens per block the
+  // tokens' h rows, which the routing kernel two launches back wrote (a
+  // kernel lets its dependents start only after its own wait, so that kernel
+  // is complete here).
   if (tid == 0) {
     if (p.stamps) stamp_min(p.stamps);
     abort_flag = 0;
     mbar_init(&hx_bar, 1);
     mbar_init(&wr_bar, 1);
     fence_mbar_init();
-    const size_t h_bytes = (SRC == kSrcCombine) ? (size_t)ntok * d * 4 : 0;
+    const size_t h_bytes = (SRC == kSrcCombine && TPB > 1) ? (size_t)ntok * d * 4 : 0;
     mbar_arrive_expect_tx(&hx_bar, (uint32_t)((size_t)d * 4 + h_bytes));
     bulk_copy(gs, p.gain, (size_t)d * 4, &hx_bar);
     if (h_bytes) bulk_copy(xs, p.h + (size_t)t0 * d, h_bytes, &hx_bar);
@@ -340,8 +228,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int e = tid; e < E; e += kRouteThreads) p.cnt_other[e] = 0;
     if (tid == 0) *p.next_item_clear = 0;
   }
-  bool ok = mbar_wait(&hx_bar, 0, &abort_flag, p.status);
-  if (ok) block_norm<SRC, TPB>(p, t0, ntok, xs, gs, xb, pitch, red);
+  mbar_wait(&hx_bar, 0, &abort_flag, p.status);
+  __syncthreads();
+  bool ok = !abort_flag;  // the same for every thread (the norm has barriers)
+  if (ok) {
+    if constexpr (TPB == 1)
+      rs::norm_token<SRC, kRouteWarps>(p, t0, gs, xb, red);
+    else
+      block_norm<SRC, TPB>(p, t0, ntok, xs, gs, xb, pitch, red);
+  }
   __syncthreads();
   const int cpr = d / 8;  // 16-byte chunks per row
   if (ok) {
@@ -356,91 +251,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   if (WR && ok) ok = mbar_wait(&wr_bar, 0, &abort_flag, p.status);
 
-  // Router logits on the tensor cores: z^T = W_r xhat^T as 16x8x16 tiles,
-  // rows = experts, columns = the block's tokens (columns >= ntok are not
-  // used), fp32 accumulation.  Warp unit u covers expert tile u % n_mt and
-  // the u / n_mt-th share of the 64-column panels; a panel is four MMA steps
-  // on two alternating accumulators, and the next panel's fragments load
-  // while the current panel's MMAs issue.  The partial sums are added in
-  // K-split order.
-  if (ok) {
-    const int npan = d / 64;
-    const int pper = (npan + ksplit - 1) / ksplit;
-    const int g = lane >> 2, t4 = lane & 3;
-    const __nv_bfloat16* xrow = xb + (size_t)min(g, TPB - 1) * pitch + 2 * t4;
-    for (int u = warp; u < n_mt * ksplit; u += kRouteWarps) {
-      const int m0 = (u % n_mt) * 16, ks = u / n_mt;
-      const int pb = ks * pper, pe = min(npan, pb + pper);
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      // WR: this lane's ldmatrix row ar and the byte offsets of its four
-      // 16-byte chunks in a panel (chunk c of row r sits at r * 128 +
-      // ((c ^ (r % 8)) * 16)); otherwise the rows of its direct loads
-      const int mi = lane >> 3;
-      const int ar = min(m0 + (lane & 7) + (mi & 1) * 8, E - 1);
-      uint32_t off[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        off[j] = (uint32_t)ar * 128u + ((uint32_t)(((j << 1) | (mi >> 1)) ^ (ar & 7)) << 4);
-      const __nv_bfloat16* r0 = p.Wr + (size_t)min(m0 + g, E - 1) * d + 2 * t4;
-      const __nv_bfloat16* r1 = p.Wr + (size_t)min(m0 + g + 8, E - 1) * d + 2 * t4;
-      auto load_panel = [&](int pn, uint32_t(&a)[4][4], uint32_t(&b)[4][2]) {
-        const uint8_t* pbase = wr_s + (size_t)pn * panel;
-        const __nv_bfloat16* xp = xrow + pn * 64;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (WR) {
-            ldmatrix_x4(a[j], pbase + off[j]);
-          } else {
-            const int k0 = pn * 64 + j * 16;
-            a[j][0] = __ldg(reinterpret_cast<const uint32_t*>(r0 + k0));
-            a[j][1] = __ldg(reinterpret_cast<const uint32_t*>(r1 + k0));
-            a[j][2] = __ldg(reinterpret_cast<const uint32_t*>(r0 + k0 + 8));
-            a[j][3] = __ldg(reinterpret_cast<const uint32_t*>(r1 + k0 + 8));
-          }
-          b[j][0] = *reinterpret_cast<const uint32_t*>(xp + j * 16);
-          b[j][1] = *reinterpret_cast<const uint32_t*>(xp + j * 16 + 8);
-        }
-      };
-      auto mma_panel = [&](const uint32_t(&a)[4][4], const uint32_t(&b)[4][2]) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_16816_bf16(acc[j & 1], a[j], b[j][0], b[j][1]);
-      };
-      uint32_t fa[2][4][4], fb[2][4][2];
-      if (pb < pe) load_panel(pb, fa[0], fb[0]);
-      for (int pn = pb; pn < pe; pn += 2) {
-        if (pn + 1 < pe) load_panel(pn + 1, fa[1], fb[1]);
-        mma_panel(fa[0], fb[0]);
-        if (pn + 2 < pe) load_panel(pn + 2, fa[0], fb[0]);
-        if (pn + 1 < pe) mma_panel(fa[1], fb[1]);
-      }
-      float* pt = part + ((size_t)ks * n_mt * 16 + m0) * 8;
-      pt[g * 8 + 2 * t4] = acc[0][0] + acc[1][0];
-      pt[g * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1];
-      pt[(g + 8) * 8 + 2 * t4] = acc[0][2] + acc[1][2];
-      pt[(g + 8) * 8 + 2 * t4 + 1] = acc[0][3] + acc[1][3];
-    }
-  }
-  __syncthreads();
-  if (ok) {
-    for (int i = tid; i < ntok * E; i += kRouteThreads) {
-      const int tt = i / E, e = i - tt * E;
-      float z = part[e * 8 + tt];
-      for (int ks = 1; ks < ksplit; ++ks) z += part[((size_t)ks * n_mt * 16 + e) * 8 + tt];
-      zs[tt * E + e] = z + (p.bias ? __ldg(p.bias + e) : 0.f);
-    }
-  }
-  __syncthreads();
-
-  // softmax and top-k, one warp per token.  Rank of expert e = number of
-  // experts ordered before it by (z desc, index asc); the experts of rank < k
-  // are the selection, in rank order.  Each selected expert's row is claimed
-  // with its counter (all claims of a lane issued together); shared experts
-  // take the token's own row.
+  // router logits of the block's tokens (tensor cores), then softmax and
+  // top-k, one warp per token
+  rs::router_logits<TPB, WR>(p, wr_s, xb, pitch, part, zs, ntok, kRouteWarps, ok);
   if (warp < ntok && ok) {
     if (E <= 64)
-      select_experts<2>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
+      rs::select_experts<2>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
     else
-      select_experts<8>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
+      rs::select_experts<8>(p, zs + warp * E, t0 + warp, rows + warp * (k + S));
   }
   __syncthreads();
 
@@ -472,7 +290,10 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
   pdl_launch_dependents();
   if (blockIdx.x == 0) {
     for (int e = threadIdx.x; e < p.n_cnt_clear; e += 256) p.cnt_clear[e] = 0;
-    if (threadIdx.x == 0) *p.item_clear = 0;
+    if (threadIdx.x == 0) {
+      *p.item_clear = 0;
+      if (p.route_done_clear) *p.route_done_clear = 0;
+    }
   }
   __shared__ float red[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -485,7 +306,8 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
     float4 v = reinterpret_cast<const float4*>(hrow)[c];
     float4 acc[1];
     const int cj[1] = {c};
-    sum_slots<1>(yr, nc, p.kS, cj, acc);
+    const float4* yrs[1] = {yr};
+    sum_slots<1>(yrs, nc, p.kS, cj, acc);
     v.x += acc[0].x; v.y += acc[0].y; v.z += acc[0].z; v.w += acc[0].w;
     reinterpret_cast<float4*>(hrow)[c] = v;
     if (p.probe_hidden) reinterpret_cast<float4*>(p.probe_hidden + (size_t)t * d)[c] = v;
@@ -561,7 +383,7 @@ size_t route_smem_bytes(int tpb, int d, int E, int k, int S, bool wr_smem) {
   const size_t pitch = (size_t)d + 8;
   const size_t part = (size_t)route_ksplit(E) * ((E + 15) / 16) * 16 * 8;
   return 1024 /* alignment slack */ + (wr_smem ? (size_t)(d / 64) * route_wr_panel(E) : 0) +
-         (size_t)d * 4 + (size_t)tpb * d * 4 +
+         (size_t)d * 4 + (tpb > 1 ? (size_t)tpb * d * 4 : 0) +
          (size_t)tpb * pitch * 2 + (part + (size_t)tpb * E + kRouteWarps * 8) * sizeof(float) +
          (size_t)tpb * (k + S) * sizeof(int);
 }

@@ -288,21 +288,25 @@ def test_full_step_same_bits_on_any_grid(full):
         ctx.set_grid(8 * sms + 1)
 
 
-def test_full_step_launch_stamps(full):
+# B = 1 with the layer kernel: routing and expert items in one launch per layer
+@pytest.mark.parametrize("Bn,fused", [(32, False), (1, False), (1, True)])
+def test_full_step_launch_stamps(full, Bn, fused):
     """Launch timestamps of a graph-replayed step: each launch starts before
     it ends, and its wait for the preceding launch returns only after that
-    launch's last CTA has ended (the dependency the launch chain relies on).
-    Targets are unchanged by the stamps."""
+    launch's last CTA has ended (the dependency the launch chain relies on;
+    in the single-kernel layer, the expert items start only after the layer's
+    routing tasks have ended).  Targets are unchanged by the stamps."""
     ctx, _ = full
     L = S.FULL.n_layers
-    ids = S.uniform_ids(32 * 4, 89, 1, S.FULL.vocab).reshape(32, 4)
+    ids = S.uniform_ids(Bn * 4, 89, 1, S.FULL.vocab).reshape(Bn, 4)
     ctxi, dr = _i32(ids[:, 0]), _i32(ids[:, 1:])
     want = ctx.step(ctxi, dr).clone()
     stamps = torch.zeros((2 * L + 1, 4), dtype=torch.int64, device="cuda")
     init = torch.zeros_like(stamps)
     init[:, 0] = -1  # all bits set: UINT64_MAX as the library reads it
-    tg = torch.empty((32, 4), dtype=torch.int32, device="cuda")
+    tg = torch.empty((Bn, 4), dtype=torch.int32, device="cuda")
     ctx.set_stamps(stamps)
+    ctx.set_layer_kernel(8 if fused else 0)
     try:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -311,6 +315,7 @@ def test_full_step_launch_stamps(full):
             ctx.step(ctxi, dr, target_ids=tg, stream=s)
     finally:
         ctx.set_stamps(None)
+        ctx.set_layer_kernel(0)
     for _ in range(2):
         stamps.copy_(init)
         g.replay()
