@@ -371,7 +371,7 @@ MOE_VERIFY_API int moe_verify_set_grid(moe_verify_ctx* ctx, int32_t ctas);
  * running CTA, and gives up after 2 s like the others (timeout status).
  * 0 <= max_tokens <= 8; 0, the initial value, turns it off (a routing
  * launch and an expert-FFN launch per layer): on one GB300 the two launches
- * are faster (0.545 against 0.61 ms for the 12-layer step at B = 1, K = 3).  It applies where the router
+ * are faster (0.548 against 0.577 ms for the 12-layer step at B = 1, K = 3).  It applies where the router
  * weights (E x d bf16) fit in the kernel's shared-memory ring and d <= 2048;
  * moe_verify_layer, moe_verify_draft and moe_verify_step_attn always run the
  * two launches.  Host-buffer decode graphs already captured keep the setting

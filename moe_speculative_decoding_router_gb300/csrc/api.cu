@@ -37,8 +37,10 @@ struct moe_verify_ctx {
           *dep = nullptr;
   float* perm_w = nullptr;
   unsigned int *done_ffn = nullptr, *done_lm = nullptr;
-  // the single-kernel layer: routed tokens [2] and finished CTAs [2] by parity
+  // the single-kernel layer: routed tokens [2] by parity, and each layer's
+  // ticket counter [L] (cleared by the step's final kernel)
   int32_t* route_ctr = nullptr;
+  int32_t* layer_items = nullptr;
   unsigned long long* keys = nullptr;
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
@@ -58,10 +60,9 @@ struct moe_verify_ctx {
   int grid_ctas = 0;
   // steps of at most this many verify tokens route inside the expert-FFN
   // kernel (one launch per layer); 0: off.  Off by default: measured on the
-  // 12-layer step at B = 1, K = 3, 0.61 ms per step against 0.545 ms with a
-  // routing launch per layer (the routing's stages run ~1.7x slower in the
-  // expert FFN's 6-warp CTAs than in the 16-warp routing blocks, more than
-  // the launch handoff it saves)
+  // 12-layer step at B = 1, K = 3, 0.577 ms per step against 0.548 ms with a
+  // routing launch per layer (its routing tasks and expert phase each take
+  // ~1.5 us longer than in the two launches, more than the handoff it saves)
   int fuse_max_T = 0;
   int lm_pair_max = 0;  // lm_head CTA pairs that fit on the GPU at once
   // the stack with attention (moe_verify_init_attn)
@@ -517,7 +518,9 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
     fp.rt = rp;
     fp.route_done = c->route_ctr + parity;
     fp.route_done_clear = c->route_ctr + (1 - parity);
-    fp.exit_ctr = c->route_ctr + 2 + parity;
+    // the layer's own ticket counter: the launch claims on it from its first
+    // instruction, and nothing else uses it before the final kernel clears it
+    fp.next_item = c->layer_items + l;
   }
   if (sh.tokm) {
     fp.spec = 0;
@@ -650,6 +653,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   AL(c->done_ffn, 16);
   AL(c->done_lm, 16);
   AL(c->route_ctr, 16);
+  AL(c->layer_items, (size_t)c->L * 4);
   AL(c->keys, z.keys);
   AL(c->status, 16);
   AL(c->io_ctx, z.io);
@@ -668,6 +672,7 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   CKF(cudaMemsetAsync(c->done_ffn, 0, 16, s));
   CKF(cudaMemsetAsync(c->done_lm, 0, 16, s));
   CKF(cudaMemsetAsync(c->route_ctr, 0, 16, s));
+  CKF(cudaMemsetAsync(c->layer_items, 0, (size_t)c->L * 4, s));
   CKF(cudaMemsetAsync(c->status, 0, 16, s));
   CKF(cudaMemsetAsync(c->bias, 0, z.bias, s));
 
@@ -739,6 +744,8 @@ static int enqueue_head(moe_verify_ctx* ctx, int T, const StepShape& sh, int las
   fp.n_cnt_clear = ctx->E;
   fp.item_clear = item_counter(ctx, last_parity);
   fp.route_done_clear = ctx->route_ctr + last_parity;
+  fp.layer_items_clear = ctx->layer_items;
+  fp.n_layer_items = ctx->L;
   {
     Timed tm(ctx, 3, s);
     CK(mv::launch_final(fp, s, pdl));

@@ -48,6 +48,9 @@ namespace mv {
 namespace {
 
 constexpr int kGemmThreads = 192;
+// The single-kernel layer's CTAs: 16 warps, for its routing tasks (the
+// routing kernel's block size); warps 6.. take no expert-FFN role.
+constexpr int kLayerThreads = 512;
 constexpr int kStageA = 128 * 128;  // 128 weight rows x 64 bf16
 constexpr int kXbufBytes = 2 * 16 * 64 * 4;
 constexpr int kCtrlBytes = 1024;
@@ -361,7 +364,7 @@ __host__ __device__ inline size_t route_task_bytes(int d, int E, int k, int S) {
 // returns its first expert item.
 template <int SRC>
 __device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring, int first) {
-  constexpr int NW = kGemmThreads / 32;
+  constexpr int NW = kLayerThreads / 32;
   const RouteParams& rt = p.rt;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int d = rt.d, E = rt.E, k = rt.k, S = rt.S;
@@ -378,8 +381,8 @@ __device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring,
   pdl_launch_dependents();
   if (tid == 0 && rt.stamps) stamp_max(rt.stamps + 1);
   if (first == -p.n_route) {
-    for (int i = tid; i < rt.n_dep_clear; i += kGemmThreads) rt.dep_clear[i] = 0;
-    for (int e = tid; e < E; e += kGemmThreads) rt.cnt_other[e] = 0;
+    for (int i = tid; i < rt.n_dep_clear; i += kLayerThreads) rt.dep_clear[i] = 0;
+    for (int e = tid; e < E; e += kLayerThreads) rt.cnt_other[e] = 0;
     if (tid == 0) *p.route_done_clear = 0;
   }
   mbar_wait(C.rbar, 0, C.abort_flag, rt.status);
@@ -387,11 +390,11 @@ __device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring,
   const bool ok = !*C.abort_flag;  // the same for every thread (barriers below)
   while (first < 0) {
     const int t = first + p.n_route;
-    for (int i = tid; i < k + S; i += kGemmThreads) rows[i] = -1;
+    for (int i = tid; i < k + S; i += kLayerThreads) rows[i] = -1;
     if (ok) rs::norm_token<SRC, NW, 16>(rt, t, gs, xb, red);  // d <= 2048
     __syncthreads();
     if (ok)
-      for (int i = tid; i < S * cpr; i += kGemmThreads) {
+      for (int i = tid; i < S * cpr; i += kLayerThreads) {
         const int sx = i / cpr, c = i - sx * cpr;
         reinterpret_cast<uint4*>(rt.xperm + ((size_t)(E + sx) * rt.T + t) * d)[c] =
             reinterpret_cast<const uint4*>(xb)[c];
@@ -405,7 +408,7 @@ __device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring,
     }
     __syncthreads();
     if (ok)
-      for (int i = tid; i < k * cpr; i += kGemmThreads) {
+      for (int i = tid; i < k * cpr; i += kLayerThreads) {
         const int q = i / cpr, c = i - q * cpr;
         const int row = rows[q];
         if (row >= 0)
@@ -432,7 +435,7 @@ __device__ int ffn_route_tasks(const FfnParams& p, const Ctrl& C, uint8_t* ring,
 // kRoute: the single-kernel layer (FfnParams::n_route tokens routed here
 // first, with the router map map_wr); otherwise map_wr is not read.
 template <bool kRoute>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kRoute ? kLayerThreads : kGemmThreads, 1)
     ffn_kernel(const __grid_constant__ CUtensorMap map_gu, const __grid_constant__ CUtensorMap map_x,
                const __grid_constant__ CUtensorMap map_dn, const __grid_constant__ CUtensorMap map_a,
                const __grid_constant__ CUtensorMap map_pf, const __grid_constant__ CUtensorMap map_wr,
@@ -691,7 +694,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       mma_drain(C);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------ epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -785,16 +788,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
   }
   if (threadIdx.x == 0 && p.stamps) stamp_max(p.stamps + 2);
-  // the counters this launch used are cleared by the next routing kernel
-  // (the single-kernel layer: its ticket counter by its last CTA to finish;
-  // the next launch claiming on it starts after this one is complete)
-  if (kRoute && threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1) {
-      *p.next_item = 0;
-      *p.exit_ctr = 0;
-    }
-  }
+  // the counters this launch used are cleared by the next routing kernel (the
+  // single-kernel layer: its layer's own ticket counter, by the step's final
+  // kernel)
 }
 
 // End of an lm_head launch: the last CTA to finish turns the argmax keys into
@@ -2030,13 +2026,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <typename Kern, typename... Args>
-cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, bool pdl,
-                           Args... args) {
+cudaError_t launch_gemm_threads(Kern kern, int grid, int threads, size_t smem, cudaStream_t s,
+                                bool pdl, Args... args) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -2045,6 +2041,12 @@ cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, boo
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_gemm_ex(Kern kern, int grid, size_t smem, cudaStream_t s, bool pdl,
+                           Args... args) {
+  return launch_gemm_threads(kern, grid, kGemmThreads, smem, s, pdl, args...);
 }
 
 }  // namespace
@@ -2066,8 +2068,9 @@ cudaError_t launch_ffn(const CUtensorMap& map_gu, const CUtensorMap& map_x,
                        const CUtensorMap& map_pf, const CUtensorMap& map_wr, const FfnParams& p,
                        int grid, cudaStream_t s, bool pdl) {
   if (p.n_route > 0)
-    return launch_gemm_ex(ffn_kernel<true>, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl,
-                          map_gu, map_x, map_dn, map_a, map_pf, map_wr, p);
+    return launch_gemm_threads(ffn_kernel<true>, grid, kLayerThreads,
+                               gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu, map_x, map_dn,
+                               map_a, map_pf, map_wr, p);
   return launch_gemm_ex(ffn_kernel<false>, grid, gemm_smem_bytes(p.nch, p.stages), s, pdl, map_gu,
                         map_x, map_dn, map_a, map_pf, map_wr, p);
 }

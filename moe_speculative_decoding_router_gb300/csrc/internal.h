@@ -101,15 +101,14 @@ struct FfnParams {
   unsigned long long* stamps;  // nullptr, or this launch's [start, ready, end] timer slots
   // The single-kernel layer (a few verify tokens): n_route > 0 makes the
   // first n_route tickets route one token each (rt, with rt.stamps the
-  // routing's timer slots) before any expert item runs; route_done counts the
-  // tokens routed (zero on entry; the first routing task clears
-  // route_done_clear, the other parity's), exit_ctr the CTAs that have
-  // finished (the last one resets it and next_item).
+  // routing's timer slots) before any expert item runs; next_item is then the
+  // layer's own ticket counter (cleared by the step's final kernel), and
+  // route_done counts the tokens routed (zero on entry; the first routing
+  // task clears route_done_clear, the other parity's).
   int n_route;
   RouteParams rt;
   int32_t* route_done;
   int32_t* route_done_clear;
-  int32_t* exit_ctr;
 };
 
 struct FinalParams {
@@ -126,6 +125,8 @@ struct FinalParams {
   int n_cnt_clear;
   int32_t* item_clear;         // item counter of the last layer's expert FFN, cleared
   int32_t* route_done_clear;   // routed-token counter of the last layer, cleared (or nullptr)
+  int32_t* layer_items_clear;  // [n_layer_items] the single-kernel layers' ticket counters, cleared
+  int n_layer_items;
 };
 
 // The lm_head GEMM with its argmax epilogue.

@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(256) final_kernel(FinalParams p) {
       *p.item_clear = 0;
       if (p.route_done_clear) *p.route_done_clear = 0;
     }
+    for (int i = threadIdx.x; i < p.n_layer_items; i += 256) p.layer_items_clear[i] = 0;
   }
   __shared__ float red[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
