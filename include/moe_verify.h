@@ -163,17 +163,19 @@ MOE_VERIFY_API int moe_verify_accept(moe_verify_ctx* ctx, const int32_t* draft_i
 MOE_VERIFY_API int moe_verify_layer(moe_verify_ctx* ctx, int32_t layer, const void* h_in, int32_t T, void* h_out,
                      const moe_verify_probe* probe, void* cuda_stream);
 
-/* Convenience form of one decode iteration on HOST buffers: copies
- * context_ids [B] and draft_ids [B, K] from host memory (pinned memory makes
- * the copies asynchronous), runs moe_verify_step and moe_verify_accept on
- * cuda_stream, copies committed [B, K+1] and accept_len [B] back to host
- * memory, and waits for the stream (the targets stay in a context-owned
- * device buffer).  1 <= B <= max_batch, 0 <= K <= max_k.  Not capturable.
- * The first call for a given (B, K) captures the device part (step + accept
- * on the context's own buffers) into a CUDA graph on a library-owned stream;
- * later calls with that shape launch the graph on cuda_stream (up to 16
- * shapes are kept; others, and calls while per-launch timing is on, enqueue
- * the kernels directly).  Calls on one context must not run concurrently. */
+/* Convenience form of one decode iteration on HOST buffers: packs
+ * context_ids [B] and draft_ids [B, K] (any host memory) into a
+ * context-owned pinned staging buffer, then on cuda_stream copies them to the
+ * device in one copy, runs moe_verify_step and moe_verify_accept, copies
+ * accept_len and committed back in one copy, waits for the stream, and
+ * unpacks committed [B, K+1] and accept_len [B] into the caller's buffers
+ * (the targets stay in a context-owned device buffer).  1 <= B <= max_batch,
+ * 0 <= K <= max_k.  Not capturable.  The first call for a given (B, K)
+ * captures the device part (both copies, step and accept on the context's
+ * own buffers) into a CUDA graph on a library-owned stream; later calls with
+ * that shape launch the graph on cuda_stream (up to 16 shapes are kept;
+ * others, and calls while per-launch timing is on, enqueue it directly).
+ * Calls on one context must not run concurrently. */
 MOE_VERIFY_API int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
                            const int32_t* host_draft_ids, int32_t B, int32_t K,
                            int32_t* host_committed, int32_t* host_accept_len,

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <new>
+#include <cstring>
 #include <vector>
 
 #include "moe_verify.h"
@@ -45,6 +46,11 @@ struct moe_verify_ctx {
   uint32_t* status = nullptr;
   int32_t *io_ctx = nullptr, *io_drafts = nullptr, *io_targets = nullptr, *io_committed = nullptr,
           *io_alen = nullptr;
+  // host-buffer decode: ids in [B + B K] and accept_len + committed out
+  // [B + B (K + 1)], on the device and in a pinned host staging buffer
+  // (stage: T_max ints in, then T_max + max_batch out)
+  int32_t* io_out = nullptr;
+  int32_t* stage = nullptr;
   CUtensorMap map_gu, map_dn, map_lm, map_wr;
   // the expert weights with 256-row boxes (the token-major expert FFN)
   CUtensorMap map_gu256, map_dn256;
@@ -249,6 +255,8 @@ int encode_map_box(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
 void free_all(moe_verify_ctx* c) {
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
+  if (c->stage) cudaFreeHost(c->stage);
+  c->stage = nullptr;
   // timing pairs not yet read back by moe_verify_get_timing are outside the pool
   for (auto& tp : c->pending) {
     cudaEventDestroy(tp.a);
@@ -661,6 +669,12 @@ int moe_verify_init(const moe_verify_config* config, const moe_verify_weights* w
   AL(c->io_targets, z.io);
   AL(c->io_committed, z.io);
   AL(c->io_alen, z.io);
+  AL(c->io_out, z.io + (size_t)config->max_batch * 4);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->stage),
+                    2 * z.io + (size_t)config->max_batch * 4, cudaHostAllocDefault) != cudaSuccess) {
+    c->stage = nullptr;
+    return fail(MOE_VERIFY_ERR_OOM);
+  }
 
   // zero the workspace so that padding rows read by the MMAs are finite
   CKF(cudaMemsetAsync(c->y, 0, z.y, s));
@@ -863,11 +877,20 @@ namespace {
 
 // The device part of a host-buffer decode call: step + accept on the
 // context's own io buffers.
+// One host-buffer decode iteration on the device: the ids in from the pinned
+// stage (one copy: [B context ids][B K drafts]), step + accept, and
+// accept_len and committed out to the stage (one copy: [B][B (K + 1)]).
 int enqueue_decode(moe_verify_ctx* ctx, int B, int K, cudaStream_t s) {
-  int rc = enqueue_step(ctx, ctx->io_ctx, ctx->io_drafts, B, K, ctx->io_targets, nullptr, s);
+  const int32_t* stage_in = ctx->stage;
+  int32_t* stage_out = ctx->stage + ctx->T_max;
+  int32_t* drafts = ctx->io_ctx + B;
+  CK(cudaMemcpyAsync(ctx->io_ctx, stage_in, (size_t)B * (K + 1) * 4, cudaMemcpyHostToDevice, s));
+  int rc = enqueue_step(ctx, ctx->io_ctx, drafts, B, K, ctx->io_targets, nullptr, s);
   if (rc != MOE_VERIFY_OK) return rc;
-  return moe_verify_accept(ctx, ctx->io_drafts, ctx->io_targets, B, K, ctx->io_committed,
-                           ctx->io_alen, s);
+  rc = moe_verify_accept(ctx, drafts, ctx->io_targets, B, K, ctx->io_out + B, ctx->io_out, s);
+  if (rc != MOE_VERIFY_OK) return rc;
+  CK(cudaMemcpyAsync(stage_out, ctx->io_out, (size_t)B * (K + 2) * 4, cudaMemcpyDeviceToHost, s));
+  return MOE_VERIFY_OK;
 }
 
 // The captured graph of enqueue_decode for (B, K), built on first use
@@ -911,10 +934,9 @@ int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
   if (B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MOE_VERIFY_ERR_ARG;
   if (K > 0 && !host_draft_ids) return MOE_VERIFY_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  CK(cudaMemcpyAsync(ctx->io_ctx, host_context_ids, (size_t)B * 4, cudaMemcpyHostToDevice, s));
-  if (K > 0)
-    CK(cudaMemcpyAsync(ctx->io_drafts, host_draft_ids, (size_t)B * K * 4, cudaMemcpyHostToDevice,
-                       s));
+  // the previous call has synchronised: the stage is free
+  std::memcpy(ctx->stage, host_context_ids, (size_t)B * 4);
+  if (K > 0) std::memcpy(ctx->stage + B, host_draft_ids, (size_t)B * K * 4);
   cudaGraphExec_t exec = ctx->timing ? nullptr : decode_graph(ctx, B, K);
   if (exec) {
     CK(cudaGraphLaunch(exec, s));
@@ -922,10 +944,10 @@ int moe_verify_decode_host(moe_verify_ctx* ctx, const int32_t* host_context_ids,
     int rc = enqueue_decode(ctx, B, K, s);
     if (rc != MOE_VERIFY_OK) return rc;
   }
-  CK(cudaMemcpyAsync(host_committed, ctx->io_committed, (size_t)B * (K + 1) * 4,
-                     cudaMemcpyDeviceToHost, s));
-  CK(cudaMemcpyAsync(host_accept_len, ctx->io_alen, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
+  const int32_t* out = ctx->stage + ctx->T_max;
+  std::memcpy(host_accept_len, out, (size_t)B * 4);
+  std::memcpy(host_committed, out + B, (size_t)B * (K + 1) * 4);
   return MOE_VERIFY_OK;
 }
 
