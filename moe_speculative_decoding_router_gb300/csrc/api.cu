@@ -513,6 +513,13 @@ int run_layer(moe_verify_ctx* c, int l, int parity, int src, const StepShape& sh
       fp.pf_pair = 1;
       fp.pf_limit = 2 * lm_pairs(c);
     }
+  } else if (l + 1 < c->L && src == mv::kSrcH) {
+    // the stack with attention: the next layer starts with its q/k/v
+    // projection, whose 128-row tiles each CTA c < tiles pulls once
+    map_pf = &c->map_qkv;
+    fp.pf_base = (l + 1) * c->rows_qkv;
+    fp.pf_div = 1;
+    fp.pf_limit = c->rows_qkv / 128;
   } else if (l + 1 < c->L && src != mv::kSrcBf16 && fp.spec > 0) {
     fp.pf_items = 1;
     fp.pf_base = (l + 1) * c->nE * c->mt_gu * 128;

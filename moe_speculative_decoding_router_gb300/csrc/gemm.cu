@@ -1925,10 +1925,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int q = warp & 3;
       const int K1 = p.K + 1, half = p.hd >> 1;
       // The global inputs of 16 token columns, loaded ahead of use (the
-      // item's first 16 while its MMAs run, the next 16 while the current
-      // ones are stored).  MODE 0: each column's cache row (slot * H * max_pos
-      // + position; -1 for a column past the chunk or a sequence out of range)
-      // and this row's rotary (cos, sin); MODE 1: h[t, row].
+      // item's first 32 while its MMAs run, then each group two ahead of the
+      // one being stored).  MODE 0: each column's cache row (slot * H *
+      // max_pos + position; -1 for a column past the chunk or a sequence out
+      // of range) and this row's rotary (cos, sin); MODE 1: h[t, row].
       struct Cols {
         int crow[MODE == 0 ? 16 : 1];
         float2 cs[MODE == 0 ? 16 : 1];
@@ -1970,11 +1970,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const QkvRow r = qkv_row(p, prow);
         Cols cur, nxt;
         fetch(it, r, prow, 0, cur);
+        if (16 < npad) fetch(it, r, prow, 16, nxt);
         if (!mbar_wait(&C.tfull[buf], use & 1u, C.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.nch);
         for (int c0 = 0; c0 < npad; c0 += 16) {
-          if (c0 + 16 < npad) fetch(it, r, prow, c0 + 16, nxt);
+          Cols nn;
+          if (c0 + 32 < npad) fetch(it, r, prow, c0 + 32, nn);
           uint32_t v[16];
           tmem_ld16(tb + (uint32_t)c0, v);
           tmem_ld_wait();
@@ -2009,6 +2011,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     __float2bfloat16_rn(__uint_as_float(v[j]));
           }
           cur = nxt;
+          nxt = nn;
         }
         tc_fence_before();
         __syncwarp();
