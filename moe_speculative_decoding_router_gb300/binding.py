@@ -180,8 +180,7 @@ def _dev_i32(t, name: str = "ids", shape=None):
 
 
 def _host_i32(a, name: str, shape, writable: bool = False):
-    """a must be a C-contiguous int32 numpy array of `shape` (pinned memory
-    makes the library's copies asynchronous; pageable memory also works)."""
+    """a must be a C-contiguous int32 numpy array of `shape`."""
     if (not isinstance(a, np.ndarray) or a.dtype != np.int32 or not a.flags["C_CONTIGUOUS"]
             or a.shape != tuple(shape)):
         raise ValueError(f"{name}: a C-contiguous int32 array of shape {tuple(shape)} is expected")
@@ -410,7 +409,8 @@ class MoeVerify:
 
     def decode_host(self, context_ids: np.ndarray, draft_ids: Optional[np.ndarray],
                     committed: np.ndarray, accept_len: np.ndarray, stream=None):
-        """Host buffers in and out (pinned numpy views make the copies asynchronous)."""
+        """Host buffers in and out (any C-contiguous int32 arrays: the library
+        stages them through its own pinned buffer)."""
         if getattr(context_ids, "ndim", 0) != 1:
             raise ValueError("context_ids: a 1-D array [B] is expected")
         B = context_ids.shape[0]
