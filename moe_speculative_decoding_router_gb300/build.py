@@ -4,7 +4,7 @@
 
 Each CUDA translation unit compiles in parallel; the shared library links the
 CUDA runtime statically, so loading it needs no libcudart on the loader path
-(the driver is only opened on the first CUDA call).
+(the CUDA driver library is only opened on the first CUDA call).
 """
 from __future__ import annotations
 

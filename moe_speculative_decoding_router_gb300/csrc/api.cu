@@ -200,7 +200,7 @@ int dalloc(moe_verify_ctx* c, T** p, uint64_t bytes) {
   return MOE_VERIFY_OK;
 }
 
-// The driver's tensor-map encoder, looked up once (a function-local static's
+// The CUDA driver API's tensor-map encoder, looked up once (a function-local static's
 // initialisation is thread safe).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {

@@ -39,7 +39,7 @@ std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;  // guarded by g_setup_mu
 
-// Device address of g_scratch on the current device, and the driver's
+// Device address of g_scratch on the current device, and the CUDA driver API's
 // tensor-map encoder.  In host code the name g_scratch is only a host-side
 // stand-in, so the address is asked for once per device, with that device
 // current.
