@@ -78,8 +78,10 @@ def test_tiny_every_id_matches_oracle(tiny):
 
 
 # T = 68 and 96 reach the tokens-on-M lm_head with ragged chunks (65..128 tokens)
+# T = 260, 300, 400, 512: lm_head on CTA pairs (260 and 300: the last 256-token
+# chunk holds 4 and 44 tokens, so the odd CTA of its pairs holds none)
 @pytest.mark.parametrize("Bn,K", [(1, 0), (1, 3), (3, 1), (4, 3), (17, 3), (24, 3), (128, 0),
-                                  (77, 2), (100, 3), (128, 3)])  # T = 400, 512: lm_head on CTA pairs
+                                  (77, 2), (65, 3), (75, 3), (100, 3), (128, 3)])
 def test_tiny_batch_shapes(tiny, Bn, K):
     ctx, orc = tiny
     ids = S.uniform_ids(Bn * (K + 1), 41 + Bn, K, 512).reshape(Bn, K + 1)
