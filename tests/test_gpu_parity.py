@@ -770,3 +770,40 @@ def test_decode_iteration_in_one_graph(full, full_draft):
         assert torch.equal(out_d, ref[r][1]), r
         in_c.copy_(t)
         in_d.copy_(out_d)
+
+
+@pytest.fixture(scope="module")
+def full_two_layers():
+    """Two blocks of the full-width stack, room for 128 x 4 tokens."""
+    import dataclasses
+    B = _B()
+    cfg = dataclasses.replace(S.FULL, n_layers=2, name="full_two_layers")
+    ctx = B.MoeVerify(cfg, B.weights_to_device(S.make_weights(cfg)), max_batch=128, max_k=3)
+    torch.cuda.empty_cache()
+    yield ctx, cfg
+    ctx.close()
+
+
+def test_large_batch_same_bits_on_any_grid(full_two_layers):
+    """512 tokens (token-major expert FFN, lm_head on CTA pairs) on 1 CTA
+    (the lm_head falls back to single CTAs: no pair fits), 3 CTAs (one pair)
+    and twice as many as fit at once: targets and every block's residual
+    stream are the same bits as on one CTA per SM."""
+    ctx, cfg = full_two_layers
+    B = _B()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ids = S.uniform_ids(128 * 4, 91, 1, cfg.vocab).reshape(128, 4)
+    pa, ta = B.make_probe(cfg.n_layers, 512, cfg, topk=False)
+    want = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=pa).cpu().numpy()
+    hw = ta["hidden"].cpu().numpy()
+    assert ctx.sync_status() == B.OK
+    try:
+        for ctas in (3, 2 * sms, 1):
+            ctx.set_grid(ctas)
+            pb, tb = B.make_probe(cfg.n_layers, 512, cfg, topk=False)
+            got = ctx.step(_i32(ids[:, 0]), _i32(ids[:, 1:]), probe=pb).cpu().numpy()
+            assert ctx.sync_status() == B.OK, ctas
+            assert np.array_equal(got, want), ctas
+            assert np.array_equal(tb["hidden"].cpu().numpy(), hw), ctas
+    finally:
+        ctx.set_grid(0)
