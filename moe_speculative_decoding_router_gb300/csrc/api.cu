@@ -362,13 +362,10 @@ int shape_for(const moe_verify_ctx* c, int T, StepShape* out) {
     // the pair form needs at least one pair that fits; else the single-CTA form
     const int pairs = lm_pairs(c);
     if (pairs < 1) {
-      s.lm.pair = false;
-      s.lm.n_chunks = (T + 255) / 256;
-      s.lm.nch = round_up((T + s.lm.n_chunks - 1) / s.lm.n_chunks, 16);
-      s.lm.tmem_cols = pow2_at_least(2 * s.lm.nch);
-      s.lm.stages = mv::gemm_max_stages(s.lm.nch);
+      s.lm = mv::lm_layout_single(T);
       s.n_chunks_lm = s.lm.n_chunks;
       s.nch_lm = s.lm.nch;
+      s.tmem_cols = s.tokm ? 512 : pow2_at_least(2 * (s.nch > s.nch_lm ? s.nch : s.nch_lm));
       if (encode_map(&s.map_f, c->xf, c->d, round_up(c->T_max, 16), (uint32_t)s.nch_lm))
         return MOE_VERIFY_ERR_CUDA;
     } else if (encode_map(&s.map_f128, c->xf, c->d, round_up(c->T_max, 16), 128)) {

@@ -2114,18 +2114,23 @@ cudaError_t launch_proj(const CUtensorMap& map_w, const CUtensorMap& map_x, cons
 }
 
 LmLayout lm_layout(int T) {
+  if (T <= kLmPairMinT) return lm_layout_single(T);
+  LmLayout l;
+  l.tokens_on_m = false;
+  l.pair = true;
+  // chunks of 256 tokens, each CTA of a pair loading 128 of them
+  l.n_chunks = (T + 255) / 256;
+  l.nch = 128;
+  l.tmem_cols = 512;  // two accumulators of 256 token columns
+  l.stages = gemm_max_stages(l.nch);
+  if (l.stages > 16) l.stages = 16;
+  return l;
+}
+
+LmLayout lm_layout_single(int T) {
   LmLayout l;
   l.tokens_on_m = T > 64 && T <= 128;
-  l.pair = T > kLmPairMinT;
-  if (l.pair) {
-    // chunks of 256 tokens, each CTA of a pair loading 128 of them
-    l.n_chunks = (T + 255) / 256;
-    l.nch = 128;
-    l.tmem_cols = 512;  // two accumulators of 256 token columns
-    l.stages = gemm_max_stages(l.nch);
-    if (l.stages > 16) l.stages = 16;
-    return l;
-  }
+  l.pair = false;
   if (l.tokens_on_m) {
     l.n_chunks = 1;
     l.nch = (T + 15) / 16 * 16;

@@ -284,13 +284,18 @@ cudaError_t launch_ffn_tokm(const CUtensorMap& map_gu256, const CUtensorMap& map
 // The lm_head launch for T tokens: tokens on the MMA's M side for 65..128
 // tokens (one chunk); above kLmPairMinT tokens on CTA pairs (256 vocabulary
 // rows x chunks of 256 tokens, each CTA loading half of each); else
-// vocabulary rows on M with chunks of <= 256 tokens.
-constexpr int kLmPairMinT = 256;
+// vocabulary rows on M with chunks of <= 256 tokens.  Pairs measured faster
+// from 136 tokens on (136: 59.5 -> 57.4 us, 192: 67.4 -> 59.6 us, 256: 86.3
+// -> 60.6 us per launch).
+constexpr int kLmPairMinT = 128;
 struct LmLayout {
   bool tokens_on_m, pair;
   int nch, n_chunks, tmem_cols, stages;
 };
 LmLayout lm_layout(int T);
+// The single-CTA layout for T tokens (whatever T; the form lm_layout picks
+// for T <= kLmPairMinT, and the fallback when no CTA pair fits).
+LmLayout lm_layout_single(int T);
 // CTA pairs of the lm_head that fit on the GPU at once (0: none).
 int lmhead_pair_max_clusters(int stages);
 // map_x128: the final normalised rows with 128-row boxes; grid = 2 * pairs.

@@ -159,7 +159,7 @@ extern "C" MOE_VERIFY_API int moe_verify_greedy_head_noalloc(const float* h,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
   // a chunk's normalised rows arrive as one box of nch rows
-  const mv::LmLayout lay = mv::lm_layout(T);
+  const mv::LmLayout lay = mv::lm_layout_single(T);  // the single-CTA kernel below
   const int nch = lay.nch;
   CUtensorMap map_lm, map_xf;
   // rows past V (the last vocabulary tile) and past T are read as zeros
